@@ -1,0 +1,674 @@
+// api.cu -- the C ABI (include/tfl.h) and the runtime behind it: shape
+// validation, weight packing, workspace carve-up, TMA descriptors, the
+// per-forward launch sequence and its CUDA-graph capture.
+//
+// Launch sequence of one forward ("TikTok TechJam 2026 -- Problem 3",
+// sections 1.A and 1.B; 5 or 7 kernels per layer, replayed as one graph):
+//   [length check] [layer-0 input LayerNorm, no residual copy]
+//   per layer: QKV GEMM (+bias) -> flash attention -> o_proj GEMM (+bias
+//   +residual, LayerNorm fused when d_model = 128) -> FFN-in GEMM (+bias
+//   +GELU) -> FFN-out GEMM (+bias +residual, then LayerNorm of the next
+//   layer, or the model tail on the last layer).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/tfl.h"
+#include "kernels.h"
+
+using namespace tfl;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(TFL_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define TFL_CUDA(call, what)                         \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D fp16 map over a row-major [rows, cols] matrix, box {64, box_rows}, 128B swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D fp16 map over qkv [B, S, 3D]: box {atom_cols, box_rows, 1}.
+bool make_map_qkv(CUtensorMap* m, const void* base, uint64_t B, uint64_t S, uint64_t C3, uint32_t atom_cols,
+                  uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {C3, S, B};
+  cuuint64_t strides[2] = {C3 * 2, S * C3 * 2};
+  cuuint32_t box[3] = {atom_cols, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = atom_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct LayerDev {
+  __half *wqkv, *wo, *w1, *w2;
+  float *bqkv, *bo, *b1, *b2, *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+  CUtensorMap tm_wqkv, tm_wo, tm_w1, tm_w2;
+};
+
+struct GraphEntry {
+  int causal;
+  const void* x;
+  const void* len;
+  void* out;
+  cudaGraphExec_t exec;
+};
+
+struct WsLayout {
+  size_t h32, n16, qkv16, o16, g16, status, total;
+};
+
+WsLayout ws_layout(const tfl_shape& s) {
+  const size_t M = (size_t)s.B * s.S, D = s.d_model, F = s.d_ff;
+  WsLayout w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 1024);
+    return o;
+  };
+  w.h32 = take(M * D * 4);
+  w.n16 = take(M * D * 2);
+  w.qkv16 = take(M * 3 * D * 2);
+  w.o16 = take(M * D * 2);
+  w.g16 = take(M * F * 2);
+  w.status = take(256);
+  w.total = off;
+  return w;
+}
+
+int gemm_bn(int N) { return N % 256 == 0 ? 256 : 128; }
+
+}  // namespace
+
+struct tfl_handle {
+  tfl_shape shape{};
+  tfl_options opt{};
+  int device = 0, num_sms = 0;
+  int M = 0, D = 0, H = 0, hd = 0, F = 0, L = 0;
+  void* wmem = nullptr;
+  void* ws = nullptr;
+  WsLayout lay{};
+  std::vector<LayerDev> layers;
+  float *lnf_g = nullptr, *lnf_b = nullptr;
+  float* h32 = nullptr;
+  __half *n16 = nullptr, *qkv16 = nullptr, *o16 = nullptr, *g16 = nullptr;
+  int* status = nullptr;
+  CUtensorMap tm_n16{}, tm_o16{}, tm_g16{}, tm_q{}, tm_kv{};
+  std::vector<GraphEntry> graphs;
+  float *hx_dev = nullptr, *hout_dev = nullptr;
+  int* hlen_dev = nullptr;
+  cudaStream_t cap_stream = nullptr;  // graphs are captured here (the legacy stream cannot be captured)
+};
+
+namespace {
+
+int check_shape(const tfl_shape* s) {
+  if (!s) return fail(TFL_ERR_INVALID_ARG, "shape is NULL");
+  if (s->B < 1 || s->S < 1 || s->d_model < 1 || s->n_heads < 1 || s->d_ff < 1 || s->n_layers < 1)
+    return fail(TFL_ERR_INVALID_ARG, "every shape field must be >= 1");
+  if (s->norm_placement != 0 && s->norm_placement != 1)
+    return fail(TFL_ERR_INVALID_ARG, "norm_placement must be 0 (pre-LN) or 1 (post-LN)");
+  if (s->d_model % s->n_heads != 0) return fail(TFL_ERR_INVALID_ARG, "n_heads must divide d_model");
+  const int hd = s->d_model / s->n_heads;
+  if (s->d_model % 128 != 0 || !(s->d_model / 128 == 1 || s->d_model / 128 == 2 || s->d_model / 128 == 4 ||
+                                 s->d_model / 128 == 8))
+    return fail(TFL_ERR_UNSUPPORTED, "d_model must be 128, 256, 512 or 1024");
+  if (s->d_ff % 128 != 0) return fail(TFL_ERR_UNSUPPORTED, "d_ff must be a multiple of 128");
+  if (!(hd == 32 || hd == 64 || hd == 256)) return fail(TFL_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 256");
+  if ((int64_t)s->B * s->S >= (int64_t)1 << 31) return fail(TFL_ERR_UNSUPPORTED, "B*S must be < 2^31");
+  return TFL_OK;
+}
+
+// Copy a float32 tensor from host or device memory into a device scratch buffer.
+int stage_f32(const float* src, size_t n, float* tmp, const char* name) {
+  if (!src) return fail(TFL_ERR_INVALID_ARG, std::string("weight pointer ") + name + " is NULL");
+  TFL_CUDA(cudaMemcpy(tmp, src, n * sizeof(float), cudaMemcpyDefault), name);
+  return TFL_OK;
+}
+
+int pack_f16(const float* src, size_t n, float* tmp, __half* dst, const char* name) {
+  int rc = stage_f32(src, n, tmp, name);
+  if (rc) return rc;
+  TFL_CUDA(launch_f32_to_f16(tmp, dst, n, 0), name);
+  TFL_CUDA(cudaDeviceSynchronize(), name);
+  return TFL_OK;
+}
+
+int copy_f32(const float* src, size_t n, float* dst, const char* name) {
+  if (!src) return fail(TFL_ERR_INVALID_ARG, std::string("weight pointer ") + name + " is NULL");
+  TFL_CUDA(cudaMemcpy(dst, src, n * sizeof(float), cudaMemcpyDefault), name);
+  return TFL_OK;
+}
+
+struct Rec {
+  bool on = false;
+  std::vector<cudaEvent_t>* ev = nullptr;
+  std::vector<int>* kinds = nullptr;
+};
+
+cudaError_t rec_mark(const Rec& r, cudaStream_t s, int kind) {
+  if (!r.on) return cudaSuccess;
+  cudaEvent_t e;
+  cudaError_t err = cudaEventCreate(&e);
+  if (err != cudaSuccess) return err;
+  r.ev->push_back(e);
+  if (kind) r.kinds->push_back(kind);
+  return cudaEventRecord(e, s);
+}
+
+// Enqueue the whole forward on `st`.
+int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out, cudaStream_t st,
+            const Rec& rec) {
+  const bool pre = h->shape.norm_placement == 0;
+  Common c;
+  c.M = h->M;
+  c.S = h->shape.S;
+  c.lengths = lengths;
+  c.status = h->status;
+  c.timeout_ns = h->opt.wait_timeout_ns;
+  const float eps = h->opt.ln_eps;
+  const int D = h->D, F = h->F, L = h->L;
+
+  TFL_CUDA(launch_check_lengths(lengths, h->shape.B, h->shape.S, h->status, st), "length check launch");
+
+  TFL_CUDA(rec_mark(rec, st, 0), "event");
+  {
+    RowArgs ra;
+    ra.c = c;
+    ra.D = D;
+    ra.in32 = x;
+    ra.row.eps = eps;
+    ra.row.n16 = h->n16;
+    if (pre) {
+      ra.row.flags = ROW_NORM16;
+      ra.row.gb = h->layers[0].ln1_g;
+      ra.row.bb = h->layers[0].ln1_b;
+    } else {
+      ra.row.flags = ROW_CAST16;
+    }
+    TFL_CUDA(launch_rows(ra, st), "input row kernel launch");
+  }
+  TFL_CUDA(rec_mark(rec, st, TFL_KIND_ROWNORM), "event");
+
+  for (int l = 0; l < L; ++l) {
+    const LayerDev& ly = h->layers[l];
+    const bool last = l == L - 1;
+    // QKV projection
+    {
+      GemmArgs g;
+      g.c = c;
+      g.N = 3 * D;
+      g.K = D;
+      g.bias = ly.bqkv;
+      g.c16 = h->qkv16;
+      TFL_CUDA(launch_gemm(gemm_bn(3 * D), EPI_BIAS_F16, h->tm_n16, ly.tm_wqkv, g, h->num_sms, st), "qkv gemm");
+      TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_QKV), "event");
+    }
+    // attention
+    {
+      AttnArgs a;
+      a.c = c;
+      a.B = h->shape.B;
+      a.H = h->H;
+      a.D = D;
+      a.causal = causal;
+      a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->hd));
+      a.o16 = h->o16;
+      TFL_CUDA(launch_attention(h->hd, h->tm_q, h->tm_kv, a, h->num_sms, st), "attention");
+      TFL_CUDA(rec_mark(rec, st, TFL_KIND_ATTENTION), "event");
+    }
+    // o_proj + bias + residual (+ LayerNorm)
+    {
+      GemmArgs g;
+      g.c = c;
+      g.N = D;
+      g.K = D;
+      g.bias = ly.bo;
+      g.res = (l == 0) ? x : h->h32;
+      RowOps ro;
+      ro.eps = eps;
+      ro.h32 = h->h32;
+      ro.n16 = h->n16;
+      if (pre) {
+        ro.flags = ROW_NORM16;
+        ro.gb = ly.ln2_g;
+        ro.bb = ly.ln2_b;
+      } else {
+        ro.flags = ROW_POST_LN | ROW_WRITE_H | ROW_CAST16;
+        ro.ga = ly.ln1_g;
+        ro.ba = ly.ln1_b;
+      }
+      if (D == 128) {
+        ro.flags |= ROW_WRITE_H;
+        g.row = ro;
+        TFL_CUDA(launch_gemm(128, EPI_BIAS_RES_ROW, h->tm_o16, ly.tm_wo, g, h->num_sms, st), "o_proj gemm");
+        TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_OPROJ), "event");
+      } else {
+        g.h32 = h->h32;
+        TFL_CUDA(launch_gemm(gemm_bn(D), EPI_BIAS_RES_F32, h->tm_o16, ly.tm_wo, g, h->num_sms, st), "o_proj gemm");
+        TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_OPROJ), "event");
+        RowArgs ra;
+        ra.c = c;
+        ra.D = D;
+        ra.in32 = h->h32;
+        ra.row = ro;
+        TFL_CUDA(launch_rows(ra, st), "row kernel");
+        TFL_CUDA(rec_mark(rec, st, TFL_KIND_ROWNORM), "event");
+      }
+    }
+    // FFN-in + bias + GELU
+    {
+      GemmArgs g;
+      g.c = c;
+      g.N = F;
+      g.K = D;
+      g.bias = ly.b1;
+      g.c16 = h->g16;
+      TFL_CUDA(launch_gemm(gemm_bn(F), EPI_BIAS_GELU_F16, h->tm_n16, ly.tm_w1, g, h->num_sms, st), "ffn1 gemm");
+      TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN1), "event");
+    }
+    // FFN-out + bias + residual (+ next LayerNorm or the tail)
+    {
+      GemmArgs g;
+      g.c = c;
+      g.N = D;
+      g.K = F;
+      g.bias = ly.b2;
+      g.res = h->h32;
+      RowOps ro;
+      ro.eps = eps;
+      ro.h32 = h->h32;
+      ro.n16 = h->n16;
+      ro.out32 = out;
+      if (!pre) {
+        ro.flags |= ROW_POST_LN;
+        ro.ga = ly.ln2_g;
+        ro.ba = ly.ln2_b;
+      }
+      if (last) {
+        ro.flags |= ROW_FINAL;
+        ro.gf = h->lnf_g;
+        ro.bf = h->lnf_b;
+      } else if (pre) {
+        ro.flags |= ROW_NORM16;
+        ro.gb = h->layers[l + 1].ln1_g;
+        ro.bb = h->layers[l + 1].ln1_b;
+      } else {
+        ro.flags |= ROW_WRITE_H | ROW_CAST16;
+      }
+      if (D == 128) {
+        if (pre && !last) ro.flags |= ROW_WRITE_H;
+        g.row = ro;
+        TFL_CUDA(launch_gemm(128, EPI_BIAS_RES_ROW, h->tm_g16, ly.tm_w2, g, h->num_sms, st), "ffn2 gemm");
+        TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
+      } else {
+        g.h32 = h->h32;
+        TFL_CUDA(launch_gemm(gemm_bn(D), EPI_BIAS_RES_F32, h->tm_g16, ly.tm_w2, g, h->num_sms, st), "ffn2 gemm");
+        TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
+        RowArgs ra;
+        ra.c = c;
+        ra.D = D;
+        ra.in32 = h->h32;
+        ra.row = ro;
+        TFL_CUDA(launch_rows(ra, st), "row kernel");
+        TFL_CUDA(rec_mark(rec, st, TFL_KIND_ROWNORM), "event");
+      }
+    }
+  }
+  return TFL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tfl_default_options(tfl_options* o) {
+  if (!o) return fail(TFL_ERR_INVALID_ARG, "options is NULL");
+  o->precision = 0;
+  o->ln_eps = 1e-5f;
+  o->wait_timeout_ns = 2000000000LL;
+  o->max_workspace_bytes = 0;
+  o->use_graph = 1;
+  return TFL_OK;
+}
+
+size_t tfl_workspace_bytes(const tfl_shape* s) {
+  if (check_shape(s) != TFL_OK) return 0;
+  return ws_layout(*s).total;
+}
+
+const char* tfl_last_error(void) { return g_err.c_str(); }
+
+int tfl_launch_count(const tfl_handle* h, int causal) {
+  (void)causal;
+  if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  const int per_layer = h->D == 128 ? 5 : 7;
+  return 2 + per_layer * h->L;
+}
+
+int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* opt, tfl_handle** out) {
+  g_err.clear();
+  if (!out) return fail(TFL_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!w || !w->layers) return fail(TFL_ERR_INVALID_ARG, "weights are NULL");
+  if (w->n_layers != shape->n_layers) return fail(TFL_ERR_INVALID_ARG, "weights.n_layers != shape.n_layers");
+  tfl_options o;
+  tfl_default_options(&o);
+  if (opt) o = *opt;
+  if (o.precision != 0) return fail(TFL_ERR_UNSUPPORTED, "only precision 0 (fp16 operands) is implemented");
+  if (!(o.ln_eps > 0.f)) return fail(TFL_ERR_INVALID_ARG, "ln_eps must be > 0");
+  if (o.wait_timeout_ns <= 0) o.wait_timeout_ns = 2000000000LL;
+
+  int dev = 0;
+  TFL_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  cudaDeviceProp prop;
+  TFL_CUDA(cudaGetDeviceProperties(&prop, dev), "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(TFL_ERR_UNSUPPORTED, "device is sm_" + std::to_string(prop.major) + std::to_string(prop.minor) +
+                                         "; this library is built for sm_103a (GB300)");
+  if (!get_encode()) return fail(TFL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  TFL_CUDA(prepare_gemm_kernels(), "gemm kernel attributes");
+  TFL_CUDA(prepare_attention_kernels(), "attention kernel attributes");
+
+  const int D = shape->d_model, F = shape->d_ff, L = shape->n_layers;
+  const WsLayout lay = ws_layout(*shape);
+  // weights block: per layer 3D*D + D*D + F*D + D*F halves, 3D + D + F + D + 4D floats; + final LN
+  const size_t wl_half = (size_t)3 * D * D + (size_t)D * D + 2 * (size_t)F * D;
+  const size_t wl_float = (size_t)3 * D + D + F + D + 4 * (size_t)D;
+  const size_t per_layer = align_up(wl_half * 2, 1024) + align_up(wl_float * 4, 1024);
+  const size_t wbytes = per_layer * L + align_up((size_t)2 * D * 4, 1024);
+  if (o.max_workspace_bytes > 0 && (int64_t)(lay.total + wbytes) > o.max_workspace_bytes)
+    return fail(TFL_ERR_OOM, "workspace + weights (" + std::to_string(lay.total + wbytes) +
+                                 " bytes) exceed max_workspace_bytes");
+
+  tfl_handle* h = new tfl_handle();
+  h->shape = *shape;
+  h->opt = o;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->M = shape->B * shape->S;
+  h->D = D;
+  h->H = shape->n_heads;
+  h->hd = D / shape->n_heads;
+  h->F = F;
+  h->L = L;
+  h->lay = lay;
+  auto bail = [&](int code) {
+    tfl_destroy(h);
+    return code;
+  };
+
+  cudaError_t e = cudaMalloc(&h->ws, lay.total);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(TFL_ERR_OOM, "workspace allocation of " + std::to_string(lay.total) + " bytes failed"));
+  }
+  e = cudaMalloc(&h->wmem, wbytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(TFL_ERR_OOM, "weight allocation failed"));
+  }
+  if ((e = cudaMemset(h->ws, 0, lay.total)) != cudaSuccess) return bail(cuda_fail(e, "workspace memset"));
+  if ((e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking)) != cudaSuccess)
+    return bail(cuda_fail(e, "capture stream"));
+  uint8_t* wsb = static_cast<uint8_t*>(h->ws);
+  h->h32 = reinterpret_cast<float*>(wsb + lay.h32);
+  h->n16 = reinterpret_cast<__half*>(wsb + lay.n16);
+  h->qkv16 = reinterpret_cast<__half*>(wsb + lay.qkv16);
+  h->o16 = reinterpret_cast<__half*>(wsb + lay.o16);
+  h->g16 = reinterpret_cast<__half*>(wsb + lay.g16);
+  h->status = reinterpret_cast<int*>(wsb + lay.status);
+
+  float* tmp = nullptr;
+  if ((e = cudaMalloc(&tmp, (size_t)D * (F > 3 * D ? F : 3 * D) * sizeof(float))) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(TFL_ERR_OOM, "staging allocation failed"));
+  }
+  uint8_t* wp = static_cast<uint8_t*>(h->wmem);
+  h->layers.resize(L);
+  for (int l = 0; l < L && rc == TFL_OK; ++l) {
+    const tfl_layer_weights& src = w->layers[l];
+    LayerDev& d = h->layers[l];
+    uint8_t* base = wp + per_layer * l;
+    d.wqkv = reinterpret_cast<__half*>(base);
+    d.wo = d.wqkv + (size_t)3 * D * D;
+    d.w1 = d.wo + (size_t)D * D;
+    d.w2 = d.w1 + (size_t)F * D;
+    float* fb = reinterpret_cast<float*>(base + align_up(wl_half * 2, 1024));
+    d.bqkv = fb;
+    d.bo = d.bqkv + 3 * D;
+    d.b1 = d.bo + D;
+    d.b2 = d.b1 + F;
+    d.ln1_g = d.b2 + D;
+    d.ln1_b = d.ln1_g + D;
+    d.ln2_g = d.ln1_b + D;
+    d.ln2_b = d.ln2_g + D;
+    const size_t DD = (size_t)D * D;
+    if (!rc) rc = pack_f16(src.wq, DD, tmp, d.wqkv, "wq");
+    if (!rc) rc = pack_f16(src.wk, DD, tmp, d.wqkv + DD, "wk");
+    if (!rc) rc = pack_f16(src.wv, DD, tmp, d.wqkv + 2 * DD, "wv");
+    if (!rc) rc = pack_f16(src.wo, DD, tmp, d.wo, "wo");
+    if (!rc) rc = pack_f16(src.w1, (size_t)F * D, tmp, d.w1, "w1");
+    if (!rc) rc = pack_f16(src.w2, (size_t)F * D, tmp, d.w2, "w2");
+    if (!rc) rc = copy_f32(src.bq, D, d.bqkv, "bq");
+    if (!rc) rc = copy_f32(src.bk, D, d.bqkv + D, "bk");
+    if (!rc) rc = copy_f32(src.bv, D, d.bqkv + 2 * D, "bv");
+    if (!rc) rc = copy_f32(src.bo, D, d.bo, "bo");
+    if (!rc) rc = copy_f32(src.b1, F, d.b1, "b1");
+    if (!rc) rc = copy_f32(src.b2, D, d.b2, "b2");
+    if (!rc) rc = copy_f32(src.ln1_g, D, d.ln1_g, "ln1_g");
+    if (!rc) rc = copy_f32(src.ln1_b, D, d.ln1_b, "ln1_b");
+    if (!rc) rc = copy_f32(src.ln2_g, D, d.ln2_g, "ln2_g");
+    if (!rc) rc = copy_f32(src.ln2_b, D, d.ln2_b, "ln2_b");
+    if (!rc) {
+      bool ok = make_map_2d(&d.tm_wqkv, d.wqkv, 3 * D, D, gemm_bn(3 * D)) &&
+                make_map_2d(&d.tm_wo, d.wo, D, D, D == 128 ? 128 : gemm_bn(D)) &&
+                make_map_2d(&d.tm_w1, d.w1, F, D, gemm_bn(F)) &&
+                make_map_2d(&d.tm_w2, d.w2, D, F, D == 128 ? 128 : gemm_bn(D));
+      if (!ok) rc = fail(TFL_ERR_CUDA, "weight tensor map encoding failed");
+    }
+  }
+  cudaFree(tmp);
+  if (rc) return bail(rc);
+  float* lnf = reinterpret_cast<float*>(wp + per_layer * L);
+  h->lnf_g = lnf;
+  h->lnf_b = lnf + D;
+  if ((rc = copy_f32(w->lnf_g, D, h->lnf_g, "lnf_g")) != TFL_OK) return bail(rc);
+  if ((rc = copy_f32(w->lnf_b, D, h->lnf_b, "lnf_b")) != TFL_OK) return bail(rc);
+
+  const uint64_t M = (uint64_t)h->M;
+  const int atom = h->hd < 64 ? h->hd : 64;
+  bool ok = make_map_2d(&h->tm_n16, h->n16, M, D, kGemmBM) && make_map_2d(&h->tm_o16, h->o16, M, D, kGemmBM) &&
+            make_map_2d(&h->tm_g16, h->g16, M, F, kGemmBM) &&
+            make_map_qkv(&h->tm_q, h->qkv16, shape->B, shape->S, 3 * D, atom, kAttnBM) &&
+            make_map_qkv(&h->tm_kv, h->qkv16, shape->B, shape->S, 3 * D, atom, attn_block_n(h->hd));
+  if (!ok) return bail(fail(TFL_ERR_CUDA, "activation tensor map encoding failed"));
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(cuda_fail(e, "create"));
+  *out = h;
+  return TFL_OK;
+}
+
+static int run_forward(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out,
+                       cudaStream_t st) {
+  if (!h->opt.use_graph) return enqueue(h, x, lengths, causal, out, st, Rec{});
+  for (auto& g : h->graphs)
+    if (g.causal == causal && g.x == x && g.len == lengths && g.out == out) {
+      TFL_CUDA(cudaGraphLaunch(g.exec, st), "cudaGraphLaunch");
+      return TFL_OK;
+    }
+  cudaGraph_t graph = nullptr;
+  cudaStream_t cs = h->cap_stream;
+  TFL_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "cudaStreamBeginCapture");
+  int rc = enqueue(h, x, lengths, causal, out, cs, Rec{});
+  cudaError_t e = cudaStreamEndCapture(cs, &graph);
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
+  if (h->graphs.size() >= 8) {
+    cudaGraphExecDestroy(h->graphs.front().exec);
+    h->graphs.erase(h->graphs.begin());
+  }
+  h->graphs.push_back(GraphEntry{causal, x, lengths, out, exec});
+  TFL_CUDA(cudaGraphLaunch(exec, st), "cudaGraphLaunch");
+  return TFL_OK;
+}
+
+int tfl_forward(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out, tfl_stream stream) {
+  g_err.clear();
+  if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (!x || !out) return fail(TFL_ERR_INVALID_ARG, "x and out must be non-NULL device pointers");
+  if (causal != 0 && causal != 1) return fail(TFL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  const size_t bytes = (size_t)h->M * h->D * sizeof(float);
+  const uint8_t *xb = reinterpret_cast<const uint8_t*>(x), *ob = reinterpret_cast<const uint8_t*>(out);
+  if (xb < ob + bytes && ob < xb + bytes) return fail(TFL_ERR_INVALID_ARG, "out overlaps x");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(TFL_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  return run_forward(h, x, lengths, causal, out, static_cast<cudaStream_t>(stream));
+}
+
+int tfl_status(tfl_handle* h, tfl_stream stream) {
+  if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TFL_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  int v = 0;
+  TFL_CUDA(cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost), "status read");
+  if (v) TFL_CUDA(cudaMemset(h->status, 0, sizeof(int)), "status clear");
+  if (v & TFL_DEV_TIMEOUT) return fail(TFL_ERR_DEVICE_TIMEOUT, "a device-side wait ran out of time");
+  if (v & TFL_DEV_BAD_LENGTHS) return fail(TFL_ERR_BAD_LENGTHS, "a length was outside [0, S] and was clamped");
+  return TFL_OK;
+}
+
+int tfl_forward_host(tfl_handle* h, const float* x_host, const int32_t* lengths_host, int causal, float* out_host,
+                     tfl_stream stream) {
+  g_err.clear();
+  if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (!x_host || !out_host) return fail(TFL_ERR_INVALID_ARG, "x and out must be non-NULL host pointers");
+  const size_t bytes = (size_t)h->M * h->D * sizeof(float);
+  if (!h->hx_dev) {
+    if (cudaMalloc(&h->hx_dev, bytes) != cudaSuccess || cudaMalloc(&h->hout_dev, bytes) != cudaSuccess ||
+        cudaMalloc(&h->hlen_dev, (size_t)h->shape.B * sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TFL_ERR_OOM, "staging buffers for tfl_forward_host");
+    }
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TFL_CUDA(cudaMemcpyAsync(h->hx_dev, x_host, bytes, cudaMemcpyHostToDevice, st), "x upload");
+  if (lengths_host)
+    TFL_CUDA(cudaMemcpyAsync(h->hlen_dev, lengths_host, (size_t)h->shape.B * sizeof(int), cudaMemcpyHostToDevice, st),
+             "lengths upload");
+  int rc = run_forward(h, h->hx_dev, lengths_host ? h->hlen_dev : nullptr, causal, h->hout_dev, st);
+  if (rc) return rc;
+  TFL_CUDA(cudaMemcpyAsync(out_host, h->hout_dev, bytes, cudaMemcpyDeviceToHost, st), "out download");
+  return tfl_status(h, stream);
+}
+
+int tfl_profile_forward(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out,
+                        tfl_stream stream, float* kernel_ms, int32_t* kernel_kind, int32_t cap, int32_t* n) {
+  g_err.clear();
+  if (!h || !x || !out || !n) return fail(TFL_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> kinds;
+  Rec r;
+  r.on = true;
+  r.ev = &ev;
+  r.kinds = &kinds;
+  int rc = enqueue(h, x, lengths, causal, out, st, r);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (!rc && e != cudaSuccess) rc = cuda_fail(e, "profile sync");
+  const int cnt = (int)kinds.size();
+  *n = cnt;
+  for (int i = 0; i < cnt && i < cap && !rc; ++i) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, ev[i], ev[i + 1]);
+    if (kernel_ms) kernel_ms[i] = ms;
+    if (kernel_kind) kernel_kind[i] = kinds[i];
+  }
+  for (auto e2 : ev) cudaEventDestroy(e2);
+  return rc;
+}
+
+void tfl_destroy(tfl_handle* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  if (h->ws) cudaFree(h->ws);
+  if (h->wmem) cudaFree(h->wmem);
+  if (h->hx_dev) cudaFree(h->hx_dev);
+  if (h->hout_dev) cudaFree(h->hout_dev);
+  if (h->hlen_dev) cudaFree(h->hlen_dev);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  delete h;
+}
+
+int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream) {
+  g_err.clear();
+  if (timeout_ns <= 0) return fail(TFL_ERR_INVALID_ARG, "timeout must be > 0");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = nullptr;
+  TFL_CUDA(cudaMalloc(&status, sizeof(int)), "probe alloc");
+  cudaMemset(status, 0, sizeof(int));
+  cudaError_t e = launch_probe_wait(status, timeout_ns, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  int v = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(status);
+  if (e != cudaSuccess) return cuda_fail(e, "probe");
+  if (v & TFL_DEV_TIMEOUT) return fail(TFL_ERR_DEVICE_TIMEOUT, "probe wait ran out as expected");
+  return TFL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,474 @@
+// attention.cu -- flash attention forward on tcgen05 tensor cores.
+//
+// Per (sequence b, head h, block of 128 queries) the kernel computes
+// O = softmax(Q K^T / sqrt(hd) + mask) V without materialising the score
+// matrix ("TikTok TechJam 2026 -- Problem 3", section 2.1):
+//   * S = Q K_j^T for one key block at a time goes to tensor memory (fp32).
+//   * Online softmax in fp32, one query row per thread (the row's TMEM lane):
+//     running max m, running sum l, O rescaled by exp(m_old - m_new)
+//     (section 2.1, the running-max recurrence).  The rescale is lazy: the
+//     reference max only moves when the row max grew by more than 8 in log2
+//     units, so P <= 2^8 and O is touched rarely; O / l is exact either way.
+//   * P = exp2(S * log2(e)/sqrt(hd) - m) in fp16 goes to shared memory and
+//     O += P V_j accumulates in tensor memory.
+//   * Causal: key blocks above the diagonal are never loaded (block skipping,
+//     section 1.C); the mask is applied only on the diagonal block; the key
+//     mask is not applied at all, because for a valid query i every key j <= i
+//     is valid (section 2.1, "the mask trick").
+//   * Key padding (non-causal): only the block holding len_b is masked.
+//   * Query blocks past len_b are skipped; their output rows are never read
+//     for a valid token.
+// q, k, v are strided views of the fused QKV output [B, S, 3D] (section 1.A,
+// head-split copies removed); O is written straight into [B, S, H*hd].
+//
+// Warp roles: warps 0-3 softmax + output (thread = query row), warp 4 TMA
+// producer (Q once per work item, K/V blocks into an NST-deep ring), warp 5
+// MMA issuer and TMEM owner.  Persistent CTAs walk the work items heaviest
+// first (causal: the last query blocks have the most keys).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace tfl {
+
+template <int HD>
+struct AttnCfg {
+  static constexpr int BM = kAttnBM;
+  static constexpr int BN = attn_block_n(HD);      // keys per block
+  static constexpr int ATOM_C = HD < 64 ? HD : 64;  // head-dim columns per TMA box / swizzle atom
+  static constexpr int NATOM = HD / ATOM_C;
+  static constexpr int ROWB = ATOM_C * 2;           // bytes of one row inside an atom
+  static constexpr uint32_t SWZ = ROWB == 64 ? kSw64 : kSw128;
+  static constexpr int Q_BYTES = BM * HD * 2;
+  static constexpr int KV_BYTES = BN * HD * 2;      // one K (or V) block
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int NST = HD == 32 ? 4 : 2;
+  static constexpr int CTAS_PER_SM = HD == 32 ? 2 : 1;
+  static constexpr int O_COL = HD <= 64 ? 128 : 256;
+  static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
+  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)NST * 2 * KV_BYTES + P_BYTES + 256;
+};
+
+size_t attn_smem_bytes(int hd) {
+  switch (hd) {
+    case 32: return AttnCfg<32>::SMEM;
+    case 64: return AttnCfg<64>::SMEM;
+    case 256: return AttnCfg<256>::SMEM;
+  }
+  return 0;
+}
+
+struct Item {
+  int b, h, qb, len, nkb;
+};
+
+// Work item i (heaviest first) -> (b, h, query block); false if the block is all padding.
+__device__ __forceinline__ bool decode_item(int i, const AttnArgs& a, int nqb, int bn, Item& it) {
+  const int bh_count = a.B * a.H;
+  const int qr = i / bh_count, bh = i - qr * bh_count;
+  it.qb = nqb - 1 - qr;
+  it.b = bh / a.H;
+  it.h = bh - it.b * a.H;
+  it.len = seq_len(a.c.lengths, it.b, a.c.S);
+  if (it.qb * kAttnBM >= it.len) return false;
+  const int kend = a.causal ? min((it.qb + 1) * kAttnBM, it.len) : it.len;
+  it.nkb = (kend + bn - 1) / bn;
+  return true;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
+    attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                const AttnArgs args) {
+  using C = AttnCfg<HD>;
+  constexpr int BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + C::Q_BYTES;
+  uint8_t* sV = sK + (size_t)C::NST * C::KV_BYTES;
+  uint8_t* sP = sV + (size_t)C::NST * C::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + C::P_BYTES);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* s_full = bars + 2;
+  uint64_t* p_full = bars + 3;
+  uint64_t* o_full = bars + 4;
+  uint64_t* o_empty = bars + 5;
+  uint64_t* drain = bars + 6;
+  uint64_t* kv_full = bars + 7;
+  uint64_t* kv_empty = kv_full + C::NST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kv_empty + C::NST);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* never_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 4);
+    mbar_init(drain, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    *abort_flag = 0;
+    *never_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmKV);
+  }
+  if (warp == 5) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{args.c.status, abort_flag, args.c.timeout_ns};
+
+  const int S = args.c.S, D = args.D;
+  const int nqb = (S + kAttnBM - 1) / kAttnBM;
+  const int items = args.B * args.H * nqb;
+
+  uint32_t issued_mask = 0, issued_par = 0;  // producer: stages with loads in flight (abort path)
+  bool q_issued = false;
+  uint32_t q_par = 0;
+  bool mma_issued = false;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t kvph = 0, qph = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+        Item it;
+        if (!decode_item(i, args, nqb, BN, it)) continue;
+        if (!wait_bounded(q_empty, qph ^ 1u, wc)) break;
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+        for (int a = 0; a < C::NATOM; ++a)
+          tma_load_3d(sQ + a * (kAttnBM * C::ROWB), &tmQ, q_full, it.h * HD + a * C::ATOM_C, it.qb * kAttnBM, it.b);
+        q_issued = true;
+        q_par = qph;
+        qph ^= 1u;
+        for (int j = 0; j < it.nkb; ++j) {
+          if (!wait_bounded(&kv_empty[st], kvph ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[st], 2 * C::KV_BYTES);
+          uint8_t* k = sK + (size_t)st * C::KV_BYTES;
+          uint8_t* v = sV + (size_t)st * C::KV_BYTES;
+#pragma unroll
+          for (int a = 0; a < C::NATOM; ++a) {
+            tma_load_3d(k + a * (BN * C::ROWB), &tmKV, &kv_full[st], D + it.h * HD + a * C::ATOM_C, j * BN, it.b);
+            tma_load_3d(v + a * (BN * C::ROWB), &tmKV, &kv_full[st], 2 * D + it.h * HD + a * C::ATOM_C, j * BN,
+                        it.b);
+          }
+          issued_mask |= 1u << st;
+          issued_par = (issued_par & ~(1u << st)) | (kvph << st);
+          if (++st == C::NST) {
+            st = 0;
+            kvph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    constexpr uint32_t idesc_qk = idesc_f16(128, BN, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_f16(128, HD, 0, 1);
+    const uint32_t d_s = tmem_base;
+    const uint32_t d_o = tmem_base + C::O_COL;
+    int st = 0;
+    uint32_t kvph = 0, qph = 0, pph = 0, oeph = 0;
+    bool first_item = true, ok = true;
+    auto issue_pv = [&](int pst, bool accumulate) {
+      const uint32_t sp = smem_u32(sP), sv = smem_u32(sV + (size_t)pst * C::KV_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint64_t ad = sdesc(sp + (kk >> 2) * (kAttnBM * 128) + (kk & 3) * 32, 16, 1024, kSw128);
+        const uint64_t bd = sdesc(sv + kk * 16 * C::ROWB, BN * C::ROWB, 8 * C::ROWB, C::SWZ);
+        umma_f16(d_o, ad, bd, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+      }
+    };
+    for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+      Item it;
+      if (!decode_item(i, args, nqb, BN, it)) continue;
+      if (!wait_bounded(q_full, qph, wc)) break;
+      qph ^= 1u;
+      tc_fence_after();
+      bool need_oe = !first_item;
+      int prev_st = 0;
+      for (int j = 0; j < it.nkb; ++j) {
+        if (!wait_bounded(&kv_full[st], kvph, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // Keys at or past len_b in this block: clear their V rows so stale
+        // workspace contents can never reach O through a zero probability.
+        const int vrow0 = it.len - j * BN;
+        if (vrow0 < BN) {
+          uint8_t* v = sV + (size_t)st * C::KV_BYTES;
+          for (int rr = max(vrow0, 0) + lane; rr < BN; rr += 32) {
+#pragma unroll
+            for (int a = 0; a < C::NATOM; ++a) {
+              uint4* row = reinterpret_cast<uint4*>(v + a * (BN * C::ROWB) + rr * C::ROWB);
+#pragma unroll
+              for (int c = 0; c < C::ROWB / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_async_smem();
+          __syncwarp();
+        }
+        if (j > 0) {
+          if (!wait_bounded(p_full, pph, wc)) {
+            ok = false;
+            break;
+          }
+          pph ^= 1u;
+          if (need_oe) {
+            if (!wait_bounded(o_empty, oeph, wc)) {
+              ok = false;
+              break;
+            }
+            oeph ^= 1u;
+            need_oe = false;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv(prev_st, j - 1 > 0);
+            umma_commit(&kv_empty[prev_st]);
+          }
+        }
+        if (lane == 0) {
+          const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK + (size_t)st * C::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const int a = kk / (C::ATOM_C / 16), w = kk % (C::ATOM_C / 16);
+            const uint64_t ad = sdesc(sq + a * (kAttnBM * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
+            const uint64_t bd = sdesc(sk + a * (BN * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
+            umma_f16(d_s, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_issued = true;
+          umma_commit(s_full);
+          if (j == it.nkb - 1) umma_commit(q_empty);
+        }
+        __syncwarp();
+        prev_st = st;
+        if (++st == C::NST) {
+          st = 0;
+          kvph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (!wait_bounded(p_full, pph, wc)) break;
+      pph ^= 1u;
+      if (need_oe) {
+        if (!wait_bounded(o_empty, oeph, wc)) break;
+        oeph ^= 1u;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv(prev_st, it.nkb > 1);
+        umma_commit(&kv_empty[prev_st]);
+        umma_commit(o_full);
+      }
+      __syncwarp();
+      first_item = false;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + output (warps 0-3)
+    const int r = warp * 32 + lane;  // query row within the block == TMEM lane
+    const uint32_t t_s = tmem_base + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_o = t_s + C::O_COL;
+    const float sl2 = args.scale_log2;
+    uint32_t sph = 0, oph = 0;
+    uint8_t* prow = sP + r * 128;
+    const uint32_t swz = (uint32_t)(r & 7);
+    for (int i = blockIdx.x; i < items; i += gridDim.x) {
+      Item it;
+      if (!decode_item(i, args, nqb, BN, it)) continue;
+      const int qpos = it.qb * kAttnBM + r;
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < it.nkb; ++j) {
+        if (!wait_bounded(s_full, sph, wc)) {
+          ok = false;
+          break;
+        }
+        sph ^= 1u;
+        tc_fence_after();
+        const int k0 = j * BN;
+        const bool need_mask = args.causal ? (k0 + BN - 1 > it.qb * kAttnBM) : (k0 + BN > it.len);
+        const int kmax = args.causal ? qpos : it.len - 1;  // last allowed key when masking
+        // pass 1: row max of the raw scores
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float s[32];
+          tmem_ld32(t_s + c * 32, s);
+          tmem_wait_ld();
+          if (need_mask) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (k0 + c * 32 + e <= kmax) mx = fmaxf(mx, s[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, s[e]);
+          }
+        }
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const bool resc = m_new > m_run + 8.0f;
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // O holds PV of every earlier block (s_full(j) was committed after PV(j-1)).
+          const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            float o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(t_o + c * 32, o);
+          }
+          tmem_wait_st();
+          l_run *= alpha;
+        }
+        if (resc) m_run = m_new;
+        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+        // pass 2: P = exp2(s * scale_log2 - m), fp16, into the swizzled P tile
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float s[32];
+          tmem_ld32(t_s + c * 32, s);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float p = ex2(fmaf(s[e], sl2, -mref));
+            if (need_mask && (k0 + c * 32 + e > kmax)) p = 0.f;
+            s[e] = p;
+            lsum += p;
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int key = c * 32 + g * 8;  // first of 8 keys in this 16-byte chunk
+            const uint32_t chunk = (uint32_t)((key & 63) >> 3);
+            __half2 h0 = __floats2half2_rn(s[g * 8 + 0], s[g * 8 + 1]);
+            __half2 h1 = __floats2half2_rn(s[g * 8 + 2], s[g * 8 + 3]);
+            __half2 h2 = __floats2half2_rn(s[g * 8 + 4], s[g * 8 + 5]);
+            __half2 h3 = __floats2half2_rn(s[g * 8 + 6], s[g * 8 + 7]);
+            uint4 u;
+            u.x = *reinterpret_cast<uint32_t*>(&h0);
+            u.y = *reinterpret_cast<uint32_t*>(&h1);
+            u.z = *reinterpret_cast<uint32_t*>(&h2);
+            u.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(prow + (key >> 6) * (kAttnBM * 128) + ((chunk ^ swz) << 4)) = u;
+          }
+        }
+        l_run += lsum;
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      if (!wait_bounded(o_full, oph, wc)) break;
+      oph ^= 1u;
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      const bool store = qpos < S;
+      __half* orow = args.o16 + ((size_t)it.b * S + (store ? qpos : 0)) * D + it.h * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float o[32];
+        tmem_ld32(t_o + c * 32, o);
+        tmem_wait_ld();
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            __half2 h0 = __floats2half2_rn(o[g * 8 + 0] * inv, o[g * 8 + 1] * inv);
+            __half2 h1 = __floats2half2_rn(o[g * 8 + 2] * inv, o[g * 8 + 3] * inv);
+            __half2 h2 = __floats2half2_rn(o[g * 8 + 4] * inv, o[g * 8 + 5] * inv);
+            __half2 h3 = __floats2half2_rn(o[g * 8 + 6] * inv, o[g * 8 + 7] * inv);
+            uint4 u;
+            u.x = *reinterpret_cast<uint32_t*>(&h0);
+            u.y = *reinterpret_cast<uint32_t*>(&h1);
+            u.z = *reinterpret_cast<uint32_t*>(&h2);
+            u.w = *reinterpret_cast<uint32_t*>(&h3);
+            dst[g] = u;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    const WaitCtl dc{args.c.status, never_flag, 100000000LL};
+    if (warp == 4 && lane == 0) {
+      if (q_issued) wait_bounded(q_full, q_par, dc);
+      for (int s = 0; s < C::NST; ++s)
+        if (issued_mask & (1u << s)) wait_bounded(&kv_full[s], (issued_par >> s) & 1u, dc);
+    }
+    if (warp == 5 && lane == 0 && mma_issued) {
+      umma_commit(drain);
+      wait_bounded(drain, 0, dc);
+    }
+    __syncthreads();
+  }
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int HD>
+static cudaError_t launch_attn_hd(const CUtensorMap& tq, const CUtensorMap& tkv, const AttnArgs& a, int num_sms,
+                                  cudaStream_t s) {
+  using C = AttnCfg<HD>;
+  auto kern = attn_kernel<HD>;
+  const int items = a.B * a.H * ((a.c.S + kAttnBM - 1) / kAttnBM);
+  const int cap = num_sms * C::CTAS_PER_SM;
+  const int grid = items < cap ? items : cap;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, 192, C::SMEM, s>>>(tq, tkv, a);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_attention_kernels() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)AttnCfg<32>::SMEM)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)AttnCfg<64>::SMEM)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(attn_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)AttnCfg<256>::SMEM);
+}
+
+cudaError_t launch_attention(int hd, const CUtensorMap& tq, const CUtensorMap& tkv, const AttnArgs& a,
+                             int num_sms, cudaStream_t s) {
+  switch (hd) {
+    case 32: return launch_attn_hd<32>(tq, tkv, a, num_sms, s);
+    case 64: return launch_attn_hd<64>(tq, tkv, a, num_sms, s);
+    case 256: return launch_attn_hd<256>(tq, tkv, a, num_sms, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tfl

@@ -1,0 +1,103 @@
+// kernels.h -- argument blocks and host launchers of the forward's kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+// Bits of the device status word (OR-ed by kernels, read by tfl_status).
+#define TFL_DEV_TIMEOUT 1
+#define TFL_DEV_BAD_LENGTHS 2
+
+namespace tfl {
+
+// Row-epilogue operations (GEMM epilogue with BN == d_model, and the
+// standalone row kernel).  Starting from the fp32 row t:
+//   POST_LN     t = LN(t; ga, ba)                     (post-LN residual norm)
+//   WRITE_H     h32[row] = t                          (residual stream)
+//   FINAL       out32[row] = valid ? LN(t; gf, bf) : 0 (model tail)
+//   NORM16      n16[row] = fp16(LN(t; gb, bb))        (pre-LN sublayer input)
+//   CAST16      n16[row] = fp16(t)                    (post-LN sublayer input)
+enum RowFlags : int {
+  ROW_POST_LN = 1,
+  ROW_WRITE_H = 2,
+  ROW_FINAL = 4,
+  ROW_NORM16 = 8,
+  ROW_CAST16 = 16,
+};
+
+struct RowOps {
+  int flags = 0;
+  float eps = 1e-5f;
+  const float *ga = nullptr, *ba = nullptr;  // POST_LN affine
+  const float *gb = nullptr, *bb = nullptr;  // NORM16 affine
+  const float *gf = nullptr, *bf = nullptr;  // FINAL affine
+  float* h32 = nullptr;                      // [M, D]
+  __half* n16 = nullptr;                     // [M, D]
+  float* out32 = nullptr;                    // [M, D]
+};
+
+struct Common {
+  int M = 0;                       // B * S rows
+  int S = 0;
+  const int* lengths = nullptr;    // device [B] or null
+  int* status = nullptr;           // device status word
+  int64_t timeout_ns = 2000000000LL;
+};
+
+// GEMM: C[M, N] = A[M, K] (fp16, K-major) * W[N, K]^T (fp16, K-major), fp32 accumulate.
+enum GemmEpi : int {
+  EPI_BIAS_F16 = 0,       // c16 = acc + bias
+  EPI_BIAS_GELU_F16 = 1,  // c16 = GELU(acc + bias)
+  EPI_BIAS_RES_F32 = 2,   // h32 = acc + bias + (valid ? res : 0)
+  EPI_BIAS_RES_ROW = 3,   // t = acc + bias + (valid ? res : 0), then RowOps (N == BN == d_model)
+};
+
+struct GemmArgs {
+  Common c;
+  int N = 0, K = 0;
+  const float* bias = nullptr;   // [N]
+  __half* c16 = nullptr;         // [M, N] for the fp16 epilogues
+  const float* res = nullptr;    // [M, N] residual for the fp32 epilogues (may alias h32)
+  float* h32 = nullptr;          // EPI_BIAS_RES_F32 output
+  RowOps row;                    // EPI_BIAS_RES_ROW
+};
+
+struct AttnArgs {
+  Common c;
+  int B = 0, H = 0, D = 0;
+  int causal = 0;
+  float scale_log2 = 0.f;        // log2(e) / sqrt(head_dim)
+  __half* o16 = nullptr;         // [M, D]
+};
+
+struct RowArgs {
+  Common c;
+  int D = 0;
+  const float* in32 = nullptr;   // [M, D] fp32 input rows (x or h32)
+  RowOps row;
+};
+
+// One-time kernel attributes (dynamic shared memory opt-in); call before any capture.
+cudaError_t prepare_gemm_kernels();
+cudaError_t prepare_attention_kernels();
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                        int num_sms, cudaStream_t s);
+cudaError_t launch_attention(int hd, const CUtensorMap& tq, const CUtensorMap& tkv, const AttnArgs& a,
+                             int num_sms, cudaStream_t s);
+cudaError_t launch_rows(const RowArgs& a, cudaStream_t s);
+cudaError_t launch_check_lengths(const int* lengths, int B, int S, int* status, cudaStream_t s);
+cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s);
+cudaError_t launch_probe_wait(int* status, int64_t timeout_ns, cudaStream_t s);
+
+// Tile sizes shared by the host planner and the kernels.
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;
+constexpr int kAttnBM = 128;
+__host__ __device__ constexpr int attn_block_n(int hd) { return hd >= 128 ? 64 : 128; }
+size_t gemm_smem_bytes(int bn);
+size_t attn_smem_bytes(int hd);
+
+}  // namespace tfl

@@ -1,0 +1,158 @@
+// rows.cu -- row-wise kernels: LayerNorm / cast / model tail, weight cast,
+// length check and the bounded-wait self-test.
+//
+// The row kernel is one warp per token row, fp32 statistics with the
+// variance taken in a second pass over registers ("TikTok TechJam 2026 --
+// Problem 3", section 3: the one-pass variance was rejected), coalesced
+// float4 loads and warp-shuffle reductions.  It serves the layer-0 input
+// LayerNorm (the layer_norm_cast item of section 1.A: no residual copy is
+// written, the residual stream starts as x) and, when d_model > 128, the
+// add-LayerNorm that follows each residual GEMM and the model tail (final
+// LayerNorm + pad-mask + fp32 output).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace tfl {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Normalise the lane's V float4 chunks of a row of D = 128 * V values.
+template <int V>
+__device__ __forceinline__ void warp_ln(float4* t, float eps, const float* g, const float* b, int lane, float4* y) {
+  constexpr float invD = 1.0f / (128 * V);
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < V; ++k) s += t[k].x + t[k].y + t[k].z + t[k].w;
+  const float mean = warp_sum(s) * invD;
+  float q = 0.f;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const float a = t[k].x - mean, bb = t[k].y - mean, c = t[k].z - mean, d = t[k].w - mean;
+    q += a * a + bb * bb + c * c + d * d;
+  }
+  const float rstd = rsqrtf(warp_sum(q) * invD + eps);
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int col = (k * 32 + lane) * 4;
+    const float4 gg = __ldg(reinterpret_cast<const float4*>(g + col));
+    const float4 bv = __ldg(reinterpret_cast<const float4*>(b + col));
+    y[k] = make_float4((t[k].x - mean) * rstd * gg.x + bv.x, (t[k].y - mean) * rstd * gg.y + bv.y,
+                       (t[k].z - mean) * rstd * gg.z + bv.z, (t[k].w - mean) * rstd * gg.w + bv.w);
+  }
+}
+
+__device__ __forceinline__ void store_h4(__half* p, float4 v) {
+  __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <int V>
+__global__ void __launch_bounds__(256) rows_kernel(const RowArgs a) {
+  constexpr int D = 128 * V;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x * 8 + warp;
+  if (m >= a.c.M) return;
+  const RowOps& ro = a.row;
+  const bool valid = row_valid(m, a.c.S, a.c.lengths);
+  float4 t[V];
+  const float4* in = reinterpret_cast<const float4*>(a.in32 + (size_t)m * D);
+#pragma unroll
+  for (int k = 0; k < V; ++k) t[k] = valid ? in[k * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (ro.flags & ROW_POST_LN) warp_ln<V>(t, ro.eps, ro.ga, ro.ba, lane, t);
+  if (ro.flags & ROW_WRITE_H) {
+    float4* hp = reinterpret_cast<float4*>(ro.h32 + (size_t)m * D);
+#pragma unroll
+    for (int k = 0; k < V; ++k) hp[k * 32 + lane] = t[k];
+  }
+  if (ro.flags & ROW_FINAL) {
+    float4 y[V];
+    warp_ln<V>(t, ro.eps, ro.gf, ro.bf, lane, y);
+    float4* op = reinterpret_cast<float4*>(ro.out32 + (size_t)m * D);
+#pragma unroll
+    for (int k = 0; k < V; ++k) op[k * 32 + lane] = valid ? y[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+  } else if (ro.flags & ROW_NORM16) {
+    float4 y[V];
+    warp_ln<V>(t, ro.eps, ro.gb, ro.bb, lane, y);
+#pragma unroll
+    for (int k = 0; k < V; ++k) store_h4(ro.n16 + (size_t)m * D + (k * 32 + lane) * 4, y[k]);
+  } else if (ro.flags & ROW_CAST16) {
+#pragma unroll
+    for (int k = 0; k < V; ++k) store_h4(ro.n16 + (size_t)m * D + (k * 32 + lane) * 4, t[k]);
+  }
+}
+
+cudaError_t launch_rows(const RowArgs& a, cudaStream_t s) {
+  const int grid = (a.c.M + 7) / 8;
+  if (grid <= 0) return cudaSuccess;
+  switch (a.D / 128) {
+    case 1: rows_kernel<1><<<grid, 256, 0, s>>>(a); break;
+    case 2: rows_kernel<2><<<grid, 256, 0, s>>>(a); break;
+    case 4: rows_kernel<4><<<grid, 256, 0, s>>>(a); break;
+    case 8: rows_kernel<8><<<grid, 256, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// Flags TFL_DEV_BAD_LENGTHS if any length is outside [0, S] (kernels clamp).
+__global__ void check_lengths_kernel(const int* lengths, int B, int S, int* status) {
+  if (lengths == nullptr) return;
+  bool bad = false;
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
+    const int l = lengths[b];
+    bad |= (l < 0) || (l > S);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, TFL_DEV_BAD_LENGTHS);
+}
+
+cudaError_t launch_check_lengths(const int* lengths, int B, int S, int* status, cudaStream_t s) {
+  int grid = (B + 255) / 256;
+  if (grid > 64) grid = 64;
+  check_lengths_kernel<<<grid, 256, 0, s>>>(lengths, B, S, status);
+  return cudaGetLastError();
+}
+
+__global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __float2half_rn(src[i]);
+}
+
+cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  size_t grid = (n + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  f32_to_f16_kernel<<<(unsigned)grid, 256, 0, s>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+// One block waits on an mbarrier that nothing completes, with the same
+// bounded wait every pipeline kernel uses; it must give up and flag a timeout.
+__global__ void probe_wait_kernel(int* status, int64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl wc{status, &abort_flag, timeout_ns};
+    wait_bounded(&bar, 0, wc);
+  }
+  __syncthreads();
+}
+
+cudaError_t launch_probe_wait(int* status, int64_t timeout_ns, cudaStream_t s) {
+  probe_wait_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace tfl

@@ -1,0 +1,347 @@
+"""Benchmark: forward tokens/s of the Transformer-stack forward on one GB300.
+
+Default workload: B=64, S=1024, d_model=128, H=4 (head_dim 32), d_ff=512,
+4 layers, causal, right-padded lengths uniform in [512, 1024] (seed 0).
+A step is one whole forward (all layers) over that batch; tokens per step =
+B*S (every position, as the pages count tokens).
+
+Prints ONE JSON line (rank 0).  Keys beyond the base contract:
+  roofline      dominant kernel of the step: algorithmic work per launch /
+                its CUDA-event duration, against the measured peak
+  cpu_baseline  the fp64 oracle timed on this host on a bounded sample
+  e2e           tokens/s through tfl_forward_host (pinned host x / out,
+                host<->device copies inside the timed region)
+  clocks        SM clock samples taken during the timed region
+With --impl reference the fp64 oracle itself is timed as the reference arm.
+Multi-GPU (torchrun): every rank runs an independent replica on its own
+batch (sequences are independent; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+MUFU_PER_CLK_PER_SM = 16  # ex2 throughput of one SM per clock
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "tc_tflops": float(d["bf16_tflops"]),
+                "tc_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "tc_tflops": 1900.0, "tc_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle sampling in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def workload(idx: int) -> synth.Shape:
+    return synth.WORKLOADS[idx]
+
+
+def algorithmic(shape: synth.Shape, lens: np.ndarray, causal: bool):
+    """Per-forward algorithmic FLOPs and per-kernel units (valid rows, allowed pairs only)."""
+    D, F, H, L = shape.d_model, shape.d_ff, shape.n_heads, shape.n_layers
+    hd = D // H
+    lens = lens.astype(np.float64)
+    valid = float(lens.sum())
+    pairs = float((lens * (lens + 1) / 2).sum()) if causal else float((lens * lens).sum())
+    lin = 2.0 * valid * (3 * D * D + D * D + 2 * D * F) * L
+    att = 4.0 * pairs * hd * H * L
+    return {"valid_tokens": valid, "pairs": pairs, "linear_flops": lin, "attn_flops": att,
+            "attn_exps_per_launch": pairs * H, "attn_flops_per_launch": 4.0 * pairs * hd * H}
+
+
+def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
+    """Algorithmic HBM bytes per launch of the row-streaming kernels (valid rows only)."""
+    D, F = shape.d_model, shape.d_ff
+    return {
+        "gemm_qkv": valid * (D * 2 + 3 * D * 2),
+        "gemm_ffn1": valid * (D * 2 + F * 2),
+        "gemm_oproj": valid * (D * 2 + D * 4 + D * 4 + D * 2),
+        "gemm_ffn2": valid * (F * 2 + D * 4 + D * 4 + D * 2),
+        "rownorm": valid * (D * 4 + D * 2),
+    }.get(kind)
+
+
+def run_oracle_sample(shape, prm, seed, n_seq):
+    import oracle
+    lens = synth.lengths(seed, shape)
+    batches = np.arange(n_seq)
+    x = synth.input_x(seed, shape, batches=batches)
+    t0 = time.perf_counter()
+    oracle.forward(prm, shape.n_heads, x, lens[batches], shape.causal)
+    dt = time.perf_counter() - t0
+    return dt, n_seq * shape.S
+
+
+def reference_arm(args, shape, world, rank):
+    """The fp64 oracle timed as the reference arm (host cores, bounded sample per step)."""
+    if rank != 0:
+        return 0
+    prm = synth.params(0, shape)
+    n_seq = max(1, min(shape.B, args.ref_seqs))
+    for _ in range(max(0, min(args.warmup, 1))):
+        run_oracle_sample(shape, prm, 0, 1)
+    times = []
+    for _ in range(args.steps):
+        dt, tok = run_oracle_sample(shape, prm, 0, n_seq)
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    value = (n_seq * shape.S) / (ms / 1e3)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": "forward_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(shape),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_seq} of {shape.B} sequences ({n_seq * shape.S} tokens) per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(shape):
+    return {"workload": shape.name, "B": shape.B, "S": shape.S, "d_model": shape.d_model, "n_heads": shape.n_heads,
+            "d_ff": shape.d_ff, "n_layers": shape.n_layers, "causal": shape.causal,
+            "lengths": "full" if shape.len_lo is None else f"uniform[{shape.len_lo},{shape.len_hi}]",
+            "l2": "flushed (256 MiB write) between timed steps", "seed": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=1, help="index into the workload table (default: B64 S1024)")
+    ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference/oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    world, rank, local = dist_env()
+    shape = workload(args.workload)
+    if args.impl == "reference":
+        return reference_arm(args, shape, world, rank)
+
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    from attention_qkv_gemm_gb300 import build as libbuild
+
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        libbuild.build()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+        dist.barrier()
+        libbuild.build()
+    pkg.load()
+
+    seed = rank  # each replica its own batch
+    prm = synth.params(seed, shape)
+    lens_np = synth.lengths(seed, shape)
+    x_np = synth.input_x(seed, shape)
+    dev = torch.device("cuda", local)
+    x = torch.from_numpy(x_np).to(dev)
+    lens = torch.from_numpy(lens_np).to(dev)
+    out = torch.empty_like(x)
+    m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def fwd():
+        pkg.tfl_forward(m.handle, x.data_ptr(), lens.data_ptr(), int(shape.causal), out.data_ptr(), sp)
+
+    for _ in range(args.warmup):
+        fwd()
+    rc = m.status(sp)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc}: {pkg.tfl_last_error()}")
+
+    # ---------------- timed region: graph replays, L2 flushed between steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for s, e in evs:
+        flush.fill_(1.0)
+        s.record(stream)
+        fwd()
+        e.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    clocks = sampler.stop()
+    rc = m.status(sp)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc}: {pkg.tfl_last_error()}")
+    ms = float(statistics.mean(step_ms))
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = shape.B * shape.S
+    value = world * tokens / (ms / 1e3)
+
+    # ---------------- per-kernel times (eager, events around every launch)
+    prof = {}
+    for _ in range(3):
+        for kind, kms in pkg.tfl_profile_forward(m.handle, x.data_ptr(), lens.data_ptr(), int(shape.causal),
+                                                 out.data_ptr(), sp):
+            prof.setdefault(kind, []).append(kms)
+    per_kind = {k: (sum(v) / 3.0, len(v) // 3) for k, v in prof.items()}  # ms per forward, launches per forward
+    dom = max(per_kind, key=lambda k: per_kind[k][0])
+    dom_ms_launch = per_kind[dom][0] / per_kind[dom][1]
+    alg = algorithmic(shape, lens_np, shape.causal)
+    peaks = load_peaks()
+    if dom == "attention":
+        exps = alg["attn_exps_per_launch"]
+        achieved = exps / (dom_ms_launch / 1e3) / 1e9
+        peak = MUFU_PER_CLK_PER_SM * 152 * peaks["sm_max_mhz"] * 1e6 / 1e9
+        roof = {"kernel": "attention", "bound": "alu", "achieved": achieved, "peak": peak, "unit": "Gexp2/s",
+                "frac": achieved / peak, "traffic": None,
+                "note": "MUFU ex2 rate: 16/clk/SM x 152 SMs x max SM clock; per launch = causal pairs x heads",
+                "tensor_tflops": alg["attn_flops_per_launch"] / (dom_ms_launch / 1e3) / 1e12}
+    else:
+        by = kernel_bytes(dom, shape, alg["valid_tokens"])
+        achieved = by / (dom_ms_launch / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    roof["peak_source"] = peaks["source"]
+    roof["launch_ms"] = dom_ms_launch
+    roof["kernels_ms_per_forward"] = {k: round(v[0], 4) for k, v in per_kind.items()}
+
+    # ---------------- e2e through tfl_forward_host (pinned host buffers)
+    hx = torch.from_numpy(x_np).pin_memory()
+    hl = torch.from_numpy(lens_np).pin_memory()
+    ho = torch.empty_like(hx).pin_memory()
+    for _ in range(2):
+        pkg.tfl_forward_host(m.handle, hx.data_ptr(), hl.data_ptr(), int(shape.causal), ho.data_ptr(), sp)
+    e2e_t = []
+    for _ in range(max(3, min(args.steps, 10))):
+        t0 = time.perf_counter()
+        rc2 = pkg.tfl_forward_host(m.handle, hx.data_ptr(), hl.data_ptr(), int(shape.causal), ho.data_ptr(), sp)
+        e2e_t.append(time.perf_counter() - t0)
+        if rc2 != 0:
+            raise RuntimeError(f"e2e status {rc2}")
+    e2e_s = statistics.mean(e2e_t)
+    if pg:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(hx.numel() * 4 + hl.numel() * 4),
+           "d2h_bytes_per_step": int(ho.numel() * 4)}
+
+    launches = pkg.tfl_launch_count(m.handle, int(shape.causal)) * args.steps
+    m.close()
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        dt, tok = run_oracle_sample(shape, prm, seed, min(shape.B, args.ref_seqs))
+        cpu = {"value": tok / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{min(shape.B, args.ref_seqs)} of {shape.B} sequences ({tok} tokens), fp64 numpy"}
+
+    line = {
+        "metric": "forward_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic", "config": config_dict(shape), "roofline": roof, "cpu_baseline": cpu,
+        "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "algorithmic": {"valid_tokens": alg["valid_tokens"], "gflop": (alg["linear_flops"] + alg["attn_flops"]) / 1e9,
+                        "tflops_achieved": (alg["linear_flops"] + alg["attn_flops"]) / (ms / 1e3) / 1e12},
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

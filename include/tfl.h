@@ -1,0 +1,182 @@
+/*
+ * tfl.h -- C ABI of the GB300 (sm_103a) Transformer-stack forward.
+ *
+ * What it computes (the forward pass of a fixed L-layer Transformer block
+ * stack, "TikTok TechJam 2026 -- Problem 3: GPU Transformer Optimization",
+ * section 1.A and section 2):
+ *
+ *   h = x
+ *   for each layer l:
+ *     a = LN1_l(h)                                   (pre-LN, the default)
+ *     [q | k | v] = a [Wq; Wk; Wv]^T + [bq; bk; bv]  (fused QKV, section 2.2)
+ *     o = softmax(q k^T / sqrt(hd) + mask) v         (per head, section 2.1)
+ *     h = h + o Wo^T + bo ;  a2 = LN2_l(h)
+ *     h = h + GELU(a2 W1^T + b1) W2^T + b2           (exact erf GELU, 2.3)
+ *   out = LN_f(h), rows at padded positions set to 0 (section 1.A tail)
+ *
+ * mask: right-padded keys, key j of sequence b is valid iff j < len_b
+ * (section 2.1, "the mask trick"); with causal, key j is visible to query i
+ * iff j <= i, and the key mask is then redundant for every valid query.
+ * With norm_placement = 1 (post-LN): h = LN1(h + attn(h)),
+ * h = LN2(h + FFN(h)), out = LN_f(h) masked.
+ *
+ * Numerics: fp16 tensor-core operands with fp32 accumulation; residual
+ * stream, LayerNorm statistics and softmax in fp32 ("Transformerkernel",
+ * How we built it).  Output is fp32.
+ *
+ * Threading: a handle is not thread-safe; distinct handles are independent.
+ * All device pointers must belong to the device that was current when the
+ * handle was created.
+ */
+#ifndef TFL_H_
+#define TFL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  Every int-returning entry point returns one of these. */
+#define TFL_OK                   0
+#define TFL_ERR_INVALID_ARG     -1  /* null pointer, non-positive size, aliasing */
+#define TFL_ERR_UNSUPPORTED     -2  /* not sm_103, or a shape the kernels do not cover */
+#define TFL_ERR_OOM             -3  /* device allocation failed or exceeds max_workspace_bytes */
+#define TFL_ERR_CUDA            -4  /* a CUDA runtime call failed (see tfl_last_error) */
+#define TFL_ERR_DEVICE_TIMEOUT  -5  /* a kernel's bounded wait ran out; its outputs are invalid */
+#define TFL_ERR_BAD_LENGTHS     -6  /* a length was outside [0, S]; it was clamped */
+
+/* Opaque handle: packed weights, workspace, captured graphs. */
+typedef struct tfl_handle tfl_handle;
+
+/* A cudaStream_t passed as an opaque pointer (NULL = legacy default stream). */
+typedef void* tfl_stream;
+
+/*
+ * Shape of the stack (the dispatch key of "Shape-specialized Transformer
+ * Inference on Commodity GPUs", What it does: batch, seq_len, d_model,
+ * n_heads, d_ff, n_layers).
+ * Supported: B, S >= 1; d_model and d_ff multiples of 128; head_dim =
+ * d_model / n_heads in {32, 64, 256}; n_layers >= 1; B*S*max(3*d_model,
+ * d_ff) < 2^31.  norm_placement: 0 = pre-LN (default), 1 = post-LN.
+ */
+typedef struct {
+    int32_t B, S, d_model, n_heads, d_ff, n_layers;
+    int32_t norm_placement;
+} tfl_shape;
+
+/*
+ * One layer's parameters: float32, nn.Linear layout ([out, in], row-major,
+ * "in" contiguous).  wq, wk, wv, wo: [d_model, d_model]; w1: [d_ff, d_model];
+ * w2: [d_model, d_ff]; bq, bk, bv, bo, b2, ln*_g, ln*_b: [d_model]; b1: [d_ff].
+ * Pointers may be host or device memory (read once by tfl_create).
+ */
+typedef struct {
+    const float *wq, *bq, *wk, *bk, *wv, *bv, *wo, *bo;
+    const float *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+    const float *w1, *b1, *w2, *b2;
+} tfl_layer_weights;
+
+typedef struct {
+    const tfl_layer_weights* layers;   /* n_layers entries */
+    int32_t n_layers;                  /* must equal shape->n_layers */
+    const float *lnf_g, *lnf_b;        /* final LayerNorm, [d_model] */
+} tfl_weights;
+
+typedef struct {
+    int32_t precision;            /* 0 = fp16 operands, fp32 accumulate (only mode) */
+    float ln_eps;                 /* LayerNorm eps, default 1e-5 */
+    int64_t wait_timeout_ns;      /* bound on every device-side wait, default 2e9 */
+    int64_t max_workspace_bytes;  /* 0 = unlimited */
+    int32_t use_graph;            /* 1 (default): replay the forward as one CUDA graph */
+} tfl_options;
+
+/* Fill *opt with the defaults above.  Returns TFL_OK or TFL_ERR_INVALID_ARG. */
+int tfl_default_options(tfl_options* opt);
+
+/* Bytes of device workspace tfl_create will allocate for this shape (0 if invalid). */
+size_t tfl_workspace_bytes(const tfl_shape* shape);
+
+/*
+ * Validate the shape, check the current device is sm_103, allocate the
+ * workspace (one allocation), pack the weights to fp16 K-major (W_qkv =
+ * [Wq; Wk; Wv] rows, "TikTok TechJam 2026 -- Problem 3", section 2.2) and
+ * build the TMA descriptors.  The caller may free its weights afterwards.
+ * opt may be NULL (defaults).  On success *out owns all of that.
+ * Synchronous.  Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA.
+ */
+int tfl_create(const tfl_shape* shape, const tfl_weights* w,
+               const tfl_options* opt, tfl_handle** out);
+
+/*
+ * Run the forward on `stream`, asynchronously.
+ *   x:       device float32 [B, S, d_model], read only (padded rows are never read).
+ *   lengths: device int32 [B] or NULL (every sequence has length S); values
+ *            are clamped to [0, S] on the device, and an out-of-range value
+ *            makes the next tfl_status return TFL_ERR_BAD_LENGTHS.
+ *   causal:  0 or 1.
+ *   out:     device float32 [B, S, d_model], written in full (padded rows = 0);
+ *            must not overlap x.
+ * The first call for a given (causal, x, lengths, out) captures the launch
+ * sequence as a CUDA graph (not allowed while `stream` is itself capturing
+ * unless use_graph = 0); later calls replay it.
+ * Errors: INVALID_ARG, CUDA.  Device-side errors surface via tfl_status.
+ */
+int tfl_forward(tfl_handle* h, const float* x, const int32_t* lengths,
+                int causal, float* out, tfl_stream stream);
+
+/*
+ * The same forward from host buffers: copies x (and lengths, if not NULL)
+ * to handle-owned device buffers on `stream`, runs tfl_forward, copies out
+ * back and synchronizes `stream`.  Buffers may be pageable or pinned (pinned
+ * is faster).  Allocates its device buffers on the first call.
+ * Returns what tfl_status returns after the run.
+ */
+int tfl_forward_host(tfl_handle* h, const float* x_host, const int32_t* lengths_host,
+                     int causal, float* out_host, tfl_stream stream);
+
+/*
+ * Synchronize `stream` and read (then clear) the device status word.
+ * Returns TFL_OK, TFL_ERR_DEVICE_TIMEOUT or TFL_ERR_BAD_LENGTHS (timeout
+ * wins), or TFL_ERR_CUDA.
+ */
+int tfl_status(tfl_handle* h, tfl_stream stream);
+
+/* Free everything the handle owns.  Synchronizes the device.  NULL is a no-op. */
+void tfl_destroy(tfl_handle* h);
+
+/* Message of the last error on this thread ("" if none).  Valid until the next call. */
+const char* tfl_last_error(void);
+
+/*
+ * Eager forward (no graph) with a CUDA event around every launch, for
+ * profiling.  Writes up to `cap` entries: kernel_ms[i] = device time of
+ * launch i, kernel_kind[i] = TFL_KIND_* of that launch; *n = launches.
+ * Synchronizes `stream`.
+ */
+#define TFL_KIND_ROWNORM   1
+#define TFL_KIND_GEMM_QKV  2
+#define TFL_KIND_ATTENTION 3
+#define TFL_KIND_GEMM_OPROJ 4
+#define TFL_KIND_GEMM_FFN1 5
+#define TFL_KIND_GEMM_FFN2 6
+int tfl_profile_forward(tfl_handle* h, const float* x, const int32_t* lengths,
+                        int causal, float* out, tfl_stream stream,
+                        float* kernel_ms, int32_t* kernel_kind, int32_t cap, int32_t* n);
+
+/* Number of kernel launches one tfl_forward makes for this handle and causal flag. */
+int tfl_launch_count(const tfl_handle* h, int causal);
+
+/*
+ * Self-test of the device-side bounded wait: launches one block that waits
+ * on an mbarrier nothing will complete, with the given bound.  Returns
+ * TFL_ERR_DEVICE_TIMEOUT when the bound ran out as it should (the context
+ * stays usable), TFL_ERR_CUDA on a launch error.  Synchronizes `stream`.
+ */
+int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TFL_H_ */

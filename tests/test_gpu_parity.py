@@ -1,0 +1,79 @@
+"""GPU parity: the C-ABI forward against the fp64 oracle, element by element.
+
+Every case compares all B*S*D outputs (padded rows must be exactly zero)
+with the graded rule |u - r| <= 2e-3 or <= 0.02 |r|.  Shapes span several
+128-row tiles with a ragged tail (S not a multiple of 128), every supported
+head_dim (32, 64, 256), d_model 128 (fused LayerNorm epilogues) and 1024
+(separate row kernel), causal and key-padding masks, pre- and post-LN.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import assert_gate, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def case(B, S, D, H, F, L, causal, lens, seed=0, norm_placement=0, ln_affine="random", use_graph=True):
+    shape = synth.Shape(B, S, D, H, F, L, causal)
+    prm = synth.params(seed, shape, ln_affine=ln_affine)
+    x = synth.input_x(seed, shape)
+    lens = None if lens is None else np.asarray(lens, dtype=np.int32)
+    u, rc = run_gpu(shape, prm, x, lens, causal, norm_placement, use_graph=use_graph)
+    assert rc == 0
+    r = oracle.forward(prm, H, x, lens, causal, norm_placement)
+    if lens is not None:
+        for b in range(B):
+            assert np.all(u[b, lens[b]:] == 0.0), f"padded rows of sequence {b} not zero"
+    assert_gate(u, r, f"B{B} S{S} D{D} H{H} F{F} L{L} causal={causal} norm={norm_placement}")
+    return u, r
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_d128_hd32_ragged(causal):
+    case(3, 300, 128, 4, 512, 2, causal, [300, 17, 129])
+
+
+def test_d128_hd32_full_lengths_no_graph():
+    case(2, 256, 128, 4, 512, 2, True, None, use_graph=False)
+
+
+def test_d128_post_ln():
+    case(2, 200, 128, 4, 384, 2, True, [200, 90], norm_placement=1)
+
+
+def test_d128_hd64():
+    case(2, 260, 128, 2, 256, 1, True, [260, 131])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_d1024_hd256(causal):
+    case(2, 200, 1024, 4, 1024, 2, causal, [200, 70], seed=1)
+
+
+def test_d1024_hd64():
+    case(2, 300, 1024, 16, 512, 1, True, [300, 150], seed=2)
+
+
+def test_d1024_post_ln():
+    case(1, 160, 1024, 4, 512, 2, False, [100], seed=3, norm_placement=1)
+
+
+def test_edge_lengths_zero_and_one():
+    u, _ = case(4, 130, 128, 4, 256, 2, False, [0, 1, 130, 128])
+    assert np.all(u[0] == 0.0)
+
+
+def test_edge_single_token():
+    case(1, 1, 128, 4, 256, 1, True, None)
+
+
+def test_repeat_calls_are_deterministic():
+    shape = synth.Shape(2, 192, 128, 4, 512, 2, True)
+    prm = synth.params(5, shape)
+    x = synth.input_x(5, shape)
+    a, _ = run_gpu(shape, prm, x, [192, 100], True, repeat=1)
+    b, _ = run_gpu(shape, prm, x, [192, 100], True, repeat=3)
+    np.testing.assert_array_equal(a, b)
