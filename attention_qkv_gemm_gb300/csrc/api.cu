@@ -84,10 +84,17 @@ bool make_map_qkv(CUtensorMap* m, const void* base, uint64_t B, uint64_t S, uint
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// One packed weight matrix: fp16 hi (and lo) parts of W * 2^s, and the 2^-s the GEMM applies.
+struct PackedW {
+  __half* hi = nullptr;
+  __half* lo = nullptr;
+  float acc_scale = 1.f;
+  CUtensorMap tm_hi{}, tm_lo{};
+};
+
 struct LayerDev {
-  __half *wqkv, *wo, *w1, *w2;
+  PackedW wqkv, wo, w1, w2;
   float *bqkv, *bo, *b1, *b2, *ln1_g, *ln1_b, *ln2_g, *ln2_b;
-  CUtensorMap tm_wqkv, tm_wo, tm_w1, tm_w2;
 };
 
 struct GraphEntry {
@@ -99,10 +106,11 @@ struct GraphEntry {
 };
 
 struct WsLayout {
-  size_t h32, n16, qkv16, o16, g16, status, total;
+  size_t h32, n16, n16lo, qkv16, o16, g16, g16lo, status, sched, total;
 };
 
-WsLayout ws_layout(const tfl_shape& s) {
+// precision 2 adds the lo planes of the GEMM activations (normed rows, GELU output).
+WsLayout ws_layout(const tfl_shape& s, int precision) {
   const size_t M = (size_t)s.B * s.S, D = s.d_model, F = s.d_ff;
   WsLayout w{};
   size_t off = 0;
@@ -113,15 +121,20 @@ WsLayout ws_layout(const tfl_shape& s) {
   };
   w.h32 = take(M * D * 4);
   w.n16 = take(M * D * 2);
+  w.n16lo = precision == 2 ? take(M * D * 2) : 0;
   w.qkv16 = take(M * 3 * D * 2);
   w.o16 = take(M * D * 2);
   w.g16 = take(M * F * 2);
+  w.g16lo = precision == 2 ? take(M * F * 2) : 0;
   w.status = take(256);
+  w.sched = take((size_t)s.n_layers * sizeof(int));  // attention work counters, one per layer
   w.total = off;
   return w;
 }
 
-int gemm_bn(int N) { return N % 256 == 0 ? 256 : 128; }
+// Output tile width: 256 when N allows it, except with split activations (the
+// four operand tiles of a 256-wide stage leave room for only two stages).
+int gemm_bn(int N, int split_act) { return (N % 256 == 0 && !split_act) ? 256 : 128; }
 
 }  // namespace
 
@@ -137,8 +150,10 @@ struct tfl_handle {
   float *lnf_g = nullptr, *lnf_b = nullptr;
   float* h32 = nullptr;
   __half *n16 = nullptr, *qkv16 = nullptr, *o16 = nullptr, *g16 = nullptr;
+  __half *n16lo = nullptr, *g16lo = nullptr;  // precision 2 only
   int* status = nullptr;
-  CUtensorMap tm_n16{}, tm_o16{}, tm_g16{}, tm_q{}, tm_kv{};
+  int* sched = nullptr;
+  CUtensorMap tm_n16{}, tm_n16lo{}, tm_o16{}, tm_g16{}, tm_g16lo{}, tm_q{}, tm_kv{};
   std::vector<GraphEntry> graphs;
   float *hx_dev = nullptr, *hout_dev = nullptr;
   int* hlen_dev = nullptr;
@@ -171,10 +186,34 @@ int stage_f32(const float* src, size_t n, float* tmp, const char* name) {
   return TFL_OK;
 }
 
-int pack_f16(const float* src, size_t n, float* tmp, __half* dst, const char* name) {
-  int rc = stage_f32(src, n, tmp, name);
-  if (rc) return rc;
-  TFL_CUDA(launch_f32_to_f16(tmp, dst, n, 0), name);
+// Pack `count` float32 matrices (consecutive rows of one GEMM operand) into
+// hi (and lo) fp16 parts of W * 2^s, s chosen from the largest |w| so that
+// the lo parts sit well inside the normal fp16 range.
+int pack_weights(const float* const* src, const size_t* n, int count, float* tmp, unsigned* dmax, PackedW& w,
+                 bool split, const char* name) {
+  size_t off = 0, total = 0;
+  for (int i = 0; i < count; ++i) total += n[i];
+  (void)total;
+  TFL_CUDA(cudaMemset(dmax, 0, sizeof(unsigned)), name);
+  for (int i = 0; i < count; ++i) {
+    int rc = stage_f32(src[i], n[i], tmp + off, name);
+    if (rc) return rc;
+    TFL_CUDA(launch_absmax(tmp + off, n[i], dmax, 0), name);
+    off += n[i];
+  }
+  unsigned bits = 0;
+  TFL_CUDA(cudaMemcpy(&bits, dmax, sizeof(unsigned), cudaMemcpyDeviceToHost), name);
+  float amax;
+  std::memcpy(&amax, &bits, sizeof(float));
+  if (!std::isfinite(amax)) return fail(TFL_ERR_INVALID_ARG, std::string("non-finite value in weight ") + name);
+  int s = 0;
+  if (amax > 0.f) {
+    s = 4 - (int)std::ceil(std::log2((double)amax));  // largest |W * 2^s| in (8, 16]
+    s = s < -24 ? -24 : (s > 24 ? 24 : s);
+  }
+  const float scale = std::ldexp(1.0f, s);
+  w.acc_scale = std::ldexp(1.0f, -s);
+  TFL_CUDA(launch_split_f16(tmp, w.hi, split ? w.lo : nullptr, off, scale, 0), name);
   TFL_CUDA(cudaDeviceSynchronize(), name);
   return TFL_OK;
 }
@@ -205,6 +244,9 @@ cudaError_t rec_mark(const Rec& r, cudaStream_t s, int kind) {
 int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out, cudaStream_t st,
             const Rec& rec) {
   const bool pre = h->shape.norm_placement == 0;
+  const int prec = h->opt.precision;
+  const int ws = prec >= 1 ? 1 : 0;  // weights carry lo parts
+  const int as = prec == 2 ? 1 : 0;  // normed rows and GELU output carry lo planes
   Common c;
   c.M = h->M;
   c.S = h->shape.S;
@@ -213,7 +255,16 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
   c.timeout_ns = h->opt.wait_timeout_ns;
   const float eps = h->opt.ln_eps;
   const int D = h->D, F = h->F, L = h->L;
+  auto maps = [](const CUtensorMap& a, const CUtensorMap& alo, const PackedW& w) {
+    GemmMaps m;
+    m.a = a;
+    m.alo = alo;
+    m.b = w.tm_hi;
+    m.blo = w.tm_lo;
+    return m;
+  };
 
+  TFL_CUDA(cudaMemsetAsync(h->sched, 0, (size_t)L * sizeof(int), st), "work counter reset");
   TFL_CUDA(launch_check_lengths(lengths, h->shape.B, h->shape.S, h->status, st), "length check launch");
 
   TFL_CUDA(rec_mark(rec, st, 0), "event");
@@ -224,6 +275,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
     ra.in32 = x;
     ra.row.eps = eps;
     ra.row.n16 = h->n16;
+    ra.row.n16lo = h->n16lo;
     if (pre) {
       ra.row.flags = ROW_NORM16;
       ra.row.gb = h->layers[0].ln1_g;
@@ -238,15 +290,18 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
   for (int l = 0; l < L; ++l) {
     const LayerDev& ly = h->layers[l];
     const bool last = l == L - 1;
-    // QKV projection
+    // QKV projection: [q | k | v] = normed [Wq; Wk; Wv]^T + b
     {
       GemmArgs g;
       g.c = c;
       g.N = 3 * D;
       g.K = D;
+      g.acc_scale = ly.wqkv.acc_scale;
       g.bias = ly.bqkv;
       g.c16 = h->qkv16;
-      TFL_CUDA(launch_gemm(gemm_bn(3 * D), EPI_BIAS_F16, h->tm_n16, ly.tm_wqkv, g, h->num_sms, st), "qkv gemm");
+      TFL_CUDA(launch_gemm(gemm_bn(3 * D, as), EPI_BIAS_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.wqkv), g,
+                           h->num_sms, st),
+               "qkv gemm");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_QKV), "event");
     }
     // attention
@@ -259,21 +314,24 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       a.causal = causal;
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->hd));
       a.o16 = h->o16;
+      a.counter = h->sched + l;
       TFL_CUDA(launch_attention(h->hd, h->tm_q, h->tm_kv, a, h->num_sms, st), "attention");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_ATTENTION), "event");
     }
-    // o_proj + bias + residual (+ LayerNorm)
+    // o_proj + bias + residual (+ LayerNorm); the attention output has no lo plane
     {
       GemmArgs g;
       g.c = c;
       g.N = D;
       g.K = D;
+      g.acc_scale = ly.wo.acc_scale;
       g.bias = ly.bo;
       g.res = (l == 0) ? x : h->h32;
       RowOps ro;
       ro.eps = eps;
       ro.h32 = h->h32;
       ro.n16 = h->n16;
+      ro.n16lo = h->n16lo;
       if (pre) {
         ro.flags = ROW_NORM16;
         ro.gb = ly.ln2_g;
@@ -283,14 +341,15 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
         ro.ga = ly.ln1_g;
         ro.ba = ly.ln1_b;
       }
+      const GemmMaps mp = maps(h->tm_o16, h->tm_o16, ly.wo);
       if (D == 128) {
         ro.flags |= ROW_WRITE_H;
         g.row = ro;
-        TFL_CUDA(launch_gemm(128, EPI_BIAS_RES_ROW, h->tm_o16, ly.tm_wo, g, h->num_sms, st), "o_proj gemm");
+        TFL_CUDA(launch_gemm(128, EPI_BIAS_RES_ROW, 0, ws, mp, g, h->num_sms, st), "o_proj gemm");
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_OPROJ), "event");
       } else {
         g.h32 = h->h32;
-        TFL_CUDA(launch_gemm(gemm_bn(D), EPI_BIAS_RES_F32, h->tm_o16, ly.tm_wo, g, h->num_sms, st), "o_proj gemm");
+        TFL_CUDA(launch_gemm(gemm_bn(D, 0), EPI_BIAS_RES_F32, 0, ws, mp, g, h->num_sms, st), "o_proj gemm");
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_OPROJ), "event");
         RowArgs ra;
         ra.c = c;
@@ -307,9 +366,13 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       g.c = c;
       g.N = F;
       g.K = D;
+      g.acc_scale = ly.w1.acc_scale;
       g.bias = ly.b1;
       g.c16 = h->g16;
-      TFL_CUDA(launch_gemm(gemm_bn(F), EPI_BIAS_GELU_F16, h->tm_n16, ly.tm_w1, g, h->num_sms, st), "ffn1 gemm");
+      g.c16lo = h->g16lo;
+      TFL_CUDA(launch_gemm(gemm_bn(F, as), EPI_BIAS_GELU_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.w1), g,
+                           h->num_sms, st),
+               "ffn1 gemm");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN1), "event");
     }
     // FFN-out + bias + residual (+ next LayerNorm or the tail)
@@ -318,12 +381,14 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       g.c = c;
       g.N = D;
       g.K = F;
+      g.acc_scale = ly.w2.acc_scale;
       g.bias = ly.b2;
       g.res = h->h32;
       RowOps ro;
       ro.eps = eps;
       ro.h32 = h->h32;
       ro.n16 = h->n16;
+      ro.n16lo = h->n16lo;
       ro.out32 = out;
       if (!pre) {
         ro.flags |= ROW_POST_LN;
@@ -341,14 +406,15 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       } else {
         ro.flags |= ROW_WRITE_H | ROW_CAST16;
       }
+      const GemmMaps mp = maps(h->tm_g16, h->tm_g16lo, ly.w2);
       if (D == 128) {
         if (pre && !last) ro.flags |= ROW_WRITE_H;
         g.row = ro;
-        TFL_CUDA(launch_gemm(128, EPI_BIAS_RES_ROW, h->tm_g16, ly.tm_w2, g, h->num_sms, st), "ffn2 gemm");
+        TFL_CUDA(launch_gemm(128, EPI_BIAS_RES_ROW, as, ws, mp, g, h->num_sms, st), "ffn2 gemm");
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
       } else {
         g.h32 = h->h32;
-        TFL_CUDA(launch_gemm(gemm_bn(D), EPI_BIAS_RES_F32, h->tm_g16, ly.tm_w2, g, h->num_sms, st), "ffn2 gemm");
+        TFL_CUDA(launch_gemm(gemm_bn(D, as), EPI_BIAS_RES_F32, as, ws, mp, g, h->num_sms, st), "ffn2 gemm");
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
         RowArgs ra;
         ra.c = c;
@@ -369,7 +435,7 @@ extern "C" {
 
 int tfl_default_options(tfl_options* o) {
   if (!o) return fail(TFL_ERR_INVALID_ARG, "options is NULL");
-  o->precision = 0;
+  o->precision = 2;
   o->ln_eps = 1e-5f;
   o->wait_timeout_ns = 2000000000LL;
   o->max_workspace_bytes = 0;
@@ -379,7 +445,7 @@ int tfl_default_options(tfl_options* o) {
 
 size_t tfl_workspace_bytes(const tfl_shape* s) {
   if (check_shape(s) != TFL_OK) return 0;
-  return ws_layout(*s).total;
+  return ws_layout(*s, 2).total;
 }
 
 const char* tfl_last_error(void) { return g_err.c_str(); }
@@ -402,7 +468,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   tfl_options o;
   tfl_default_options(&o);
   if (opt) o = *opt;
-  if (o.precision != 0) return fail(TFL_ERR_UNSUPPORTED, "only precision 0 (fp16 operands) is implemented");
+  if (o.precision < 0 || o.precision > 2) return fail(TFL_ERR_INVALID_ARG, "precision must be 0, 1 or 2");
   if (!(o.ln_eps > 0.f)) return fail(TFL_ERR_INVALID_ARG, "ln_eps must be > 0");
   if (o.wait_timeout_ns <= 0) o.wait_timeout_ns = 2000000000LL;
 
@@ -418,9 +484,10 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   TFL_CUDA(prepare_attention_kernels(), "attention kernel attributes");
 
   const int D = shape->d_model, F = shape->d_ff, L = shape->n_layers;
-  const WsLayout lay = ws_layout(*shape);
-  // weights block: per layer 3D*D + D*D + F*D + D*F halves, 3D + D + F + D + 4D floats; + final LN
-  const size_t wl_half = (size_t)3 * D * D + (size_t)D * D + 2 * (size_t)F * D;
+  const WsLayout lay = ws_layout(*shape, o.precision);
+  const bool wsplit = o.precision >= 1;
+  // weights block: per layer (1 or 2) x (3D*D + D*D + F*D + D*F) halves, 3D + D + F + D + 4D floats; + final LN
+  const size_t wl_half = (wsplit ? 2 : 1) * ((size_t)3 * D * D + (size_t)D * D + 2 * (size_t)F * D);
   const size_t wl_float = (size_t)3 * D + D + F + D + 4 * (size_t)D;
   const size_t per_layer = align_up(wl_half * 2, 1024) + align_up(wl_float * 4, 1024);
   const size_t wbytes = per_layer * L + align_up((size_t)2 * D * 4, 1024);
@@ -464,23 +531,39 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   h->qkv16 = reinterpret_cast<__half*>(wsb + lay.qkv16);
   h->o16 = reinterpret_cast<__half*>(wsb + lay.o16);
   h->g16 = reinterpret_cast<__half*>(wsb + lay.g16);
+  if (o.precision == 2) {
+    h->n16lo = reinterpret_cast<__half*>(wsb + lay.n16lo);
+    h->g16lo = reinterpret_cast<__half*>(wsb + lay.g16lo);
+  }
   h->status = reinterpret_cast<int*>(wsb + lay.status);
+  h->sched = reinterpret_cast<int*>(wsb + lay.sched);
 
   float* tmp = nullptr;
-  if ((e = cudaMalloc(&tmp, (size_t)D * (F > 3 * D ? F : 3 * D) * sizeof(float))) != cudaSuccess) {
+  if ((e = cudaMalloc(&tmp, (size_t)D * (F > 3 * D ? F : 3 * D) * sizeof(float) + 256)) != cudaSuccess) {
     cudaGetLastError();
     return bail(fail(TFL_ERR_OOM, "staging allocation failed"));
   }
+  unsigned* dmax = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(tmp) +
+                                               (size_t)D * (F > 3 * D ? F : 3 * D) * sizeof(float));
   uint8_t* wp = static_cast<uint8_t*>(h->wmem);
   h->layers.resize(L);
   for (int l = 0; l < L && rc == TFL_OK; ++l) {
     const tfl_layer_weights& src = w->layers[l];
     LayerDev& d = h->layers[l];
     uint8_t* base = wp + per_layer * l;
-    d.wqkv = reinterpret_cast<__half*>(base);
-    d.wo = d.wqkv + (size_t)3 * D * D;
-    d.w1 = d.wo + (size_t)D * D;
-    d.w2 = d.w1 + (size_t)F * D;
+    __half* hp = reinterpret_cast<__half*>(base);
+    auto carve = [&](PackedW& pw, size_t n) {
+      pw.hi = hp;
+      hp += n;
+      if (wsplit) {
+        pw.lo = hp;
+        hp += n;
+      }
+    };
+    carve(d.wqkv, (size_t)3 * D * D);
+    carve(d.wo, (size_t)D * D);
+    carve(d.w1, (size_t)F * D);
+    carve(d.w2, (size_t)F * D);
     float* fb = reinterpret_cast<float*>(base + align_up(wl_half * 2, 1024));
     d.bqkv = fb;
     d.bo = d.bqkv + 3 * D;
@@ -490,13 +573,15 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
     d.ln1_b = d.ln1_g + D;
     d.ln2_g = d.ln1_b + D;
     d.ln2_b = d.ln2_g + D;
-    const size_t DD = (size_t)D * D;
-    if (!rc) rc = pack_f16(src.wq, DD, tmp, d.wqkv, "wq");
-    if (!rc) rc = pack_f16(src.wk, DD, tmp, d.wqkv + DD, "wk");
-    if (!rc) rc = pack_f16(src.wv, DD, tmp, d.wqkv + 2 * DD, "wv");
-    if (!rc) rc = pack_f16(src.wo, DD, tmp, d.wo, "wo");
-    if (!rc) rc = pack_f16(src.w1, (size_t)F * D, tmp, d.w1, "w1");
-    if (!rc) rc = pack_f16(src.w2, (size_t)F * D, tmp, d.w2, "w2");
+    const size_t DD = (size_t)D * D, FD = (size_t)F * D;
+    {
+      const float* qkv[3] = {src.wq, src.wk, src.wv};
+      const size_t nq[3] = {DD, DD, DD};
+      if (!rc) rc = pack_weights(qkv, nq, 3, tmp, dmax, d.wqkv, wsplit, "wq/wk/wv");
+    }
+    if (!rc) rc = pack_weights(&src.wo, &DD, 1, tmp, dmax, d.wo, wsplit, "wo");
+    if (!rc) rc = pack_weights(&src.w1, &FD, 1, tmp, dmax, d.w1, wsplit, "w1");
+    if (!rc) rc = pack_weights(&src.w2, &FD, 1, tmp, dmax, d.w2, wsplit, "w2");
     if (!rc) rc = copy_f32(src.bq, D, d.bqkv, "bq");
     if (!rc) rc = copy_f32(src.bk, D, d.bqkv + D, "bk");
     if (!rc) rc = copy_f32(src.bv, D, d.bqkv + 2 * D, "bv");
@@ -508,10 +593,15 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
     if (!rc) rc = copy_f32(src.ln2_g, D, d.ln2_g, "ln2_g");
     if (!rc) rc = copy_f32(src.ln2_b, D, d.ln2_b, "ln2_b");
     if (!rc) {
-      bool ok = make_map_2d(&d.tm_wqkv, d.wqkv, 3 * D, D, gemm_bn(3 * D)) &&
-                make_map_2d(&d.tm_wo, d.wo, D, D, D == 128 ? 128 : gemm_bn(D)) &&
-                make_map_2d(&d.tm_w1, d.w1, F, D, gemm_bn(F)) &&
-                make_map_2d(&d.tm_w2, d.w2, D, F, D == 128 ? 128 : gemm_bn(D));
+      auto maps = [&](PackedW& pw, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+        bool ok = make_map_2d(&pw.tm_hi, pw.hi, rows, cols, box_rows);
+        pw.tm_lo = pw.tm_hi;
+        if (ok && pw.lo) ok = make_map_2d(&pw.tm_lo, pw.lo, rows, cols, box_rows);
+        return ok;
+      };
+      const int aw = o.precision == 2;
+      bool ok = maps(d.wqkv, 3 * D, D, gemm_bn(3 * D, aw)) && maps(d.wo, D, D, D == 128 ? 128 : gemm_bn(D, 0)) &&
+                maps(d.w1, F, D, gemm_bn(F, aw)) && maps(d.w2, D, F, D == 128 ? 128 : gemm_bn(D, aw));
       if (!ok) rc = fail(TFL_ERR_CUDA, "weight tensor map encoding failed");
     }
   }
@@ -527,9 +617,13 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   const int atom = h->hd < 64 ? h->hd : 64;
   bool ok = make_map_2d(&h->tm_n16, h->n16, M, D, kGemmBM) && make_map_2d(&h->tm_o16, h->o16, M, D, kGemmBM) &&
             make_map_2d(&h->tm_g16, h->g16, M, F, kGemmBM) &&
+            (!h->n16lo || make_map_2d(&h->tm_n16lo, h->n16lo, M, D, kGemmBM)) &&
+            (!h->g16lo || make_map_2d(&h->tm_g16lo, h->g16lo, M, F, kGemmBM)) &&
             make_map_qkv(&h->tm_q, h->qkv16, shape->B, shape->S, 3 * D, atom, kAttnBM) &&
             make_map_qkv(&h->tm_kv, h->qkv16, shape->B, shape->S, 3 * D, atom, attn_block_n(h->hd));
   if (!ok) return bail(fail(TFL_ERR_CUDA, "activation tensor map encoding failed"));
+  if (!h->n16lo) h->tm_n16lo = h->tm_n16;
+  if (!h->g16lo) h->tm_g16lo = h->tm_g16;
   if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(cuda_fail(e, "create"));
   *out = h;
   return TFL_OK;

@@ -23,8 +23,15 @@
 //
 // Warp roles: warps 0-3 softmax + output (thread = query row), warp 4 TMA
 // producer (Q once per work item, K/V blocks into an NST-deep ring), warp 5
-// MMA issuer and TMEM owner.  Persistent CTAs walk the work items heaviest
-// first (causal: the last query blocks have the most keys).
+// MMA issuer and TMEM owner.  Persistent CTAs claim work items from a global
+// atomic counter, heaviest first (causal: the last query blocks have the most
+// keys); the producer publishes each claimed item to the other warps through
+// a small shared-memory ring.
+//
+// Softmax fast path: for key blocks after the first, P is computed in one
+// pass over S with the running max as the exponent reference while the block
+// max is tracked; only when a row's max grew by more than 2^8 does its warp
+// redo the block with the two-pass path (block max, rescale O, exponentials).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -45,7 +52,7 @@ struct AttnCfg {
   static constexpr int CTAS_PER_SM = HD == 32 ? 2 : 1;
   static constexpr int O_COL = HD <= 64 ? 128 : 256;
   static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
-  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)NST * 2 * KV_BYTES + P_BYTES + 256;
+  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)NST * 2 * KV_BYTES + P_BYTES + 384;
 };
 
 size_t attn_smem_bytes(int hd) {
@@ -60,6 +67,8 @@ size_t attn_smem_bytes(int hd) {
 struct Item {
   int b, h, qb, len, nkb;
 };
+
+constexpr int kItemRing = 4;
 
 // Work item i (heaviest first) -> (b, h, query block); false if the block is all padding.
 __device__ __forceinline__ bool decode_item(int i, const AttnArgs& a, int nqb, int bn, Item& it) {
@@ -97,7 +106,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   uint64_t* drain = bars + 6;
   uint64_t* kv_full = bars + 7;
   uint64_t* kv_empty = kv_full + C::NST;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kv_empty + C::NST);
+  uint64_t* it_full = kv_empty + C::NST;
+  uint64_t* it_empty = it_full + kItemRing;
+  int* it_slot = reinterpret_cast<int*>(it_empty + kItemRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(it_slot + kItemRing);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* never_flag = abort_flag + 1;
 
@@ -113,6 +125,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(&it_full[s], 1);
+      mbar_init(&it_empty[s], 5);  // the MMA warp and the four softmax warps
     }
     *abort_flag = 0;
     *never_flag = 0;
@@ -139,14 +155,27 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   bool mma_issued = false;
 
   if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer + scheduler
     if (lane == 0) {
-      int st = 0;
-      uint32_t kvph = 0, qph = 0;
+      int st = 0, ik = 0;
+      uint32_t kvph = 0, qph = 0, itph = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+      while (ok) {
+        // claim the next work item that holds a valid query (heaviest first)
+        int i;
         Item it;
-        if (!decode_item(i, args, nqb, BN, it)) continue;
+        do {
+          i = atomicAdd(args.counter, 1);
+        } while (i < items && !decode_item(i, args, nqb, BN, it));
+        if (i >= items) i = -1;
+        if (!wait_bounded(&it_empty[ik], itph ^ 1u, wc)) break;
+        it_slot[ik] = i;
+        mbar_arrive(&it_full[ik]);
+        if (++ik == kItemRing) {
+          ik = 0;
+          itph ^= 1u;
+        }
+        if (i < 0) break;
         if (!wait_bounded(q_empty, qph ^ 1u, wc)) break;
         mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
@@ -184,8 +213,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     constexpr uint32_t idesc_pv = idesc_f16(128, HD, 0, 1);
     const uint32_t d_s = tmem_base;
     const uint32_t d_o = tmem_base + C::O_COL;
-    int st = 0;
-    uint32_t kvph = 0, qph = 0, pph = 0, oeph = 0;
+    int st = 0, ik = 0;
+    uint32_t kvph = 0, qph = 0, pph = 0, oeph = 0, itph = 0;
     bool first_item = true, ok = true;
     auto issue_pv = [&](int pst, bool accumulate) {
       const uint32_t sp = smem_u32(sP), sv = smem_u32(sV + (size_t)pst * C::KV_BYTES);
@@ -196,9 +225,18 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         umma_f16(d_o, ad, bd, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
       }
     };
-    for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+    while (ok) {
+      if (!wait_bounded(&it_full[ik], itph, wc)) break;
+      const int i = it_slot[ik];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[ik]);
+      if (++ik == kItemRing) {
+        ik = 0;
+        itph ^= 1u;
+      }
+      if (i < 0) break;
       Item it;
-      if (!decode_item(i, args, nqb, BN, it)) continue;
+      decode_item(i, args, nqb, BN, it);
       if (!wait_bounded(q_full, qph, wc)) break;
       qph ^= 1u;
       tc_fence_after();
@@ -288,12 +326,51 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     const uint32_t t_s = tmem_base + ((uint32_t)(warp * 32) << 16);
     const uint32_t t_o = t_s + C::O_COL;
     const float sl2 = args.scale_log2;
-    uint32_t sph = 0, oph = 0;
+    uint32_t sph = 0, oph = 0, itph = 0;
+    int ik = 0;
     uint8_t* prow = sP + r * 128;
     const uint32_t swz = (uint32_t)(r & 7);
-    for (int i = blockIdx.x; i < items; i += gridDim.x) {
+
+    // exponentials of one 64-key group against reference mref, into the P tile;
+    // returns the group's sum in four partials and its max (masked keys skipped)
+    auto exp_group = [&](const float* sv, int g, int k0, bool need_mask, int kmax, float mref, float* ls,
+                         float* bm) {
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int idx = c8 * 8 + e;
+          const float v = sv[idx];
+          const bool ok2 = !need_mask || (k0 + g * 64 + idx <= kmax);
+          bm[e & 3] = ok2 ? fmaxf(bm[e & 3], v) : bm[e & 3];
+          const float pe = ex2(fmaf(v, sl2, -mref));
+          p[e] = ok2 ? pe : 0.f;
+          ls[e & 3] += p[e];
+        }
+        uint4 u;
+        __half2 h0 = __floats2half2_rn(p[0], p[1]), h1 = __floats2half2_rn(p[2], p[3]);
+        __half2 h2 = __floats2half2_rn(p[4], p[5]), h3 = __floats2half2_rn(p[6], p[7]);
+        u.x = *reinterpret_cast<uint32_t*>(&h0);
+        u.y = *reinterpret_cast<uint32_t*>(&h1);
+        u.z = *reinterpret_cast<uint32_t*>(&h2);
+        u.w = *reinterpret_cast<uint32_t*>(&h3);
+        *reinterpret_cast<uint4*>(prow + g * (kAttnBM * 128) + (((uint32_t)c8 ^ swz) << 4)) = u;
+      }
+    };
+
+    while (true) {
+      if (!wait_bounded(&it_full[ik], itph, wc)) break;
+      const int i = it_slot[ik];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[ik]);
+      if (++ik == kItemRing) {
+        ik = 0;
+        itph ^= 1u;
+      }
+      if (i < 0) break;
       Item it;
-      if (!decode_item(i, args, nqb, BN, it)) continue;
+      decode_item(i, args, nqb, BN, it);
       const int qpos = it.qb * kAttnBM + r;
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
@@ -307,72 +384,71 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         const int k0 = j * BN;
         const bool need_mask = args.causal ? (k0 + BN - 1 > it.qb * kAttnBM) : (k0 + BN > it.len);
         const int kmax = args.causal ? qpos : it.len - 1;  // last allowed key when masking
-        // pass 1: row max of the raw scores
-        float mx = -INFINITY;
+        bool slow = (j == 0);
+        if (!slow) {
+          // fast path: exponentials against the running max, block max tracked alongside
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          float bm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float s[32];
-          tmem_ld32(t_s + c * 32, s);
-          tmem_wait_ld();
-          if (need_mask) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (k0 + c * 32 + e <= kmax) mx = fmaxf(mx, s[e]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, s[e]);
+          for (int g = 0; g < BN / 64; ++g) {
+            float sv[64];
+            tmem_ld32(t_s + g * 64, sv);
+            tmem_ld32(t_s + g * 64 + 32, sv + 32);
+            tmem_wait_ld();
+            exp_group(sv, g, k0, need_mask, kmax, m_run, ls, bm);
           }
+          const float bmax = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
+          slow = __any_sync(0xffffffffu, bmax * sl2 > m_run + 8.0f);
+          if (!slow) l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
-        const float m_new = fmaxf(m_run, mx * sl2);
-        const bool resc = m_new > m_run + 8.0f;
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O holds PV of every earlier block (s_full(j) was committed after PV(j-1)).
-          const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
-#pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            float o[32];
-            tmem_ld32(t_o + c * 32, o);
+        if (slow) {
+          // pass 1: block max
+          float bm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int g = 0; g < BN / 64; ++g) {
+            float sv[64];
+            tmem_ld32(t_s + g * 64, sv);
+            tmem_ld32(t_s + g * 64 + 32, sv + 32);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(t_o + c * 32, o);
+            for (int e = 0; e < 64; ++e) {
+              const bool ok2 = !need_mask || (k0 + g * 64 + e <= kmax);
+              bm[e & 3] = ok2 ? fmaxf(bm[e & 3], sv[e]) : bm[e & 3];
+            }
           }
-          tmem_wait_st();
-          l_run *= alpha;
+          const float bmax = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
+          const float m_new = fmaxf(m_run, bmax * sl2);
+          const bool resc = m_new > m_run + 8.0f;
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+            // O holds PV of every earlier block (s_full(j) was committed after PV(j-1)).
+            const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+              float o[32];
+              tmem_ld32(t_o + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tmem_st32(t_o + c * 32, o);
+            }
+            tmem_wait_st();
+            l_run *= alpha;
+          }
+          if (resc) m_run = m_new;
+          const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+          // pass 2: exponentials
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          float bm2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int g = 0; g < BN / 64; ++g) {
+            float sv[64];
+            tmem_ld32(t_s + g * 64, sv);
+            tmem_ld32(t_s + g * 64 + 32, sv + 32);
+            tmem_wait_ld();
+            exp_group(sv, g, k0, need_mask, kmax, mref, ls, bm2);
+          }
+          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
-        if (resc) m_run = m_new;
-        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-        // pass 2: P = exp2(s * scale_log2 - m), fp16, into the swizzled P tile
-        float lsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float s[32];
-          tmem_ld32(t_s + c * 32, s);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float p = ex2(fmaf(s[e], sl2, -mref));
-            if (need_mask && (k0 + c * 32 + e > kmax)) p = 0.f;
-            s[e] = p;
-            lsum += p;
-          }
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int key = c * 32 + g * 8;  // first of 8 keys in this 16-byte chunk
-            const uint32_t chunk = (uint32_t)((key & 63) >> 3);
-            __half2 h0 = __floats2half2_rn(s[g * 8 + 0], s[g * 8 + 1]);
-            __half2 h1 = __floats2half2_rn(s[g * 8 + 2], s[g * 8 + 3]);
-            __half2 h2 = __floats2half2_rn(s[g * 8 + 4], s[g * 8 + 5]);
-            __half2 h3 = __floats2half2_rn(s[g * 8 + 6], s[g * 8 + 7]);
-            uint4 u;
-            u.x = *reinterpret_cast<uint32_t*>(&h0);
-            u.y = *reinterpret_cast<uint32_t*>(&h1);
-            u.z = *reinterpret_cast<uint32_t*>(&h2);
-            u.w = *reinterpret_cast<uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(prow + (key >> 6) * (kAttnBM * 128) + ((chunk ^ swz) << 4)) = u;
-          }
-        }
-        l_run += lsum;
         fence_async_smem();
         tc_fence_before();
         __syncwarp();

@@ -1,90 +1,123 @@
-// gemm.cu -- persistent tcgen05 GEMM with fused epilogues.
+// gemm.cu -- persistent tcgen05 GEMM with fused epilogues and split-fp16 operands.
 //
-// C[M, N] = A[M, K] * W[N, K]^T with fp16 operands and fp32 accumulation in
-// tensor memory ("TikTok TechJam 2026 -- Problem 3", section 2.3: fp16
-// tensor cores, fp32 accumulate, one rounding at the store).  The four
-// epilogues fuse the row-wise work of the forward into the GEMM that
-// produces it (section 1.A: add_layernorm_cast, bias_gelu_cast,
-// post_attn_chain_tail):
-//   EPI_BIAS_F16       QKV projection: c16 = acc + b_qkv (fused QKV, section 2.2)
-//   EPI_BIAS_GELU_F16  FFN-in: c16 = GELU_erf(acc + b1)
-//   EPI_BIAS_RES_F32   o_proj / FFN-out when d_model > 128: h = acc + b + h
-//   EPI_BIAS_RES_ROW   o_proj / FFN-out when d_model == 128: residual add plus
-//                      row LayerNorm(s) in fp32, fp16 normed output or the
-//                      model tail (final LayerNorm + pad-mask, fp32 out).
+// C[M, N] = A[M, K] * W[N, K]^T on fp16 tensor cores with fp32 accumulation
+// in tensor memory ("TikTok TechJam 2026 -- Problem 3", section 2.3: fp16
+// operands, fp32 accumulate, one rounding at the store).
+//
+// Precision.  One fp16 rounding of every operand is too coarse for the
+// graded rule over many seeds ("Transformerkernel", Challenges: a d=32 case
+// failed at 0.00208 and the B=10000 case at 0.002074 over 25 trials), so
+// operands can be carried as two fp16 terms, x = hi + lo with
+// lo = fp16(x - hi):
+//   WS  weights split: W * 2^s = W_hi + W_lo (s per matrix keeps W_lo out of
+//       the fp16 subnormal range; the epilogue multiplies by 2^-s, exactly).
+//   AS  activations split: A = A_hi + A_lo, two fp16 planes in HBM written by
+//       the producing kernel.
+// Per 16-wide k-step the MMAs A_hi*W_hi (+ A_lo*W_hi) (+ A_hi*W_lo) all
+// accumulate into the same fp32 accumulator; A_lo*W_lo (~2^-22) is dropped.
+//
+// Epilogues (the row-wise work of section 1.A fused into the GEMM):
+//   EPI_BIAS_F16       QKV projection: c16 = acc + b_qkv
+//   EPI_BIAS_GELU_F16  FFN-in: c16 = GELU_erf(acc + b1) (hi [+ lo] planes)
+//   EPI_BIAS_RES_F32   o_proj / FFN-out when d_model > 128: h = acc + b + res
+//   EPI_BIAS_RES_ROW   o_proj / FFN-out when d_model == 128: residual add and
+//                      fp32 row LayerNorm(s): normed fp16 (hi [+ lo]) for the
+//                      next sublayer, or the model tail (final LN + mask).
 //
 // Structure (one CTA per SM, persistent over 128 x BN output tiles):
-//   warp 0  TMA producer: A and W k-blocks (64 fp16 = 128 B, 128B swizzle)
-//           into a STAGES-deep shared-memory ring.
-//   warp 1  MMA issuer: 4 tcgen05.mma (K = 16 each) per k-block into one of
-//           two TMEM accumulators (double-buffered so the epilogue of tile t
-//           overlaps the MMAs of tile t+1).
-//   warps 2-5 epilogue: thread = output row (TMEM lane), tcgen05.ld of 32
-//           columns at a time, fused math, vectorised global stores.
-// Tiles whose 128 rows are all padding (s >= len_b) are skipped entirely;
-// the model-tail epilogue writes their zeros without waiting for an MMA.
+//   warp 0     TMA producer: k-blocks of 64 (128 B rows, 128B swizzle) of
+//              A_hi [A_lo] W_hi [W_lo] into a STAGES-deep ring.
+//   warp 1     MMA issuer and TMEM owner; two accumulators so the epilogue
+//              of tile t overlaps the MMAs of tile t+1.
+//   warps 2-9  epilogue: two warps per TMEM lane quarter (thread = output
+//              row), each covering half of the tile's columns.
+// Tiles whose 128 rows are all padding are skipped; the model-tail epilogue
+// writes their zeros without waiting for an MMA.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace tfl {
 
-template <int BN>
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+
+template <int BN, int AS, int WS>
 struct GemmCfg {
   static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;
   static constexpr int B_BYTES = BN * kGemmBK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196 * 1024) / STAGE > 8 ? 8 : (196 * 1024) / STAGE;
+  static constexpr int STAGE = A_BYTES * (1 + AS) + B_BYTES * (1 + WS);
+  static constexpr int STAGES = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
   static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + 256;
+  static constexpr int RED_BYTES = 4 * 2 * kGemmBM * 4;  // row-statistics exchange (EPI_BIAS_RES_ROW)
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + RED_BYTES + 256;
 };
-
-size_t gemm_smem_bytes(int bn) {
-  return bn == 256 ? GemmCfg<256>::SMEM : GemmCfg<128>::SMEM;
-}
 
 __device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.7071067811865476f)); }
 
-__device__ __forceinline__ void store_f16x32(__half* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Store 32 values as fp16 (and, when lo != nullptr, their rounding residuals as a second plane).
+__device__ __forceinline__ void store_f16x32(__half* hi, __half* lo, const float* v) {
+  uint4* dh = reinterpret_cast<uint4*>(hi);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    __half2 h0 = __floats2half2_rn(v[8 * i + 0], v[8 * i + 1]);
-    __half2 h1 = __floats2half2_rn(v[8 * i + 2], v[8 * i + 3]);
-    __half2 h2 = __floats2half2_rn(v[8 * i + 4], v[8 * i + 5]);
-    __half2 h3 = __floats2half2_rn(v[8 * i + 6], v[8 * i + 7]);
     uint4 u;
-    u.x = *reinterpret_cast<uint32_t*>(&h0);
-    u.y = *reinterpret_cast<uint32_t*>(&h1);
-    u.z = *reinterpret_cast<uint32_t*>(&h2);
-    u.w = *reinterpret_cast<uint32_t*>(&h3);
-    d[i] = u;
+    u.x = pack_h2(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_h2(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_h2(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_h2(v[8 * i + 6], v[8 * i + 7]);
+    dh[i] = u;
+    if (lo != nullptr) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 hh = *reinterpret_cast<const __half2*>(&w[k]);
+        const float2 f = __half22float2(hh);
+        r[k] = pack_h2(v[8 * i + 2 * k] - f.x, v[8 * i + 2 * k + 1] - f.y);
+      }
+      reinterpret_cast<uint4*>(lo)[i] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
   }
 }
 
-// LayerNorm of a thread-owned row of N values in registers: returns mean and rstd.
-template <int N>
-__device__ __forceinline__ void row_stats(const float* t, float eps, float& mean, float& rstd) {
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+
+// Row mean / rstd of a row split over the two epilogue warps of a lane quarter.
+template <int NH>
+__device__ __forceinline__ void row_stats_split(const float* t, float eps, float* red, int slot, int half, int r,
+                                                float& mean, float& rstd) {
+  constexpr float invN = 1.0f / (2 * NH);
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < N; ++i) s += t[i];
-  mean = s * (1.0f / N);
+  for (int i = 0; i < NH; ++i) s += t[i];
+  red[(slot * 2 + half) * kGemmBM + r] = s;
+  epi_bar();
+  mean = (red[(slot * 2 + 0) * kGemmBM + r] + red[(slot * 2 + 1) * kGemmBM + r]) * invN;
   float q = 0.f;
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
+  for (int i = 0; i < NH; ++i) {
     const float d = t[i] - mean;
     q = fmaf(d, d, q);
   }
-  rstd = rsqrtf(q * (1.0f / N) + eps);
+  red[((slot + 1) * 2 + half) * kGemmBM + r] = q;
+  epi_bar();
+  rstd = rsqrtf((red[((slot + 1) * 2 + 0) * kGemmBM + r] + red[((slot + 1) * 2 + 1) * kGemmBM + r]) * invN + eps);
 }
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+template <int BN, int EPI, int AS, int WS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAlo,
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBlo,
                 const GemmArgs args) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, AS, WS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)C::STAGES * C::STAGE);
+  float* red = reinterpret_cast<float*>(smem + (size_t)C::STAGES * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)C::STAGES * C::STAGE + C::RED_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* accf = empty + C::STAGES;
   uint64_t* acce = accf + 2;
@@ -101,7 +134,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf[a], 1);
-      mbar_init(&acce[a], 4);
+      mbar_init(&acce[a], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -111,6 +144,8 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (AS) tma_prefetch_desc(&tmAlo);
+    if (WS) tma_prefetch_desc(&tmBlo);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
@@ -124,8 +159,7 @@ __global__ void __launch_bounds__(192, 1)
   const int num_m = (M + kGemmBM - 1) / kGemmBM, num_n = args.N / BN, num_k = args.K / kGemmBK;
   const int total = num_m * num_n;
 
-  // Producer bookkeeping for the abort path: last parity issued per stage.
-  uint32_t issued_mask = 0, issued_par = 0;
+  uint32_t issued_mask = 0, issued_par = 0;  // producer: stages with loads in flight (abort path)
   bool mma_issued = false;
 
   if (warp == 0) {
@@ -144,7 +178,10 @@ __global__ void __launch_bounds__(192, 1)
           uint8_t* sa = smem + (size_t)stage * C::STAGE;
           mbar_arrive_expect_tx(&full[stage], C::STAGE);
           tma_load_2d(sa, &tmA, &full[stage], kb * kGemmBK, mb * kGemmBM);
-          tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kb * kGemmBK, nb * BN);
+          if (AS) tma_load_2d(sa + C::A_BYTES, &tmAlo, &full[stage], kb * kGemmBK, mb * kGemmBM);
+          uint8_t* sb = sa + C::A_BYTES * (1 + AS);
+          tma_load_2d(sb, &tmB, &full[stage], kb * kGemmBK, nb * BN);
+          if (WS) tma_load_2d(sb + C::B_BYTES, &tmBlo, &full[stage], kb * kGemmBK, nb * BN);
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == C::STAGES) {
@@ -173,11 +210,16 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)stage * C::STAGE);
-          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t sal = sa + C::A_BYTES;
+          const uint32_t sb = sa + C::A_BYTES * (1 + AS);
+          const uint32_t sbl = sb + C::B_BYTES;
 #pragma unroll
           for (int k = 0; k < kGemmBK / 16; ++k) {
-            umma_f16(d, sdesc(sa + k * 32, 16, 1024, kSw128), sdesc(sb + k * 32, 16, 1024, kSw128), idesc,
-                     (kb | k) != 0);
+            const uint64_t ah = sdesc(sa + k * 32, 16, 1024, kSw128);
+            const uint64_t bh = sdesc(sb + k * 32, 16, 1024, kSw128);
+            umma_f16(d, ah, bh, idesc, (kb | k) != 0);
+            if (AS) umma_f16(d, sdesc(sal + k * 32, 16, 1024, kSw128), bh, idesc, 1u);
+            if (WS) umma_f16(d, ah, sdesc(sbl + k * 32, 16, 1024, kSw128), idesc, 1u);
           }
           mma_issued = true;
           umma_commit(&empty[stage]);
@@ -195,9 +237,14 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ------------------------------------------------------------ epilogue (8 warps)
+    constexpr int NH = BN / 2;  // columns per epilogue warp
+    const int q = warp & 3;     // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
+    const float sc = args.acc_scale;
+    WaitCtl ewc = wc;
+    ewc.early_exit = false;  // the epilogue warps meet at a named barrier: leave only on their own bound
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -206,123 +253,139 @@ __global__ void __launch_bounds__(192, 1)
       if (!rows_live(mb * kGemmBM, min(mb * kGemmBM + kGemmBM, M), S, lengths)) {
         if constexpr (EPI == EPI_BIAS_RES_ROW) {
           if ((args.row.flags & ROW_FINAL) && m < M) {
-            float4* o = reinterpret_cast<float4*>(args.row.out32 + (size_t)m * BN);
+            float4* o = reinterpret_cast<float4*>(args.row.out32 + (size_t)m * BN + half * NH);
 #pragma unroll
-            for (int i = 0; i < BN / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < NH / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
         continue;
       }
-      if (!wait_bounded(&accf[acc], acc_phase, wc)) break;
+      if (!wait_bounded(&accf[acc], acc_phase, ewc)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * NH);
       const bool in_range = m < M;
 
       if constexpr (EPI == EPI_BIAS_F16 || EPI == EPI_BIAS_GELU_F16 || EPI == EPI_BIAS_RES_F32) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tb + c * 32, v);
-          tmem_wait_ld();
-          const int n0 = nb * BN + c * 32;
-          if (in_range) {
-            const float4* bp = reinterpret_cast<const float4*>(args.bias + n0);
+        float v[NH];
+#pragma unroll
+        for (int c = 0; c < NH / 32; ++c) tmem_ld32(tb + c * 32, v + c * 32);
+        tmem_wait_ld();
+        if (in_range) {
+          const int n0 = nb * BN + half * NH;
+          const bool valid = (EPI == EPI_BIAS_RES_F32) && row_valid(m, S, lengths);
+#pragma unroll
+          for (int c = 0; c < NH / 32; ++c) {
+            float* w = v + c * 32;
+            const float4* bp = reinterpret_cast<const float4*>(args.bias + n0 + c * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 b4 = __ldg(bp + i);
-              v[4 * i + 0] += b4.x;
-              v[4 * i + 1] += b4.y;
-              v[4 * i + 2] += b4.z;
-              v[4 * i + 3] += b4.w;
+              w[4 * i + 0] = fmaf(w[4 * i + 0], sc, b4.x);
+              w[4 * i + 1] = fmaf(w[4 * i + 1], sc, b4.y);
+              w[4 * i + 2] = fmaf(w[4 * i + 2], sc, b4.z);
+              w[4 * i + 3] = fmaf(w[4 * i + 3], sc, b4.w);
             }
             if constexpr (EPI == EPI_BIAS_GELU_F16) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+              for (int i = 0; i < 32; ++i) w[i] = gelu_erf(w[i]);
             }
             if constexpr (EPI == EPI_BIAS_RES_F32) {
-              float4* hp = reinterpret_cast<float4*>(args.h32 + (size_t)m * args.N + n0);
-              if (row_valid(m, S, lengths)) {
-                const float4* rp = reinterpret_cast<const float4*>(args.res + (size_t)m * args.N + n0);
+              const size_t off = (size_t)m * args.N + n0 + c * 32;
+              if (valid) {
+                const float4* rp = reinterpret_cast<const float4*>(args.res + off);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   const float4 r4 = rp[i];
-                  v[4 * i + 0] += r4.x;
-                  v[4 * i + 1] += r4.y;
-                  v[4 * i + 2] += r4.z;
-                  v[4 * i + 3] += r4.w;
+                  w[4 * i + 0] += r4.x;
+                  w[4 * i + 1] += r4.y;
+                  w[4 * i + 2] += r4.z;
+                  w[4 * i + 3] += r4.w;
                 }
               }
+              float4* hp = reinterpret_cast<float4*>(args.h32 + off);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) hp[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              for (int i = 0; i < 8; ++i) hp[i] = make_float4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
             } else {
-              store_f16x32(args.c16 + (size_t)m * args.N + n0, v);
+              const size_t off = (size_t)m * args.N + n0 + c * 32;
+              store_f16x32(args.c16 + off, args.c16lo ? args.c16lo + off : nullptr, w);
             }
           }
         }
       } else {
-        // EPI_BIAS_RES_ROW: the whole row (BN == N == d_model) is in this thread.
-        float t[BN];
+        // EPI_BIAS_RES_ROW: BN == N == d_model; this thread owns half of row m.
+        float t[NH];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tb + c * 32, t + c * 32);
+        for (int c = 0; c < NH / 32; ++c) tmem_ld32(tb + c * 32, t + c * 32);
         tmem_wait_ld();
-        if (in_range) {
-          const RowOps& ro = args.row;
-          const bool valid = row_valid(m, S, lengths);
-          const float4* bp = reinterpret_cast<const float4*>(args.bias);
+        const RowOps& ro = args.row;
+        const bool valid = in_range && row_valid(m, S, lengths);
+        const int c0 = half * NH;
+        {
+          const float4* bp = reinterpret_cast<const float4*>(args.bias + c0);
 #pragma unroll
-          for (int i = 0; i < BN / 4; ++i) {
+          for (int i = 0; i < NH / 4; ++i) {
             const float4 b4 = __ldg(bp + i);
-            t[4 * i + 0] += b4.x;
-            t[4 * i + 1] += b4.y;
-            t[4 * i + 2] += b4.z;
-            t[4 * i + 3] += b4.w;
+            t[4 * i + 0] = fmaf(t[4 * i + 0], sc, b4.x);
+            t[4 * i + 1] = fmaf(t[4 * i + 1], sc, b4.y);
+            t[4 * i + 2] = fmaf(t[4 * i + 2], sc, b4.z);
+            t[4 * i + 3] = fmaf(t[4 * i + 3], sc, b4.w);
           }
-          if (valid) {
-            const float4* rp = reinterpret_cast<const float4*>(args.res + (size_t)m * BN);
+        }
+        if (valid) {
+          const float4* rp = reinterpret_cast<const float4*>(args.res + (size_t)m * BN + c0);
 #pragma unroll
-            for (int i = 0; i < BN / 4; ++i) {
-              const float4 r4 = rp[i];
-              t[4 * i + 0] += r4.x;
-              t[4 * i + 1] += r4.y;
-              t[4 * i + 2] += r4.z;
-              t[4 * i + 3] += r4.w;
-            }
+          for (int i = 0; i < NH / 4; ++i) {
+            const float4 r4 = rp[i];
+            t[4 * i + 0] += r4.x;
+            t[4 * i + 1] += r4.y;
+            t[4 * i + 2] += r4.z;
+            t[4 * i + 3] += r4.w;
           }
-          float mean, rstd;
-          if (ro.flags & ROW_POST_LN) {
-            row_stats<BN>(t, ro.eps, mean, rstd);
+        }
+        float mean, rstd;
+        int slot = 0;
+        if (ro.flags & ROW_POST_LN) {
+          row_stats_split<NH>(t, ro.eps, red, slot, half, r, mean, rstd);
+          slot += 2;
 #pragma unroll
-            for (int i = 0; i < BN; ++i) t[i] = (t[i] - mean) * rstd * __ldg(ro.ga + i) + __ldg(ro.ba + i);
-          }
-          if (ro.flags & ROW_WRITE_H) {
-            float4* hp = reinterpret_cast<float4*>(ro.h32 + (size_t)m * BN);
+          for (int i = 0; i < NH; ++i) t[i] = (t[i] - mean) * rstd * __ldg(ro.ga + c0 + i) + __ldg(ro.ba + c0 + i);
+        }
+        if ((ro.flags & ROW_WRITE_H) && in_range) {
+          float4* hp = reinterpret_cast<float4*>(ro.h32 + (size_t)m * BN + c0);
 #pragma unroll
-            for (int i = 0; i < BN / 4; ++i) hp[i] = make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
-          }
-          if (ro.flags & (ROW_FINAL | ROW_NORM16)) {
-            row_stats<BN>(t, ro.eps, mean, rstd);
-            const bool fin = (ro.flags & ROW_FINAL) != 0;
-            const float* g = fin ? ro.gf : ro.gb;
-            const float* bb = fin ? ro.bf : ro.bb;
+          for (int i = 0; i < NH / 4; ++i) hp[i] = make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
+        }
+        if (ro.flags & (ROW_FINAL | ROW_NORM16)) {
+          row_stats_split<NH>(t, ro.eps, red, slot, half, r, mean, rstd);
+          const bool fin = (ro.flags & ROW_FINAL) != 0;
+          const float* g = fin ? ro.gf : ro.gb;
+          const float* bb = fin ? ro.bf : ro.bb;
 #pragma unroll
-            for (int i = 0; i < BN; ++i) t[i] = (t[i] - mean) * rstd * __ldg(g + i) + __ldg(bb + i);
+          for (int i = 0; i < NH; ++i) t[i] = (t[i] - mean) * rstd * __ldg(g + c0 + i) + __ldg(bb + c0 + i);
+          if (in_range) {
             if (fin) {
-              float4* op = reinterpret_cast<float4*>(ro.out32 + (size_t)m * BN);
+              float4* op = reinterpret_cast<float4*>(ro.out32 + (size_t)m * BN + c0);
               if (valid) {
 #pragma unroll
-                for (int i = 0; i < BN / 4; ++i)
+                for (int i = 0; i < NH / 4; ++i)
                   op[i] = make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
               } else {
 #pragma unroll
-                for (int i = 0; i < BN / 4; ++i) op[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < NH / 4; ++i) op[i] = make_float4(0.f, 0.f, 0.f, 0.f);
               }
             } else {
 #pragma unroll
-              for (int c = 0; c < BN / 32; ++c) store_f16x32(ro.n16 + (size_t)m * BN + c * 32, t + c * 32);
+              for (int c = 0; c < NH / 32; ++c) {
+                const size_t off = (size_t)m * BN + c0 + c * 32;
+                store_f16x32(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, t + c * 32);
+              }
             }
-          } else if (ro.flags & ROW_CAST16) {
+          }
+        } else if ((ro.flags & ROW_CAST16) && in_range) {
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) store_f16x32(ro.n16 + (size_t)m * BN + c * 32, t + c * 32);
+          for (int c = 0; c < NH / 32; ++c) {
+            const size_t off = (size_t)m * BN + c0 + c * 32;
+            store_f16x32(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, t + c * 32);
           }
         }
       }
@@ -360,51 +423,49 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int BN, int EPI>
-static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int num_sms,
-                              cudaStream_t s) {
-  auto kern = gemm_kernel<BN, EPI>;
-  const size_t smem = GemmCfg<BN>::SMEM;
+template <int BN, int EPI, int AS, int WS>
+static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int num_sms, cudaStream_t s) {
+  using C = GemmCfg<BN, AS, WS>;
   const int tiles = ((a.c.M + kGemmBM - 1) / kGemmBM) * (a.N / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, 192, smem, s>>>(ta, tb, a);
+  gemm_kernel<BN, EPI, AS, WS><<<grid, kGemmThreads, C::SMEM, s>>>(mp.a, mp.alo, mp.b, mp.blo, a);
   return cudaGetLastError();
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int AS, int WS>
 static cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)GemmCfg<BN>::SMEM);
+  return cudaFuncSetAttribute(gemm_kernel<BN, EPI, AS, WS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)GemmCfg<BN, AS, WS>::SMEM);
 }
+
+// Every (BN, EPI) pair the planner uses, at the three operand modes (AS, WS) = (0,0), (0,1), (1,1).
+#define TFL_GEMM_VARIANTS(X)                                                                       \
+  X(128, EPI_BIAS_F16) X(256, EPI_BIAS_F16) X(128, EPI_BIAS_GELU_F16) X(256, EPI_BIAS_GELU_F16) \
+  X(128, EPI_BIAS_RES_F32) X(256, EPI_BIAS_RES_F32) X(128, EPI_BIAS_RES_ROW)
 
 cudaError_t prepare_gemm_kernels() {
-  cudaError_t e;
-  if ((e = prepare_one<128, EPI_BIAS_F16>()) != cudaSuccess) return e;
-  if ((e = prepare_one<128, EPI_BIAS_GELU_F16>()) != cudaSuccess) return e;
-  if ((e = prepare_one<128, EPI_BIAS_RES_F32>()) != cudaSuccess) return e;
-  if ((e = prepare_one<128, EPI_BIAS_RES_ROW>()) != cudaSuccess) return e;
-  if ((e = prepare_one<256, EPI_BIAS_F16>()) != cudaSuccess) return e;
-  if ((e = prepare_one<256, EPI_BIAS_GELU_F16>()) != cudaSuccess) return e;
-  return prepare_one<256, EPI_BIAS_RES_F32>();
+  cudaError_t e = cudaSuccess;
+#define TFL_PREP(BN, EPI)                                 \
+  if (e == cudaSuccess) e = prepare_one<BN, EPI, 0, 0>(); \
+  if (e == cudaSuccess) e = prepare_one<BN, EPI, 0, 1>(); \
+  if (e == cudaSuccess) e = prepare_one<BN, EPI, 1, 1>();
+  TFL_GEMM_VARIANTS(TFL_PREP)
+#undef TFL_PREP
+  return e;
 }
 
-cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                        int num_sms, cudaStream_t s) {
-  if (bn == 128) {
-    switch (epi) {
-      case EPI_BIAS_F16: return launch_one<128, EPI_BIAS_F16>(ta, tb, a, num_sms, s);
-      case EPI_BIAS_GELU_F16: return launch_one<128, EPI_BIAS_GELU_F16>(ta, tb, a, num_sms, s);
-      case EPI_BIAS_RES_F32: return launch_one<128, EPI_BIAS_RES_F32>(ta, tb, a, num_sms, s);
-      case EPI_BIAS_RES_ROW: return launch_one<128, EPI_BIAS_RES_ROW>(ta, tb, a, num_sms, s);
-    }
-  } else if (bn == 256) {
-    switch (epi) {
-      case EPI_BIAS_F16: return launch_one<256, EPI_BIAS_F16>(ta, tb, a, num_sms, s);
-      case EPI_BIAS_GELU_F16: return launch_one<256, EPI_BIAS_GELU_F16>(ta, tb, a, num_sms, s);
-      case EPI_BIAS_RES_F32: return launch_one<256, EPI_BIAS_RES_F32>(ta, tb, a, num_sms, s);
-    }
+cudaError_t launch_gemm(int bn, int epi, int as, int ws, const GemmMaps& mp, const GemmArgs& a, int num_sms,
+                        cudaStream_t s) {
+  if (as && !ws) return cudaErrorInvalidValue;
+#define TFL_LAUNCH(BN, EPI)                                      \
+  if (bn == BN && epi == EPI) {                                  \
+    if (as) return launch_one<BN, EPI, 1, 1>(mp, a, num_sms, s); \
+    if (ws) return launch_one<BN, EPI, 0, 1>(mp, a, num_sms, s); \
+    return launch_one<BN, EPI, 0, 0>(mp, a, num_sms, s);         \
   }
+  TFL_GEMM_VARIANTS(TFL_LAUNCH)
+#undef TFL_LAUNCH
   return cudaErrorInvalidValue;
 }
 

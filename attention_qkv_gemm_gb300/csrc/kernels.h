@@ -33,7 +33,8 @@ struct RowOps {
   const float *gb = nullptr, *bb = nullptr;  // NORM16 affine
   const float *gf = nullptr, *bf = nullptr;  // FINAL affine
   float* h32 = nullptr;                      // [M, D]
-  __half* n16 = nullptr;                     // [M, D]
+  __half* n16 = nullptr;                     // [M, D] fp16 (hi part when split)
+  __half* n16lo = nullptr;                   // [M, D] fp16 residual plane, or null
   float* out32 = nullptr;                    // [M, D]
 };
 
@@ -56,8 +57,10 @@ enum GemmEpi : int {
 struct GemmArgs {
   Common c;
   int N = 0, K = 0;
+  float acc_scale = 1.f;         // 2^-s undoing the weight pre-scale
   const float* bias = nullptr;   // [N]
   __half* c16 = nullptr;         // [M, N] for the fp16 epilogues
+  __half* c16lo = nullptr;       // [M, N] residual plane (split activations), or null
   const float* res = nullptr;    // [M, N] residual for the fp32 epilogues (may alias h32)
   float* h32 = nullptr;          // EPI_BIAS_RES_F32 output
   RowOps row;                    // EPI_BIAS_RES_ROW
@@ -69,6 +72,7 @@ struct AttnArgs {
   int causal = 0;
   float scale_log2 = 0.f;        // log2(e) / sqrt(head_dim)
   __half* o16 = nullptr;         // [M, D]
+  int* counter = nullptr;        // work-item counter, zero before the launch
 };
 
 struct RowArgs {
@@ -82,14 +86,22 @@ struct RowArgs {
 cudaError_t prepare_gemm_kernels();
 cudaError_t prepare_attention_kernels();
 
+// TMA descriptors of one GEMM: A (and its lo plane), W (and its lo part).
+struct GemmMaps {
+  CUtensorMap a, alo, b, blo;
+};
+
 // Launchers (return cudaError_t of the launch).
-cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                        int num_sms, cudaStream_t s);
+// as: A carries a lo plane; ws: W carries a lo part (as requires ws).
+cudaError_t launch_gemm(int bn, int epi, int as, int ws, const GemmMaps& mp, const GemmArgs& a, int num_sms,
+                        cudaStream_t s);
 cudaError_t launch_attention(int hd, const CUtensorMap& tq, const CUtensorMap& tkv, const AttnArgs& a,
                              int num_sms, cudaStream_t s);
 cudaError_t launch_rows(const RowArgs& a, cudaStream_t s);
 cudaError_t launch_check_lengths(const int* lengths, int B, int S, int* status, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s);
+cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s);
+cudaError_t launch_split_f16(const float* src, __half* hi, __half* lo, size_t n, float scale, cudaStream_t s);
 cudaError_t launch_probe_wait(int* status, int64_t timeout_ns, cudaStream_t s);
 
 // Tile sizes shared by the host planner and the kernels.
@@ -97,7 +109,6 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;
 constexpr int kAttnBM = 128;
 __host__ __device__ constexpr int attn_block_n(int hd) { return hd >= 128 ? 64 : 128; }
-size_t gemm_smem_bytes(int bn);
 size_t attn_smem_bytes(int hd);
 
 }  // namespace tfl

@@ -62,6 +62,8 @@ struct WaitCtl {
   int* status;              // global, OR-ed with TFL_DEV_* bits
   volatile int* abort_flag;  // shared, set once any waiter in the CTA gave up
   int64_t timeout_ns;
+  bool early_exit = true;    // give up as soon as abort_flag is set (off for warps that
+                             // share a named barrier: they must all leave the same way)
 };
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
@@ -74,7 +76,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0) {
-      if (*c.abort_flag) return false;
+      if (c.early_exit && *c.abort_flag) return false;
       if ((int64_t)(globaltimer_ns() - t0) > c.timeout_ns) {
         *c.abort_flag = 1;
         atomicOr(c.status, TFL_DEV_TIMEOUT);

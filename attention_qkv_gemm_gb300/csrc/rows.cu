@@ -45,12 +45,21 @@ __device__ __forceinline__ void warp_ln(float4* t, float eps, const float* g, co
   }
 }
 
-__device__ __forceinline__ void store_h4(__half* p, float4 v) {
+// Store 4 values as fp16 at p and, when lo != nullptr, their rounding residuals at lo.
+__device__ __forceinline__ void store_h4(__half* p, __half* lo, float4 v) {
   __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
   uint2 u;
   u.x = *reinterpret_cast<uint32_t*>(&a);
   u.y = *reinterpret_cast<uint32_t*>(&b);
   *reinterpret_cast<uint2*>(p) = u;
+  if (lo != nullptr) {
+    const float2 fa = __half22float2(a), fb = __half22float2(b);
+    __half2 ra = __floats2half2_rn(v.x - fa.x, v.y - fa.y), rb = __floats2half2_rn(v.z - fb.x, v.w - fb.y);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&ra);
+    w.y = *reinterpret_cast<uint32_t*>(&rb);
+    *reinterpret_cast<uint2*>(lo) = w;
+  }
 }
 
 template <int V>
@@ -81,10 +90,16 @@ __global__ void __launch_bounds__(256) rows_kernel(const RowArgs a) {
     float4 y[V];
     warp_ln<V>(t, ro.eps, ro.gb, ro.bb, lane, y);
 #pragma unroll
-    for (int k = 0; k < V; ++k) store_h4(ro.n16 + (size_t)m * D + (k * 32 + lane) * 4, y[k]);
+    for (int k = 0; k < V; ++k) {
+      const size_t off = (size_t)m * D + (k * 32 + lane) * 4;
+      store_h4(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, y[k]);
+    }
   } else if (ro.flags & ROW_CAST16) {
 #pragma unroll
-    for (int k = 0; k < V; ++k) store_h4(ro.n16 + (size_t)m * D + (k * 32 + lane) * 4, t[k]);
+    for (int k = 0; k < V; ++k) {
+      const size_t off = (size_t)m * D + (k * 32 + lane) * 4;
+      store_h4(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, t[k]);
+    }
   }
 }
 
@@ -122,6 +137,43 @@ cudaError_t launch_check_lengths(const int* lengths, int B, int S, int* status, 
 __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     dst[i] = __float2half_rn(src[i]);
+}
+
+// Largest |x| over n values, as the bit pattern of a non-negative float (atomicMax on the bits).
+__global__ void absmax_kernel(const float* __restrict__ src, size_t n, unsigned* out) {
+  float m = 0.f;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(src[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+}
+
+cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  size_t grid = (n + 255) / 256;
+  if (grid > 1024) grid = 1024;
+  absmax_kernel<<<(unsigned)grid, 256, 0, s>>>(src, n, out);
+  return cudaGetLastError();
+}
+
+// hi = fp16(x * scale); lo = fp16(x * scale - hi) (lo may be null).
+__global__ void split_f16_kernel(const float* __restrict__ src, __half* __restrict__ hi, __half* __restrict__ lo,
+                                 size_t n, float scale) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = src[i] * scale;
+    const __half h = __float2half_rn(v);
+    hi[i] = h;
+    if (lo) lo[i] = __float2half_rn(v - __half2float(h));
+  }
+}
+
+cudaError_t launch_split_f16(const float* src, __half* hi, __half* lo, size_t n, float scale, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  size_t grid = (n + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  split_f16_kernel<<<(unsigned)grid, 256, 0, s>>>(src, hi, lo, n, scale);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s) {

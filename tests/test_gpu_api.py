@@ -1,0 +1,103 @@
+"""GPU tests of the C-ABI surface: failure reporting, host-buffer entry,
+profiling entry, and the precision modes (against the fp64 oracle)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import assert_gate, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    import attention_qkv_gemm_gb300 as pkg
+    # a wait on an mbarrier nothing completes must give up after ~1 ms and say so
+    assert pkg.tfl_probe_wait_timeout(1_000_000) == pkg.TFL_ERR_DEVICE_TIMEOUT
+    # the context is still usable: a normal forward runs and passes
+    shape = synth.Shape(1, 128, 128, 4, 256, 1, True)
+    prm = synth.params(0, shape)
+    x = synth.input_x(0, shape)
+    u, rc = run_gpu(shape, prm, x, None, True)
+    assert rc == 0
+    assert_gate(u, oracle.forward(prm, 4, x, None, True))
+
+
+def test_out_of_range_lengths_are_flagged_and_clamped():
+    shape = synth.Shape(3, 140, 128, 4, 256, 1, False)
+    prm = synth.params(1, shape)
+    x = synth.input_x(1, shape)
+    u, rc = run_gpu(shape, prm, x, [500, -3, 70], False)
+    import attention_qkv_gemm_gb300 as pkg
+    assert rc == pkg.TFL_ERR_BAD_LENGTHS
+    r = oracle.forward(prm, 4, x, np.array([140, 0, 70], dtype=np.int32), False)
+    assert_gate(u, r, "clamped lengths")
+    assert np.all(u[1] == 0.0)
+
+
+def test_precision_modes_order_errors():
+    shape = synth.Shape(2, 256, 128, 4, 512, 2, True)
+    prm = synth.params(3, shape, ln_affine="random")
+    x = synth.input_x(3, shape)
+    r = oracle.forward(prm, 4, x, None, True)
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    errs = []
+    for prec in (0, 1, 2):
+        o = pkg.tfl_default_options()
+        o.precision = prec
+        m = pkg.TransformerStack(*[shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers],
+                                 prm, options=o)
+        u = m.forward(torch.from_numpy(x).cuda(), None, causal=True).cpu().numpy()
+        assert m.status() == 0
+        m.close()
+        errs.append(float(np.sqrt(np.mean((u - r) ** 2))))
+    assert errs[2] < errs[1] < errs[0], errs
+    assert errs[2] < 0.6 * errs[0], errs
+
+
+def test_forward_host_matches_device_path():
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    shape = synth.Shape(2, 200, 128, 4, 512, 2, True)
+    prm = synth.params(4, shape)
+    x = synth.input_x(4, shape)
+    lens = np.array([200, 111], dtype=np.int32)
+    m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm)
+    try:
+        dev = m.forward(torch.from_numpy(x).cuda(), torch.from_numpy(lens).cuda(), causal=True).cpu().numpy()
+        hx = torch.from_numpy(x).pin_memory()
+        hl = torch.from_numpy(lens).pin_memory()
+        ho = torch.empty_like(hx).pin_memory()
+        rc = pkg.tfl_forward_host(m.handle, hx.data_ptr(), hl.data_ptr(), 1, ho.data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+        np.testing.assert_array_equal(ho.numpy(), dev)
+        # pageable host buffers work too
+        xo = np.empty_like(x)
+        rc = pkg.tfl_forward_host(m.handle, x.ctypes.data, lens.ctypes.data, 1, xo.ctypes.data, 0)
+        assert rc == 0
+        np.testing.assert_array_equal(xo, dev)
+    finally:
+        m.close()
+
+
+def test_profile_forward_reports_every_launch():
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    for D, H in ((128, 4), (256, 4)):
+        shape = synth.Shape(1, 128, D, H, 256, 2, True)
+        prm = synth.params(5, shape)
+        m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm)
+        try:
+            x = torch.from_numpy(synth.input_x(5, shape)).cuda()
+            out = torch.empty_like(x)
+            prof = pkg.tfl_profile_forward(m.handle, x.data_ptr(), None, 1, out.data_ptr(),
+                                           torch.cuda.current_stream().cuda_stream)
+            kinds = [k for k, _ in prof]
+            # every launch except the length check is timed
+            assert len(kinds) == pkg.tfl_launch_count(m.handle, 1) - 1
+            assert kinds.count("attention") == 2 and kinds.count("gemm_qkv") == 2
+            assert all(ms > 0 for _, ms in prof)
+        finally:
+            m.close()
