@@ -30,7 +30,9 @@ KIND_NAMES = {1: "rownorm", 2: "gemm_qkv", 3: "attention", 4: "gemm_oproj", 5: "
 
 EXPORTS = ("tfl_default_options", "tfl_workspace_bytes", "tfl_create", "tfl_forward", "tfl_forward_host",
            "tfl_status", "tfl_destroy", "tfl_last_error", "tfl_profile_forward", "tfl_launch_count",
-           "tfl_probe_wait_timeout")
+           "tfl_probe_wait_timeout", "tfl_forward_noalloc")
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class TflShape(ctypes.Structure):
@@ -86,6 +88,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.tfl_create.restype = ctypes.c_int
     lib.tfl_forward.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
     lib.tfl_forward.restype = ctypes.c_int
+    lib.tfl_forward_noalloc.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.tfl_forward_noalloc.restype = ctypes.c_int
     lib.tfl_forward_host.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
     lib.tfl_forward_host.restype = ctypes.c_int
     lib.tfl_status.argtypes = [vp, vp]
@@ -141,6 +145,11 @@ def tfl_create(shape: TflShape, layer_ptrs: Sequence[dict], lnf_g: int, lnf_b: i
 
 def tfl_forward(handle: int, x: int, lengths: Optional[int], causal: int, out: int, stream: int = 0) -> None:
     _check(load().tfl_forward(handle, x, lengths, int(causal), out, stream))
+
+
+def tfl_forward_noalloc(handle: int, x: int, lengths: Optional[int], causal: int, out: int, stream: int = 0) -> None:
+    """The forward with its intermediates in the library's fixed device array (no allocation)."""
+    _check(load().tfl_forward_noalloc(handle, x, lengths, int(causal), out, stream))
 
 
 def tfl_forward_host(handle: int, x: int, lengths: Optional[int], causal: int, out: int, stream: int = 0) -> int:

@@ -15,6 +15,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <mutex>
 #include <vector>
 
 #include "../../include/tfl.h"
@@ -746,6 +747,115 @@ void tfl_destroy(tfl_handle* h) {
   if (h->hlen_dev) cudaFree(h->hlen_dev);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   delete h;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward: every intermediate of the forward (residual, normed
+// rows, qkv, attention output, FFN activations, attention work counters) lives
+// in this file-scope device array instead of the handle's workspace.  It is
+// created with the library's device code, so every GPU that loads the library
+// holds it until the process exits; calls on one device share it.
+static constexpr size_t kNoallocScratchBytes = (size_t)32 << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+// Device address of g_noalloc_scratch per device (host code cannot use the
+// symbol itself: on the host it names a stand-in, not device memory).
+std::mutex g_noalloc_mu;
+void* g_noalloc_base[128] = {};
+}  // namespace
+
+extern "C" {
+
+int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out,
+                        tfl_stream stream) {
+  g_err.clear();
+  if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (!x || !out) return fail(TFL_ERR_INVALID_ARG, "x and out must be non-NULL device pointers");
+  if (causal != 0 && causal != 1) return fail(TFL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  const size_t bytes = (size_t)h->M * h->D * sizeof(float);
+  const uint8_t *xb = reinterpret_cast<const uint8_t*>(x), *ob = reinterpret_cast<const uint8_t*>(out);
+  if (xb < ob + bytes && ob < xb + bytes) return fail(TFL_ERR_INVALID_ARG, "out overlaps x");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(TFL_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  const WsLayout lay = ws_layout(h->shape, h->opt.precision);
+  if (lay.total > kNoallocScratchBytes)
+    return fail(TFL_ERR_UNSUPPORTED, "tfl_forward_noalloc: this shape needs " + std::to_string(lay.total) +
+                                         " bytes of scratch, more than its fixed " +
+                                         std::to_string(kNoallocScratchBytes) + "-byte device array");
+  int dev = 0;
+  TFL_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev != h->device) return fail(TFL_ERR_INVALID_ARG, "the current device is not the handle's device");
+  if (dev < 0 || dev >= 128) return fail(TFL_ERR_UNSUPPORTED, "device ordinal above 127");
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+      void* p = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+      g_noalloc_base[dev] = p;
+    }
+    base = g_noalloc_base[dev];
+  }
+
+  // Point this call's intermediates at the scratch (the handle keeps its own
+  // weights and status word), run the launch sequence eagerly, then restore.
+  uint8_t* sb = static_cast<uint8_t*>(base);
+  struct Intermediates {
+    float* h32;
+    __half *n16, *n16lo, *qkv16, *o16, *g16, *g16lo;
+    int* sched;
+    CUtensorMap tm_n16, tm_n16lo, tm_o16, tm_g16, tm_g16lo, tm_q, tm_kv;
+  };
+  const Intermediates saved{h->h32,    h->n16,      h->n16lo,   h->qkv16,  h->o16,    h->g16,
+                            h->g16lo,  h->sched,    h->tm_n16,  h->tm_n16lo, h->tm_o16, h->tm_g16,
+                            h->tm_g16lo, h->tm_q,   h->tm_kv};
+  auto restore = [&]() {
+    h->h32 = saved.h32;
+    h->n16 = saved.n16;
+    h->n16lo = saved.n16lo;
+    h->qkv16 = saved.qkv16;
+    h->o16 = saved.o16;
+    h->g16 = saved.g16;
+    h->g16lo = saved.g16lo;
+    h->sched = saved.sched;
+    h->tm_n16 = saved.tm_n16;
+    h->tm_n16lo = saved.tm_n16lo;
+    h->tm_o16 = saved.tm_o16;
+    h->tm_g16 = saved.tm_g16;
+    h->tm_g16lo = saved.tm_g16lo;
+    h->tm_q = saved.tm_q;
+    h->tm_kv = saved.tm_kv;
+  };
+  h->h32 = reinterpret_cast<float*>(sb + lay.h32);
+  h->n16 = reinterpret_cast<__half*>(sb + lay.n16);
+  h->n16lo = h->opt.precision == 2 ? reinterpret_cast<__half*>(sb + lay.n16lo) : nullptr;
+  h->qkv16 = reinterpret_cast<__half*>(sb + lay.qkv16);
+  h->o16 = reinterpret_cast<__half*>(sb + lay.o16);
+  h->g16 = reinterpret_cast<__half*>(sb + lay.g16);
+  h->g16lo = h->opt.precision == 2 ? reinterpret_cast<__half*>(sb + lay.g16lo) : nullptr;
+  h->sched = reinterpret_cast<int*>(sb + lay.sched);  // zeroed by the launch sequence itself
+  const uint64_t M = (uint64_t)h->M;
+  const int D = h->D, F = h->F;
+  const int atom = h->hd < 64 ? h->hd : 64;
+  bool ok = make_map_2d(&h->tm_n16, h->n16, M, D, kGemmBM) && make_map_2d(&h->tm_o16, h->o16, M, D, kGemmBM) &&
+            make_map_2d(&h->tm_g16, h->g16, M, F, kGemmBM) &&
+            (!h->n16lo || make_map_2d(&h->tm_n16lo, h->n16lo, M, D, kGemmBM)) &&
+            (!h->g16lo || make_map_2d(&h->tm_g16lo, h->g16lo, M, F, kGemmBM)) &&
+            make_map_qkv(&h->tm_q, h->qkv16, h->shape.B, h->shape.S, 3 * D, atom, kAttnBM) &&
+            make_map_qkv(&h->tm_kv, h->qkv16, h->shape.B, h->shape.S, 3 * D, atom, attn_block_n(h->hd));
+  if (!ok) {
+    restore();
+    return fail(TFL_ERR_CUDA, "scratch tensor map encoding failed");
+  }
+  if (!h->n16lo) h->tm_n16lo = h->tm_n16;
+  if (!h->g16lo) h->tm_g16lo = h->tm_g16;
+  const int rc = enqueue(h, x, lengths, causal, out, static_cast<cudaStream_t>(stream), Rec{});
+  restore();
+  return rc;
 }
 
 int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream) {

@@ -186,6 +186,44 @@ int tfl_launch_count(const tfl_handle* h, int causal);
  */
 int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream);
 
+/*
+ * tfl_forward_noalloc -- the forward for callers that cannot allocate device
+ * memory when they run it.
+ *
+ * Who needs it: code that runs the forward where cudaMalloc is off limits --
+ * for instance inside another component's CUDA-graph capture (allocation and
+ * graph instantiation are not allowed while a capture is open), under a host
+ * framework whose memory pool owns the device budget, or in a latency-critical
+ * loop that must never hit the allocator's implicit synchronisation.
+ * tfl_forward needs no allocation once warm, but its first call per buffer set
+ * instantiates a CUDA graph; tfl_forward_host allocates staging buffers.  This
+ * entry point does neither: it enqueues the same kernels eagerly on `stream`.
+ *
+ * This is an addition of this library; the pages describe no counterpart.
+ *
+ * Arguments, layouts and errors are those of tfl_forward (the handle supplies
+ * the packed weights and the status word read by tfl_status).  Every
+ * intermediate of the forward -- residual stream, normed rows, qkv, attention
+ * output, FFN activations, attention work counters -- lives in one fixed
+ * device array inside the library, TFL_NOALLOC_SCRATCH_BYTES (32 MiB) on each
+ * GPU that loads the library, held until the process exits.  A shape whose
+ * intermediates do not fit (tfl_workspace_bytes(shape) at the handle's
+ * precision > 32 MiB, e.g. more than roughly 7000 tokens at d_model 128) is
+ * rejected with TFL_ERR_UNSUPPORTED and a message naming both sizes.
+ *
+ * The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress with that device current); make that first call before
+ * any stream capture.  All calls, on every handle and stream of a device,
+ * share the array and it keeps the last call's contents: calls that overlap
+ * on the GPU race and corrupt each other, so serialize them (one stream, or
+ * events).  The work counters that must start at zero are cleared by each
+ * call on `stream`.  The handle is used only on the host during the call (not
+ * thread-safe with other calls on the same handle).
+ */
+#define TFL_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths,
+                        int causal, float* out, tfl_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
