@@ -26,11 +26,12 @@ TFL_ERR_CUDA = -4
 TFL_ERR_DEVICE_TIMEOUT = -5
 TFL_ERR_BAD_LENGTHS = -6
 
-KIND_NAMES = {1: "rownorm", 2: "gemm_qkv", 3: "attention", 4: "gemm_oproj", 5: "gemm_ffn1", 6: "gemm_ffn2"}
+KIND_NAMES = {1: "rownorm", 2: "gemm_qkv", 3: "attention", 4: "gemm_oproj", 5: "gemm_ffn1", 6: "gemm_ffn2",
+              7: "postchain"}
 
 EXPORTS = ("tfl_default_options", "tfl_workspace_bytes", "tfl_create", "tfl_forward", "tfl_forward_host",
            "tfl_status", "tfl_destroy", "tfl_last_error", "tfl_profile_forward", "tfl_launch_count",
-           "tfl_probe_wait_timeout", "tfl_forward_noalloc")
+           "tfl_probe_wait_timeout", "tfl_forward_noalloc", "tfl_selftest_gelu")
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -103,6 +104,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.tfl_profile_forward.restype = ctypes.c_int
     lib.tfl_launch_count.argtypes = [vp, ctypes.c_int]
     lib.tfl_launch_count.restype = ctypes.c_int
+    lib.tfl_selftest_gelu.argtypes = [i32, ctypes.POINTER(ctypes.c_float), vp]
+    lib.tfl_selftest_gelu.restype = ctypes.c_int
     lib.tfl_probe_wait_timeout.argtypes = [i64, vp]
     lib.tfl_probe_wait_timeout.restype = ctypes.c_int
     _lib = lib
@@ -181,6 +184,13 @@ def tfl_profile_forward(handle: int, x: int, lengths: Optional[int], causal: int
     n = ctypes.c_int32()
     _check(load().tfl_profile_forward(handle, x, lengths, int(causal), out, stream, ms, kinds, cap, ctypes.byref(n)))
     return [(KIND_NAMES.get(kinds[i], str(kinds[i])), float(ms[i])) for i in range(min(n.value, cap))]
+
+
+def tfl_selftest_gelu(n: int = 1 << 20, stream: int = 0) -> float:
+    """Largest |GELU(A&S 7.1.26) - GELU(erff)| on the GPU over n points of [-12, 12]."""
+    v = ctypes.c_float()
+    _check(load().tfl_selftest_gelu(int(n), ctypes.byref(v), stream))
+    return float(v.value)
 
 
 def tfl_probe_wait_timeout(timeout_ns: int, stream: int = 0) -> int:

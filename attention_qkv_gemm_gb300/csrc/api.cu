@@ -18,7 +18,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/tfl.h"
+#include "tfl.h"
 #include "kernels.h"
 
 using namespace tfl;
@@ -91,6 +91,7 @@ struct PackedW {
   __half* lo = nullptr;
   float acc_scale = 1.f;
   CUtensorMap tm_hi{}, tm_lo{};
+  CUtensorMap tm_hi64{}, tm_lo64{};  // 64-row boxes (the fused chain's FFN-in chunks)
 };
 
 struct LayerDev {
@@ -132,6 +133,9 @@ WsLayout ws_layout(const tfl_shape& s, int precision) {
   w.total = off;
   return w;
 }
+
+// The fused post-attention chain serves d_model = 128, d_ff <= 2048 at precision 2.
+bool use_chain(int D, int F, int precision) { return D == 128 && F <= 2048 && precision == 2; }
 
 // Output tile width: 256 when N allows it, except with split activations (the
 // four operand tiles of a 256-wide stage leave room for only two stages).
@@ -319,6 +323,47 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       TFL_CUDA(launch_attention(h->hd, h->tm_q, h->tm_kv, a, h->num_sms, st), "attention");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_ATTENTION), "event");
     }
+    if (use_chain(D, F, prec)) {
+      // o_proj .. FFN-out .. next LayerNorm in one kernel
+      ChainArgs ca;
+      ca.c = c;
+      ca.F = F;
+      ca.eps = eps;
+      ca.post_ln = pre ? 0 : 1;
+      ca.last = last ? 1 : 0;
+      ca.scale_o = ly.wo.acc_scale;
+      ca.scale_1 = ly.w1.acc_scale;
+      ca.scale_2 = ly.w2.acc_scale;
+      ca.bo = ly.bo;
+      ca.b1 = ly.b1;
+      ca.b2 = ly.b2;
+      ca.ln1_g = ly.ln1_g;
+      ca.ln1_b = ly.ln1_b;
+      ca.ln2_g = ly.ln2_g;
+      ca.ln2_b = ly.ln2_b;
+      if (!last) {
+        ca.lnn_g = h->layers[l + 1].ln1_g;
+        ca.lnn_b = h->layers[l + 1].ln1_b;
+      }
+      ca.lnf_g = h->lnf_g;
+      ca.lnf_b = h->lnf_b;
+      ca.res = (l == 0) ? x : h->h32;
+      ca.h32 = h->h32;
+      ca.n16 = h->n16;
+      ca.n16lo = h->n16lo;
+      ca.out32 = out;
+      ChainMaps cm;
+      cm.o = h->tm_o16;
+      cm.wo = ly.wo.tm_hi;
+      cm.wo_lo = ly.wo.tm_lo;
+      cm.w1 = ly.w1.tm_hi64;
+      cm.w1_lo = ly.w1.tm_lo64;
+      cm.w2 = ly.w2.tm_hi;
+      cm.w2_lo = ly.w2.tm_lo;
+      TFL_CUDA(launch_postchain(cm, ca, h->num_sms, st), "post-attention chain");
+      TFL_CUDA(rec_mark(rec, st, TFL_KIND_POSTCHAIN), "event");
+      continue;
+    }
     // o_proj + bias + residual (+ LayerNorm); the attention output has no lo plane
     {
       GemmArgs g;
@@ -454,7 +499,7 @@ const char* tfl_last_error(void) { return g_err.c_str(); }
 int tfl_launch_count(const tfl_handle* h, int causal) {
   (void)causal;
   if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
-  const int per_layer = h->D == 128 ? 5 : 7;
+  const int per_layer = use_chain(h->D, h->F, h->opt.precision) ? 3 : (h->D == 128 ? 5 : 7);
   return 2 + per_layer * h->L;
 }
 
@@ -483,6 +528,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   if (!get_encode()) return fail(TFL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   TFL_CUDA(prepare_gemm_kernels(), "gemm kernel attributes");
   TFL_CUDA(prepare_attention_kernels(), "attention kernel attributes");
+  TFL_CUDA(prepare_postchain_kernel(), "chain kernel attributes");
 
   const int D = shape->d_model, F = shape->d_ff, L = shape->n_layers;
   const WsLayout lay = ws_layout(*shape, o.precision);
@@ -603,6 +649,8 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
       const int aw = o.precision == 2;
       bool ok = maps(d.wqkv, 3 * D, D, gemm_bn(3 * D, aw)) && maps(d.wo, D, D, D == 128 ? 128 : gemm_bn(D, 0)) &&
                 maps(d.w1, F, D, gemm_bn(F, aw)) && maps(d.w2, D, F, D == 128 ? 128 : gemm_bn(D, aw));
+      if (ok && use_chain(D, F, o.precision))
+        ok = make_map_2d(&d.w1.tm_hi64, d.w1.hi, F, D, 64) && make_map_2d(&d.w1.tm_lo64, d.w1.lo, F, D, 64);
       if (!ok) rc = fail(TFL_ERR_CUDA, "weight tensor map encoding failed");
     }
   }
@@ -856,6 +904,23 @@ int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths, i
   const int rc = enqueue(h, x, lengths, causal, out, static_cast<cudaStream_t>(stream), Rec{});
   restore();
   return rc;
+}
+
+int tfl_selftest_gelu(int32_t n, float* max_abs_diff, tfl_stream stream) {
+  g_err.clear();
+  if (n < 2 || !max_abs_diff) return fail(TFL_ERR_INVALID_ARG, "n must be >= 2 and max_abs_diff non-NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* d = nullptr;
+  TFL_CUDA(cudaMalloc(&d, sizeof(unsigned)), "selftest alloc");
+  cudaError_t e = cudaMemsetAsync(d, 0, sizeof(unsigned), st);
+  if (e == cudaSuccess) e = launch_gelu_selftest(n, d, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  unsigned bits = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&bits, d, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  cudaFree(d);
+  if (e != cudaSuccess) return cuda_fail(e, "gelu selftest");
+  std::memcpy(max_abs_diff, &bits, sizeof(float));
+  return TFL_OK;
 }
 
 int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream) {

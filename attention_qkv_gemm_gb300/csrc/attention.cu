@@ -9,8 +9,9 @@
 //     (section 2.1, the running-max recurrence).  The rescale is lazy: the
 //     reference max only moves when the row max grew by more than 8 in log2
 //     units, so P <= 2^8 and O is touched rarely; O / l is exact either way.
-//   * P = exp2(S * log2(e)/sqrt(hd) - m) in fp16 goes to shared memory and
-//     O += P V_j accumulates in tensor memory.
+//   * P = exp2(S * log2(e)/sqrt(hd) - m) in fp16 goes to tensor memory (two
+//     values per column) and O += P V_j takes its A operand from there
+//     (tcgen05.mma with A in TMEM), so only V is read from shared memory.
 //   * Causal: key blocks above the diagonal are never loaded (block skipping,
 //     section 1.C); the mask is applied only on the diagonal block; the key
 //     mask is not applied at all, because for a valid query i every key j <= i
@@ -32,8 +33,11 @@
 // pass over S with the running max as the exponent reference while the block
 // max is tracked; only when a row's max grew by more than 2^8 does its warp
 // redo the block with the two-pass path (block max, rescale O, exponentials).
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
+#include "xpose.cuh"
 
 namespace tfl {
 
@@ -47,12 +51,14 @@ struct AttnCfg {
   static constexpr uint32_t SWZ = ROWB == 64 ? kSw64 : kSw128;
   static constexpr int Q_BYTES = BM * HD * 2;
   static constexpr int KV_BYTES = BN * HD * 2;      // one K (or V) block
-  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int XP_BYTES = 4 * 32 * 128;     // output transpose stage, one per softmax warp
   static constexpr int NST = HD == 32 ? 4 : 2;
-  static constexpr int CTAS_PER_SM = HD == 32 ? 2 : 1;
-  static constexpr int O_COL = HD <= 64 ? 128 : 256;
+  static constexpr int CTAS_PER_SM = HD <= 64 ? 2 : 1;
+  // tensor memory: S [0, BN), P (fp16 pairs) [BN, BN + BN/2), O from O_COL
+  static constexpr int P_COL = BN;
+  static constexpr int O_COL = HD <= 64 ? 192 : 256;
   static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
-  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)NST * 2 * KV_BYTES + P_BYTES + 384;
+  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)NST * 2 * KV_BYTES + XP_BYTES + 384;
 };
 
 size_t attn_smem_bytes(int hd) {
@@ -95,8 +101,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::Q_BYTES;
   uint8_t* sV = sK + (size_t)C::NST * C::KV_BYTES;
-  uint8_t* sP = sV + (size_t)C::NST * C::KV_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + C::P_BYTES);
+  uint8_t* sX = sV + (size_t)C::NST * C::KV_BYTES;  // output transpose stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sX + C::XP_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* s_full = bars + 2;
@@ -216,13 +222,13 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     int st = 0, ik = 0;
     uint32_t kvph = 0, qph = 0, pph = 0, oeph = 0, itph = 0;
     bool first_item = true, ok = true;
+    const uint32_t t_p = tmem_base + C::P_COL;
     auto issue_pv = [&](int pst, bool accumulate) {
-      const uint32_t sp = smem_u32(sP), sv = smem_u32(sV + (size_t)pst * C::KV_BYTES);
+      const uint32_t sv = smem_u32(sV + (size_t)pst * C::KV_BYTES);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t ad = sdesc(sp + (kk >> 2) * (kAttnBM * 128) + (kk & 3) * 32, 16, 1024, kSw128);
         const uint64_t bd = sdesc(sv + kk * 16 * C::ROWB, BN * C::ROWB, 8 * C::ROWB, C::SWZ);
-        umma_f16(d_o, ad, bd, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+        umma_f16_ts(d_o, t_p + kk * 8, bd, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
       }
     };
     while (ok) {
@@ -325,37 +331,53 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     const int r = warp * 32 + lane;  // query row within the block == TMEM lane
     const uint32_t t_s = tmem_base + ((uint32_t)(warp * 32) << 16);
     const uint32_t t_o = t_s + C::O_COL;
+    const uint32_t t_p = t_s + C::P_COL;
     const float sl2 = args.scale_log2;
     uint32_t sph = 0, oph = 0, itph = 0;
     int ik = 0;
-    uint8_t* prow = sP + r * 128;
-    const uint32_t swz = (uint32_t)(r & 7);
+    uint8_t* xst = sX + warp * 4096;
 
-    // exponentials of one 64-key group against reference mref, into the P tile;
-    // returns the group's sum in four partials and its max (masked keys skipped)
-    auto exp_group = [&](const float* sv, int g, int k0, bool need_mask, int kmax, float mref, float* ls,
+    // exponentials of one 64-key group against reference mref, packed as fp16
+    // pairs into this row's 32 P columns of group g; returns the group's sum in
+    // four partials and its max.  MASKED: keys past kmax get p = 0 and no max.
+    auto exp_group = [&](auto masked, const float* sv, int g, int kbase, int kmax, float mref, float* ls,
                          float* bm) {
+      constexpr bool MASKED = decltype(masked)::value;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        float p[8];
+      for (int e2 = 0; e2 < 32; ++e2) {
+        float p2[2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int idx = c8 * 8 + e;
+        for (int u = 0; u < 2; ++u) {
+          const int idx = 2 * e2 + u;
           const float v = sv[idx];
-          const bool ok2 = !need_mask || (k0 + g * 64 + idx <= kmax);
-          bm[e & 3] = ok2 ? fmaxf(bm[e & 3], v) : bm[e & 3];
-          const float pe = ex2(fmaf(v, sl2, -mref));
-          p[e] = ok2 ? pe : 0.f;
-          ls[e & 3] += p[e];
+          if constexpr (MASKED) {
+            const bool ok2 = kbase + idx <= kmax;
+            bm[idx & 3] = ok2 ? fmaxf(bm[idx & 3], v) : bm[idx & 3];
+            p2[u] = ok2 ? ex2(fmaf(v, sl2, -mref)) : 0.f;
+          } else {
+            bm[idx & 3] = fmaxf(bm[idx & 3], v);
+            p2[u] = ex2(fmaf(v, sl2, -mref));
+          }
+          ls[idx & 3] += p2[u];
         }
-        uint4 u;
-        __half2 h0 = __floats2half2_rn(p[0], p[1]), h1 = __floats2half2_rn(p[2], p[3]);
-        __half2 h2 = __floats2half2_rn(p[4], p[5]), h3 = __floats2half2_rn(p[6], p[7]);
-        u.x = *reinterpret_cast<uint32_t*>(&h0);
-        u.y = *reinterpret_cast<uint32_t*>(&h1);
-        u.z = *reinterpret_cast<uint32_t*>(&h2);
-        u.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(prow + g * (kAttnBM * 128) + (((uint32_t)c8 ^ swz) << 4)) = u;
+        const __half2 hp = __floats2half2_rn(p2[0], p2[1]);  // first key in the low half
+        pk[e2] = *reinterpret_cast<const uint32_t*>(&hp);
+      }
+      tmem_st32_u(t_p + g * 32, pk);
+    };
+    // one pass over S against reference mref: P into TMEM, partial sums and maxima
+    auto exp_block = [&](bool need_mask, int k0, int kmax, float mref, float* ls, float* bm) {
+#pragma unroll
+      for (int g = 0; g < BN / 64; ++g) {
+        float sv[64];
+        tmem_ld32(t_s + g * 64, sv);
+        tmem_ld32(t_s + g * 64 + 32, sv + 32);
+        tmem_wait_ld();
+        if (need_mask)
+          exp_group(std::true_type{}, sv, g, k0 + g * 64, kmax, mref, ls, bm);
+        else
+          exp_group(std::false_type{}, sv, g, k0 + g * 64, kmax, mref, ls, bm);
       }
     };
 
@@ -389,14 +411,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           // fast path: exponentials against the running max, block max tracked alongside
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
           float bm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int g = 0; g < BN / 64; ++g) {
-            float sv[64];
-            tmem_ld32(t_s + g * 64, sv);
-            tmem_ld32(t_s + g * 64 + 32, sv + 32);
-            tmem_wait_ld();
-            exp_group(sv, g, k0, need_mask, kmax, m_run, ls, bm);
-          }
+          exp_block(need_mask, k0, kmax, m_run, ls, bm);
           const float bmax = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
           slow = __any_sync(0xffffffffu, bmax * sl2 > m_run + 8.0f);
           if (!slow) l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
@@ -404,7 +419,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         if (slow) {
           // pass 1: block max
           float bm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+#pragma unroll 1
           for (int g = 0; g < BN / 64; ++g) {
             float sv[64];
             tmem_ld32(t_s + g * 64, sv);
@@ -439,17 +454,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           // pass 2: exponentials
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
           float bm2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int g = 0; g < BN / 64; ++g) {
-            float sv[64];
-            tmem_ld32(t_s + g * 64, sv);
-            tmem_ld32(t_s + g * 64 + 32, sv + 32);
-            tmem_wait_ld();
-            exp_group(sv, g, k0, need_mask, kmax, mref, ls, bm2);
-          }
+          exp_block(need_mask, k0, kmax, mref, ls, bm2);
           l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
-        fence_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
@@ -459,28 +467,22 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       oph ^= 1u;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      const bool store = qpos < S;
-      __half* orow = args.o16 + ((size_t)it.b * S + (store ? qpos : 0)) * D + it.h * HD;
-#pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      const int q0 = it.qb * kAttnBM + warp * 32;  // first query row of this warp
+      const uint32_t rows = __ballot_sync(0xffffffffu, qpos < S);
+      __half* orow0 = args.o16 + ((size_t)it.b * S + q0) * D + it.h * HD;
+      if constexpr (HD == 32) {
         float o[32];
-        tmem_ld32(t_o + c * 32, o);
+        tmem_ld32(t_o, o);
         tmem_wait_ld();
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            __half2 h0 = __floats2half2_rn(o[g * 8 + 0] * inv, o[g * 8 + 1] * inv);
-            __half2 h1 = __floats2half2_rn(o[g * 8 + 2] * inv, o[g * 8 + 3] * inv);
-            __half2 h2 = __floats2half2_rn(o[g * 8 + 4] * inv, o[g * 8 + 5] * inv);
-            __half2 h3 = __floats2half2_rn(o[g * 8 + 6] * inv, o[g * 8 + 7] * inv);
-            uint4 u;
-            u.x = *reinterpret_cast<uint32_t*>(&h0);
-            u.y = *reinterpret_cast<uint32_t*>(&h1);
-            u.z = *reinterpret_cast<uint32_t*>(&h2);
-            u.w = *reinterpret_cast<uint32_t*>(&h3);
-            dst[g] = u;
-          }
+        xp_store_f16<32>(xst, lane, o, orow0, nullptr, D, rows, inv);
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < HD / 64; ++c) {
+          float o[64];
+          tmem_ld32(t_o + c * 64, o);
+          tmem_ld32(t_o + c * 64 + 32, o + 32);
+          tmem_wait_ld();
+          xp_store_f16<64>(xst, lane, o, orow0 + c * 64, nullptr, D, rows, inv);
         }
       }
       tc_fence_before();

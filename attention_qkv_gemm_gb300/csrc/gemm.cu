@@ -18,7 +18,7 @@
 //
 // Epilogues (the row-wise work of section 1.A fused into the GEMM):
 //   EPI_BIAS_F16       QKV projection: c16 = acc + b_qkv
-//   EPI_BIAS_GELU_F16  FFN-in: c16 = GELU_erf(acc + b1) (hi [+ lo] planes)
+//   EPI_BIAS_GELU_F16  FFN-in: c16 = GELU(acc + b1), exact-erf form (hi [+ lo] planes)
 //   EPI_BIAS_RES_F32   o_proj / FFN-out when d_model > 128: h = acc + b + res
 //   EPI_BIAS_RES_ROW   o_proj / FFN-out when d_model == 128: residual add and
 //                      fp32 row LayerNorm(s): normed fp16 (hi [+ lo]) for the
@@ -35,6 +35,8 @@
 // writes their zeros without waiting for an MMA.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "mathfn.cuh"
+#include "xpose.cuh"
 
 namespace tfl {
 
@@ -46,42 +48,17 @@ struct GemmCfg {
   static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;
   static constexpr int B_BYTES = BN * kGemmBK * 2;
   static constexpr int STAGE = A_BYTES * (1 + AS) + B_BYTES * (1 + WS);
-  static constexpr int STAGES = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
+  static constexpr int RED_BYTES = 4 * 2 * kGemmBM * 4;     // row-statistics exchange (EPI_BIAS_RES_ROW)
+  static constexpr int XPOSE_BYTES = kEpiWarps * 32 * 128;  // one 32 x 128 B transpose stage per epilogue warp
+  static constexpr int RING_MAX = 232448 - 1024 - RED_BYTES - XPOSE_BYTES - 256;
+  static constexpr int STAGES = RING_MAX / STAGE > 8 ? 8 : RING_MAX / STAGE;
   static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  static constexpr int RED_BYTES = 4 * 2 * kGemmBM * 4;  // row-statistics exchange (EPI_BIAS_RES_ROW)
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + RED_BYTES + 256;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + RED_BYTES + XPOSE_BYTES + 256;
 };
-
-__device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.7071067811865476f)); }
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Store 32 values as fp16 (and, when lo != nullptr, their rounding residuals as a second plane).
-__device__ __forceinline__ void store_f16x32(__half* hi, __half* lo, const float* v) {
-  uint4* dh = reinterpret_cast<uint4*>(hi);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 u;
-    u.x = pack_h2(v[8 * i + 0], v[8 * i + 1]);
-    u.y = pack_h2(v[8 * i + 2], v[8 * i + 3]);
-    u.z = pack_h2(v[8 * i + 4], v[8 * i + 5]);
-    u.w = pack_h2(v[8 * i + 6], v[8 * i + 7]);
-    dh[i] = u;
-    if (lo != nullptr) {
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-      uint32_t r[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const __half2 hh = *reinterpret_cast<const __half2*>(&w[k]);
-        const float2 f = __half22float2(hh);
-        r[k] = pack_h2(v[8 * i + 2 * k] - f.x, v[8 * i + 2 * k + 1] - f.y);
-      }
-      reinterpret_cast<uint4*>(lo)[i] = make_uint4(r[0], r[1], r[2], r[3]);
-    }
-  }
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
@@ -117,7 +94,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red = reinterpret_cast<float*>(smem + (size_t)C::STAGES * C::STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)C::STAGES * C::STAGE + C::RED_BYTES);
+  uint8_t* xpose = smem + (size_t)C::STAGES * C::STAGE + C::RED_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(xpose + C::XPOSE_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* accf = empty + C::STAGES;
   uint64_t* acce = accf + 2;
@@ -241,7 +219,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr int NH = BN / 2;  // columns per epilogue warp
     const int q = warp & 3;     // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;
-    const int r = q * 32 + lane;
+    const int c0 = half * NH;   // first tile column of this warp
+    uint8_t* st = xpose + (warp - 2) * 4096;
     const float sc = args.acc_scale;
     WaitCtl ewc = wc;
     ewc.early_exit = false;  // the epilogue warps meet at a named barrier: leave only on their own bound
@@ -249,143 +228,139 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const int mb = t / num_n, nb = t - mb * num_n;
-      const int m = mb * kGemmBM + r;
+      const int m0w = mb * kGemmBM + q * 32;  // first row of this warp's 32 rows
+      const int m = m0w + lane;
+      const uint32_t in_rows = __ballot_sync(0xffffffffu, m < M);
+      const uint32_t valid_rows = __ballot_sync(0xffffffffu, m < M && row_valid(m, S, lengths));
       if (!rows_live(mb * kGemmBM, min(mb * kGemmBM + kGemmBM, M), S, lengths)) {
         if constexpr (EPI == EPI_BIAS_RES_ROW) {
-          if ((args.row.flags & ROW_FINAL) && m < M) {
-            float4* o = reinterpret_cast<float4*>(args.row.out32 + (size_t)m * BN + half * NH);
+          if (args.row.flags & ROW_FINAL) {
+            float z[32];
 #pragma unroll
-            for (int i = 0; i < NH / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < NH / 32; ++c)
+              xp_store_f32x32(st, lane, z, args.row.out32 + (size_t)m0w * BN + c0 + c * 32, BN, in_rows);
           }
         }
         continue;
       }
+      uint4 pre[8];  // EPI_BIAS_RES_ROW: first 32 residual columns, fetched before the wait
+      if constexpr (EPI == EPI_BIAS_RES_ROW)
+        XStage<128>::fetch_rows(lane, reinterpret_cast<const uint8_t*>(args.res + (size_t)m0w * BN + c0), BN * 4,
+                                valid_rows, pre);
       if (!wait_bounded(&accf[acc], acc_phase, ewc)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * NH);
-      const bool in_range = m < M;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
 
-      if constexpr (EPI == EPI_BIAS_F16 || EPI == EPI_BIAS_GELU_F16 || EPI == EPI_BIAS_RES_F32) {
-        float v[NH];
+      if constexpr (EPI == EPI_BIAS_F16 || EPI == EPI_BIAS_GELU_F16) {
+#pragma unroll 1
+        for (int g = 0; g < NH / 64; ++g) {
+          float v[64];
+          tmem_ld32(tb + g * 64, v);
+          tmem_ld32(tb + g * 64 + 32, v + 32);
+          tmem_wait_ld();
+          const int n0 = nb * BN + c0 + g * 64;
+          const float4* bp = reinterpret_cast<const float4*>(args.bias + n0);
 #pragma unroll
-        for (int c = 0; c < NH / 32; ++c) tmem_ld32(tb + c * 32, v + c * 32);
-        tmem_wait_ld();
-        if (in_range) {
-          const int n0 = nb * BN + half * NH;
-          const bool valid = (EPI == EPI_BIAS_RES_F32) && row_valid(m, S, lengths);
-#pragma unroll
-          for (int c = 0; c < NH / 32; ++c) {
-            float* w = v + c * 32;
-            const float4* bp = reinterpret_cast<const float4*>(args.bias + n0 + c * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 b4 = __ldg(bp + i);
-              w[4 * i + 0] = fmaf(w[4 * i + 0], sc, b4.x);
-              w[4 * i + 1] = fmaf(w[4 * i + 1], sc, b4.y);
-              w[4 * i + 2] = fmaf(w[4 * i + 2], sc, b4.z);
-              w[4 * i + 3] = fmaf(w[4 * i + 3], sc, b4.w);
-            }
-            if constexpr (EPI == EPI_BIAS_GELU_F16) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) w[i] = gelu_erf(w[i]);
-            }
-            if constexpr (EPI == EPI_BIAS_RES_F32) {
-              const size_t off = (size_t)m * args.N + n0 + c * 32;
-              if (valid) {
-                const float4* rp = reinterpret_cast<const float4*>(args.res + off);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float4 r4 = rp[i];
-                  w[4 * i + 0] += r4.x;
-                  w[4 * i + 1] += r4.y;
-                  w[4 * i + 2] += r4.z;
-                  w[4 * i + 3] += r4.w;
-                }
-              }
-              float4* hp = reinterpret_cast<float4*>(args.h32 + off);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) hp[i] = make_float4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-            } else {
-              const size_t off = (size_t)m * args.N + n0 + c * 32;
-              store_f16x32(args.c16 + off, args.c16lo ? args.c16lo + off : nullptr, w);
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float4 b4 = __ldg(bp + i);
+            v[4 * i + 0] = fmaf(v[4 * i + 0], sc, b4.x);
+            v[4 * i + 1] = fmaf(v[4 * i + 1], sc, b4.y);
+            v[4 * i + 2] = fmaf(v[4 * i + 2], sc, b4.z);
+            v[4 * i + 3] = fmaf(v[4 * i + 3], sc, b4.w);
           }
+          if constexpr (EPI == EPI_BIAS_GELU_F16) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = gelu_as7126(v[i]);
+          }
+          const size_t off = (size_t)m0w * args.N + n0;
+          xp_store_f16<64>(st, lane, v, args.c16 + off, args.c16lo ? args.c16lo + off : nullptr, args.N, in_rows);
+        }
+      } else if constexpr (EPI == EPI_BIAS_RES_F32) {
+#pragma unroll 1
+        for (int c = 0; c < NH / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + c * 32, v);
+          tmem_wait_ld();
+          const int n0 = nb * BN + c0 + c * 32;
+          const float4* bp = reinterpret_cast<const float4*>(args.bias + n0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 b4 = __ldg(bp + i);
+            v[4 * i + 0] = fmaf(v[4 * i + 0], sc, b4.x);
+            v[4 * i + 1] = fmaf(v[4 * i + 1], sc, b4.y);
+            v[4 * i + 2] = fmaf(v[4 * i + 2], sc, b4.z);
+            v[4 * i + 3] = fmaf(v[4 * i + 3], sc, b4.w);
+          }
+          const size_t off = (size_t)m0w * args.N + n0;
+          xp_add_f32x32(st, lane, v, args.res + off, args.N, valid_rows);
+          xp_store_f32x32(st, lane, v, args.h32 + off, args.N, in_rows);
         }
       } else {
         // EPI_BIAS_RES_ROW: BN == N == d_model; this thread owns half of row m.
-        float t[NH];
+        float tv[NH];
 #pragma unroll
-        for (int c = 0; c < NH / 32; ++c) tmem_ld32(tb + c * 32, t + c * 32);
+        for (int c = 0; c < NH / 32; ++c) tmem_ld32(tb + c * 32, tv + c * 32);
         tmem_wait_ld();
         const RowOps& ro = args.row;
-        const bool valid = in_range && row_valid(m, S, lengths);
-        const int c0 = half * NH;
+        const bool valid = (valid_rows >> lane) & 1u;
+        const int r = q * 32 + lane;
         {
           const float4* bp = reinterpret_cast<const float4*>(args.bias + c0);
 #pragma unroll
           for (int i = 0; i < NH / 4; ++i) {
             const float4 b4 = __ldg(bp + i);
-            t[4 * i + 0] = fmaf(t[4 * i + 0], sc, b4.x);
-            t[4 * i + 1] = fmaf(t[4 * i + 1], sc, b4.y);
-            t[4 * i + 2] = fmaf(t[4 * i + 2], sc, b4.z);
-            t[4 * i + 3] = fmaf(t[4 * i + 3], sc, b4.w);
+            tv[4 * i + 0] = fmaf(tv[4 * i + 0], sc, b4.x);
+            tv[4 * i + 1] = fmaf(tv[4 * i + 1], sc, b4.y);
+            tv[4 * i + 2] = fmaf(tv[4 * i + 2], sc, b4.z);
+            tv[4 * i + 3] = fmaf(tv[4 * i + 3], sc, b4.w);
           }
         }
-        if (valid) {
-          const float4* rp = reinterpret_cast<const float4*>(args.res + (size_t)m * BN + c0);
+        xp_add_fetched_f32x32(st, lane, tv, pre);
 #pragma unroll
-          for (int i = 0; i < NH / 4; ++i) {
-            const float4 r4 = rp[i];
-            t[4 * i + 0] += r4.x;
-            t[4 * i + 1] += r4.y;
-            t[4 * i + 2] += r4.z;
-            t[4 * i + 3] += r4.w;
-          }
-        }
+        for (int c = 1; c < NH / 32; ++c)
+          xp_add_f32x32(st, lane, tv + c * 32, args.res + (size_t)m0w * BN + c0 + c * 32, BN, valid_rows);
         float mean, rstd;
         int slot = 0;
         if (ro.flags & ROW_POST_LN) {
-          row_stats_split<NH>(t, ro.eps, red, slot, half, r, mean, rstd);
+          row_stats_split<NH>(tv, ro.eps, red, slot, half, r, mean, rstd);
           slot += 2;
 #pragma unroll
-          for (int i = 0; i < NH; ++i) t[i] = (t[i] - mean) * rstd * __ldg(ro.ga + c0 + i) + __ldg(ro.ba + c0 + i);
+          for (int i = 0; i < NH; ++i)
+            tv[i] = (tv[i] - mean) * rstd * __ldg(ro.ga + c0 + i) + __ldg(ro.ba + c0 + i);
         }
-        if ((ro.flags & ROW_WRITE_H) && in_range) {
-          float4* hp = reinterpret_cast<float4*>(ro.h32 + (size_t)m * BN + c0);
+        if (ro.flags & ROW_WRITE_H) {
 #pragma unroll
-          for (int i = 0; i < NH / 4; ++i) hp[i] = make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
+          for (int c = 0; c < NH / 32; ++c)
+            xp_store_f32x32(st, lane, tv + c * 32, ro.h32 + (size_t)m0w * BN + c0 + c * 32, BN, in_rows);
         }
         if (ro.flags & (ROW_FINAL | ROW_NORM16)) {
-          row_stats_split<NH>(t, ro.eps, red, slot, half, r, mean, rstd);
+          row_stats_split<NH>(tv, ro.eps, red, slot, half, r, mean, rstd);
           const bool fin = (ro.flags & ROW_FINAL) != 0;
           const float* g = fin ? ro.gf : ro.gb;
           const float* bb = fin ? ro.bf : ro.bb;
 #pragma unroll
-          for (int i = 0; i < NH; ++i) t[i] = (t[i] - mean) * rstd * __ldg(g + c0 + i) + __ldg(bb + c0 + i);
-          if (in_range) {
-            if (fin) {
-              float4* op = reinterpret_cast<float4*>(ro.out32 + (size_t)m * BN + c0);
-              if (valid) {
+          for (int i = 0; i < NH; ++i) {
+            const float y = (tv[i] - mean) * rstd * __ldg(g + c0 + i) + __ldg(bb + c0 + i);
+            tv[i] = (fin && !valid) ? 0.f : y;
+          }
+          if (fin) {
 #pragma unroll
-                for (int i = 0; i < NH / 4; ++i)
-                  op[i] = make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
-              } else {
+            for (int c = 0; c < NH / 32; ++c)
+              xp_store_f32x32(st, lane, tv + c * 32, ro.out32 + (size_t)m0w * BN + c0 + c * 32, BN, in_rows);
+          } else {
 #pragma unroll
-                for (int i = 0; i < NH / 4; ++i) op[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < NH / 32; ++c) {
-                const size_t off = (size_t)m * BN + c0 + c * 32;
-                store_f16x32(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, t + c * 32);
-              }
+            for (int c = 0; c < NH / 64; ++c) {
+              const size_t off = (size_t)m0w * BN + c0 + c * 64;
+              xp_store_f16<64>(st, lane, tv + c * 64, ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, BN, in_rows);
             }
           }
-        } else if ((ro.flags & ROW_CAST16) && in_range) {
+        } else if (ro.flags & ROW_CAST16) {
 #pragma unroll
-          for (int c = 0; c < NH / 32; ++c) {
-            const size_t off = (size_t)m * BN + c0 + c * 32;
-            store_f16x32(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, t + c * 32);
+          for (int c = 0; c < NH / 64; ++c) {
+            const size_t off = (size_t)m0w * BN + c0 + c * 64;
+            xp_store_f16<64>(st, lane, tv + c * 64, ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, BN, in_rows);
           }
         }
       }

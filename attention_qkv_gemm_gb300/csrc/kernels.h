@@ -85,6 +85,31 @@ struct RowArgs {
 // One-time kernel attributes (dynamic shared memory opt-in); call before any capture.
 cudaError_t prepare_gemm_kernels();
 cudaError_t prepare_attention_kernels();
+cudaError_t prepare_postchain_kernel();
+
+// Fused post-attention chain (d_model = 128): o_proj + residual (+LN) -> LN ->
+// FFN-in + GELU -> FFN-out + residual -> next LN / tail.  Operands split as
+// at precision 2 (weights hi/lo; normed rows and GELU output hi/lo in TMEM).
+struct ChainArgs {
+  Common c;
+  int F = 0;
+  float eps = 1e-5f;
+  int post_ln = 0;  // 1: h = LN1(h + attn), h = LN2(h + FFN)
+  int last = 0;     // 1: write the model tail (final LN + pad-mask) to out32
+  float scale_o = 1.f, scale_1 = 1.f, scale_2 = 1.f;  // weight pre-scales undone
+  const float *bo = nullptr, *b1 = nullptr, *b2 = nullptr;
+  const float *ln1_g = nullptr, *ln1_b = nullptr, *ln2_g = nullptr, *ln2_b = nullptr;
+  const float *lnn_g = nullptr, *lnn_b = nullptr;  // next layer's LN1 (pre-LN, not last)
+  const float *lnf_g = nullptr, *lnf_b = nullptr;  // final LN (last)
+  const float* res = nullptr;                      // residual in: x (layer 0) or h32
+  float* h32 = nullptr;                            // residual out (not last)
+  __half *n16 = nullptr, *n16lo = nullptr;         // next layer's QKV input, hi/lo (not last)
+  float* out32 = nullptr;                          // model output (last)
+};
+
+struct ChainMaps {
+  CUtensorMap o, wo, wo_lo, w1, w1_lo, w2, w2_lo;
+};
 
 // TMA descriptors of one GEMM: A (and its lo plane), W (and its lo part).
 struct GemmMaps {
@@ -98,6 +123,8 @@ cudaError_t launch_gemm(int bn, int epi, int as, int ws, const GemmMaps& mp, con
 cudaError_t launch_attention(int hd, const CUtensorMap& tq, const CUtensorMap& tkv, const AttnArgs& a,
                              int num_sms, cudaStream_t s);
 cudaError_t launch_rows(const RowArgs& a, cudaStream_t s);
+cudaError_t launch_postchain(const ChainMaps& mp, const ChainArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_gelu_selftest(int n, unsigned* out, cudaStream_t s);
 cudaError_t launch_check_lengths(const int* lengths, int B, int S, int* status, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s);
 cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s);

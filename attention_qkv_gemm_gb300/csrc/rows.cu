@@ -10,6 +10,7 @@
 // add-LayerNorm that follows each residual GEMM and the model tail (final
 // LayerNorm + pad-mask + fp32 output).
 #include "kernels.h"
+#include "mathfn.cuh"
 #include "ptx.cuh"
 
 namespace tfl {
@@ -200,6 +201,23 @@ __global__ void probe_wait_kernel(int* status, int64_t timeout_ns) {
     wait_bounded(&bar, 0, wc);
   }
   __syncthreads();
+}
+
+// Largest |gelu_as7126(x) - gelu_erff(x)| over n points evenly spaced on [-12, 12].
+__global__ void gelu_selftest_kernel(int n, unsigned* out) {
+  float m = 0.f;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const float x = -12.0f + 24.0f * (float)i / (float)(n - 1);
+    m = fmaxf(m, fabsf(gelu_as7126(x) - gelu_erff(x)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+}
+
+cudaError_t launch_gelu_selftest(int n, unsigned* out, cudaStream_t s) {
+  gelu_selftest_kernel<<<64, 256, 0, s>>>(n, out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_probe_wait(int* status, int64_t timeout_ns, cudaStream_t s) {

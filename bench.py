@@ -133,6 +133,9 @@ def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
         "gemm_oproj": valid * (D * 2 + D * 4 + D * 4 + D * 2),
         "gemm_ffn2": valid * (F * 2 + D * 4 + D * 4 + D * 2),
         "rownorm": valid * (D * 4 + D * 2),
+        # o_proj .. FFN-out fused (d_model 128): attention output in, residual in/out,
+        # next layer's normed rows out as fp16 hi/lo planes
+        "postchain": valid * (D * 2 + D * 4 + D * 4 + 2 * D * 2),
     }.get(kind)
 
 

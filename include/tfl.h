@@ -171,9 +171,18 @@ const char* tfl_last_error(void);
 #define TFL_KIND_GEMM_OPROJ 4
 #define TFL_KIND_GEMM_FFN1 5
 #define TFL_KIND_GEMM_FFN2 6
+#define TFL_KIND_POSTCHAIN 7   /* d_model 128: o_proj .. FFN-out .. next LayerNorm fused */
 int tfl_profile_forward(tfl_handle* h, const float* x, const int32_t* lengths,
                         int causal, float* out, tfl_stream stream,
                         float* kernel_ms, int32_t* kernel_kind, int32_t cap, int32_t* n);
+
+/*
+ * Self-test of the epilogues' GELU (exact-erf form evaluated with erf from
+ * Abramowitz & Stegun 7.1.26): writes the largest |difference| from a GELU
+ * built on CUDA's erff over n >= 2 points evenly spaced on [-12, 12].
+ * Synchronizes `stream`.  Errors: INVALID_ARG, CUDA.
+ */
+int tfl_selftest_gelu(int32_t n, float* max_abs_diff, tfl_stream stream);
 
 /* Number of kernel launches one tfl_forward makes for this handle and causal flag. */
 int tfl_launch_count(const tfl_handle* h, int causal);

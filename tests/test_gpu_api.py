@@ -101,3 +101,11 @@ def test_profile_forward_reports_every_launch():
             assert all(ms > 0 for _, ms in prof)
         finally:
             m.close()
+
+
+def test_gelu_matches_erff_gelu():
+    import attention_qkv_gemm_gb300 as pkg
+    # A&S 7.1.26 bounds |erf error| by 1.5e-7, so |GELU error| <= 0.75e-7 |x| <= 9e-7 on [-12, 12],
+    # plus the rounding of the MUFU reciprocal / exponential and of erff itself
+    d = pkg.tfl_selftest_gelu(1 << 20)
+    assert d < 2e-6, d
