@@ -139,6 +139,32 @@ def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
     }.get(kind)
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of the benchmark workload (summaries in profiles/), valid only while the
+# kernel's source file is unchanged (sha256 prefix); otherwise traffic is reported null.
+NCU_TRAFFIC = {
+    ("postchain", "B64_S1024_D128_causal_ragged"):
+        ("attention_qkv_gemm_gb300/csrc/postchain.cu", "7b1481155367", 40.311296e6 + 10.486016e6),
+    ("attention", "B64_S1024_D128_causal_ragged"):
+        ("attention_qkv_gemm_gb300/csrc/attention.cu", "d63c1b8b8d1a", 41.476608e6 + 0.4736e6),
+    ("gemm_qkv", "B64_S1024_D128_causal_ragged"):
+        ("attention_qkv_gemm_gb300/csrc/gemm.cu", "fd2104ecbbcd", 27.823872e6 + 0.707328e6),
+}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    import hashlib
+    e = NCU_TRAFFIC.get((kernel, workload))
+    if e is None:
+        return None
+    path, sha, nbytes = e
+    try:
+        cur = hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:12]
+    except OSError:
+        return None
+    return nbytes if cur == sha else None
+
+
 def run_oracle_sample(shape, prm, seed, n_seq):
     import oracle
     lens = synth.lengths(seed, shape)
@@ -285,14 +311,15 @@ def main():
         achieved = exps / (dom_ms_launch / 1e3) / 1e9
         peak = MUFU_PER_CLK_PER_SM * 152 * peaks["sm_max_mhz"] * 1e6 / 1e9
         roof = {"kernel": "attention", "bound": "alu", "achieved": achieved, "peak": peak, "unit": "Gexp2/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": ncu_traffic("attention", shape.name),
                 "note": "MUFU ex2 rate: 16/clk/SM x 152 SMs x max SM clock; per launch = causal pairs x heads",
                 "tensor_tflops": alg["attn_flops_per_launch"] / (dom_ms_launch / 1e3) / 1e12}
     else:
         by = kernel_bytes(dom, shape, alg["valid_tokens"])
         achieved = by / (dom_ms_launch / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom, shape.name),
+                "algorithmic_bytes_per_launch": by}
     roof["peak_source"] = peaks["source"]
     roof["launch_ms"] = dom_ms_launch
     roof["kernels_ms_per_forward"] = {k: round(v[0], 4) for k, v in per_kind.items()}
