@@ -3,20 +3,26 @@
 // Per (sequence b, head h, block of 128 queries) the kernel computes
 // O = softmax(Q K^T / sqrt(hd) + mask) V without materialising the score
 // matrix ("TikTok TechJam 2026 -- Problem 3", section 2.1):
-//   * S = Q K_j^T for one key block at a time goes to tensor memory (fp32).
+//   * Keys are taken in sub-blocks of 64.  S = Q K_u^T of sub-block u goes to
+//     tensor memory (fp32), in one of two buffers, so the tensor cores compute
+//     S of sub-block u + 2 while the softmax warps still work on u.
 //   * Online softmax in fp32, one query row per thread (the row's TMEM lane):
 //     running max m, running sum l, O rescaled by exp(m_old - m_new)
-//     (section 2.1, the running-max recurrence).  The rescale is lazy: the
-//     reference max only moves when the row max grew by more than 8 in log2
-//     units, so P <= 2^8 and O is touched rarely; O / l is exact either way.
+//     (section 2.1, the running-max recurrence).  The row max of a sub-block
+//     is taken from registers before its exponentials, and the rescale is
+//     lazy: the reference max only moves when the row max grew by more than 8
+//     in log2 units, so P <= 2^8 and O is touched rarely; O / l is exact
+//     either way.
 //   * P = exp2(S * log2(e)/sqrt(hd) - m) in fp16 goes to tensor memory (two
-//     values per column) and O += P V_j takes its A operand from there
-//     (tcgen05.mma with A in TMEM), so only V is read from shared memory.
+//     values per column, double-buffered) and O += P V_u takes its A operand
+//     from there (tcgen05.mma with A in TMEM), so only V is read from shared
+//     memory.
 //   * Causal: key blocks above the diagonal are never loaded (block skipping,
-//     section 1.C); the mask is applied only on the diagonal block; the key
-//     mask is not applied at all, because for a valid query i every key j <= i
-//     is valid (section 2.1, "the mask trick").
-//   * Key padding (non-causal): only the block holding len_b is masked.
+//     section 1.C); a warp whose 32 rows lie entirely below a sub-block skips
+//     it, and only sub-blocks crossing the diagonal are masked per key; the
+//     key mask is not applied at all, because for a valid query i every key
+//     j <= i is valid (section 2.1, "the mask trick").
+//   * Key padding (non-causal): only the sub-block holding len_b is masked.
 //   * Query blocks past len_b are skipped; their output rows are never read
 //     for a valid token.
 // q, k, v are strided views of the fused QKV output [B, S, 3D] (section 1.A,
@@ -28,11 +34,6 @@
 // atomic counter, heaviest first (causal: the last query blocks have the most
 // keys); the producer publishes each claimed item to the other warps through
 // a small shared-memory ring.
-//
-// Softmax fast path: for key blocks after the first, P is computed in one
-// pass over S with the running max as the exponent reference while the block
-// max is tracked; only when a row's max grew by more than 2^8 does its warp
-// redo the block with the two-pass path (block max, rescale O, exponentials).
 #include <type_traits>
 
 #include "kernels.h"
@@ -54,8 +55,17 @@ struct AttnCfg {
   static constexpr int XP_BYTES = 4 * 32 * 128;     // output transpose stage, one per softmax warp
   static constexpr int NST = HD == 32 ? 4 : 2;
   static constexpr int CTAS_PER_SM = HD <= 64 ? 2 : 1;
-  // tensor memory: S [0, BN), P (fp16 pairs) [BN, BN + BN/2), O from O_COL
-  static constexpr int P_COL = BN;
+  // Keys are taken 64 at a time (a sub-block; a K/V stage holds BN / 64 of
+  // them).  Tensor memory: S[b] (fp32) at 64 b and P[b] (fp16 pairs) at
+  // 128 + 32 b for the two sub-block buffers b, O from O_COL.
+  static constexpr int SUB = 64;
+  static constexpr int SUBS = BN / SUB;
+  static constexpr int S_COL = 0;
+  static constexpr int P_COL = 128;
+  // QK^T runs this many sub-blocks ahead of P V: at most 2 (two S buffers)
+  // and below the sub-blocks the K/V ring holds, since the ring slot of
+  // sub-block u + LOOKAHEAD is freed by a P V issued before it.
+  static constexpr int LOOKAHEAD = NST * SUBS >= 3 ? 2 : 1;
   static constexpr int O_COL = HD <= 64 ? 192 : 256;
   static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
   static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)NST * 2 * KV_BYTES + XP_BYTES + 384;
@@ -90,6 +100,16 @@ __device__ __forceinline__ bool decode_item(int i, const AttnArgs& a, int nqb, i
   return true;
 }
 
+// How a warp's rows meet a sub-block's keys (see the softmax loop).
+enum SubMode { kFull = 0, kNone = 1, kTriLo = 2, kTriHi = 3, kKeyPad = 4 };
+
+// Sub-blocks of 64 keys an item visits: keys [0, kend) with kend the last
+// allowed key + 1 (causal: the block's last query; otherwise len_b).
+__device__ __forceinline__ int item_subblocks(const Item& it, int causal) {
+  const int kend = causal ? min((it.qb + 1) * kAttnBM, it.len) : it.len;
+  return (kend + 63) / 64;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
@@ -105,12 +125,14 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sX + C::XP_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* s_full = bars + 2;
-  uint64_t* p_full = bars + 3;
-  uint64_t* o_full = bars + 4;
-  uint64_t* o_empty = bars + 5;
-  uint64_t* drain = bars + 6;
-  uint64_t* kv_full = bars + 7;
+  uint64_t* o_full = bars + 2;
+  uint64_t* o_empty = bars + 3;
+  uint64_t* drain = bars + 4;
+  uint64_t* s_full = bars + 5;   // [2] MMA -> softmax: S[b] computed
+  uint64_t* s_free = bars + 7;   // [2] softmax -> MMA: S[b] read
+  uint64_t* p_full = bars + 9;   // [2] softmax -> MMA: P[b] written
+  uint64_t* pv_done = bars + 11; // [2] MMA -> softmax: P[b] V done (P[b] free, O current)
+  uint64_t* kv_full = bars + 13;
   uint64_t* kv_empty = kv_full + C::NST;
   uint64_t* it_full = kv_empty + C::NST;
   uint64_t* it_empty = it_full + kItemRing;
@@ -123,8 +145,12 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 4);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&pv_done[b], 1);
+    }
     mbar_init(o_full, 1);
     mbar_init(o_empty, 4);
     mbar_init(drain, 1);
@@ -215,20 +241,33 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer (whole warp)
-    constexpr uint32_t idesc_qk = idesc_f16(128, BN, 0, 0);
+    constexpr uint32_t idesc_qk = idesc_f16(128, C::SUB, 0, 0);
     constexpr uint32_t idesc_pv = idesc_f16(128, HD, 0, 1);
-    const uint32_t d_s = tmem_base;
     const uint32_t d_o = tmem_base + C::O_COL;
-    int st = 0, ik = 0;
-    uint32_t kvph = 0, qph = 0, pph = 0, oeph = 0, itph = 0;
+    int st = 0, pst = 0, ik = 0;  // stage of the next QK / of the next PV
+    uint32_t kvph = 0, qph = 0, oeph = 0, itph = 0;
+    uint32_t g = 0;  // sub-blocks of all earlier items: sub-block g uses S/P buffer g & 1
     bool first_item = true, ok = true;
-    const uint32_t t_p = tmem_base + C::P_COL;
-    auto issue_pv = [&](int pst, bool accumulate) {
-      const uint32_t sv = smem_u32(sV + (size_t)pst * C::KV_BYTES);
+    // S[b] = Q K^T for the keys of half h of stage s
+    auto issue_qk = [&](int s, int h, uint32_t b) {
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t sk = smem_u32(sK + (size_t)s * C::KV_BYTES) + h * C::SUB * C::ROWB;
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk) {
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const int a = kk / (C::ATOM_C / 16), w = kk % (C::ATOM_C / 16);
+        const uint64_t ad = sdesc(sq + a * (kAttnBM * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
+        const uint64_t bd = sdesc(sk + a * (BN * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
+        umma_f16(tmem_base + C::S_COL + b * C::SUB, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+      }
+    };
+    // O += P[b] V for the keys of half h of stage s (P from tensor memory)
+    auto issue_pv = [&](int s, int h, uint32_t b, bool accumulate) {
+      const uint32_t sv = smem_u32(sV + (size_t)s * C::KV_BYTES) + h * C::SUB * C::ROWB;
+#pragma unroll
+      for (int kk = 0; kk < C::SUB / 16; ++kk) {
         const uint64_t bd = sdesc(sv + kk * 16 * C::ROWB, BN * C::ROWB, 8 * C::ROWB, C::SWZ);
-        umma_f16_ts(d_o, t_p + kk * 8, bd, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+        umma_f16_ts(d_o, tmem_base + C::P_COL + b * (C::SUB / 2) + kk * 8, bd, idesc_pv,
+                    (accumulate || kk > 0) ? 1u : 0u);
       }
     };
     while (ok) {
@@ -243,143 +282,93 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       if (i < 0) break;
       Item it;
       decode_item(i, args, nqb, BN, it);
+      const int nsub = item_subblocks(it, args.causal);
       if (!wait_bounded(q_full, qph, wc)) break;
       qph ^= 1u;
       tc_fence_after();
-      bool need_oe = !first_item;
-      int prev_st = 0;
-      for (int j = 0; j < it.nkb; ++j) {
-        if (!wait_bounded(&kv_full[st], kvph, wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // Keys at or past len_b in this block: clear their V rows so stale
-        // workspace contents can never reach O through a zero probability.
-        const int vrow0 = it.len - j * BN;
-        if (vrow0 < BN) {
-          uint8_t* v = sV + (size_t)st * C::KV_BYTES;
-          for (int rr = max(vrow0, 0) + lane; rr < BN; rr += 32) {
-#pragma unroll
-            for (int a = 0; a < C::NATOM; ++a) {
-              uint4* row = reinterpret_cast<uint4*>(v + a * (BN * C::ROWB) + rr * C::ROWB);
-#pragma unroll
-              for (int c = 0; c < C::ROWB / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
-            }
-          }
-          fence_async_smem();
-          __syncwarp();
-        }
-        if (j > 0) {
-          if (!wait_bounded(p_full, pph, wc)) {
-            ok = false;
-            break;
-          }
-          pph ^= 1u;
-          if (need_oe) {
-            if (!wait_bounded(o_empty, oeph, wc)) {
-              ok = false;
-              break;
-            }
-            oeph ^= 1u;
-            need_oe = false;
-          }
+      const uint32_t g0 = g;
+      // QK^T of sub-block u, once its keys are resident and its S buffer has been read
+      auto qk = [&](int u) -> bool {
+        const uint32_t gg = g0 + u, b = gg & 1u;
+        const int h = u % C::SUBS;
+        if (h == 0) {
+          if (!wait_bounded(&kv_full[st], kvph, wc)) return false;
           tc_fence_after();
-          if (lane == 0) {
-            issue_pv(prev_st, j - 1 > 0);
-            umma_commit(&kv_empty[prev_st]);
+          // Keys at or past len_b in this stage: clear their V rows so stale
+          // workspace contents can never reach O through a zero probability.
+          const int vrow0 = it.len - (u / C::SUBS) * BN;
+          if (vrow0 < BN) {
+            uint8_t* v = sV + (size_t)st * C::KV_BYTES;
+            for (int rr = max(vrow0, 0) + lane; rr < BN; rr += 32) {
+#pragma unroll
+              for (int a = 0; a < C::NATOM; ++a) {
+                uint4* row = reinterpret_cast<uint4*>(v + a * (BN * C::ROWB) + rr * C::ROWB);
+#pragma unroll
+                for (int c = 0; c < C::ROWB / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
+              }
+            }
+            fence_async_smem();
+            __syncwarp();
           }
+        }
+        if (gg >= 2) {
+          if (!wait_bounded(&s_free[b], ((gg - 2) >> 1) & 1u, wc)) return false;
+          tc_fence_after();
         }
         if (lane == 0) {
-          const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK + (size_t)st * C::KV_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const int a = kk / (C::ATOM_C / 16), w = kk % (C::ATOM_C / 16);
-            const uint64_t ad = sdesc(sq + a * (kAttnBM * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
-            const uint64_t bd = sdesc(sk + a * (BN * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
-            umma_f16(d_s, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-          }
+          issue_qk(st, h, b);
           mma_issued = true;
-          umma_commit(s_full);
-          if (j == it.nkb - 1) umma_commit(q_empty);
+          umma_commit(&s_full[b]);
+          if (u == nsub - 1) umma_commit(q_empty);
         }
         __syncwarp();
-        prev_st = st;
-        if (++st == C::NST) {
-          st = 0;
-          kvph ^= 1u;
+        if (h == C::SUBS - 1 || u == nsub - 1) {
+          if (++st == C::NST) {
+            st = 0;
+            kvph ^= 1u;
+          }
         }
+        return true;
+      };
+      // P V of sub-block u, once its probabilities are in P[b]
+      auto pv = [&](int u) -> bool {
+        const uint32_t gg = g0 + u, b = gg & 1u;
+        const int h = u % C::SUBS;
+        if (!wait_bounded(&p_full[b], (gg >> 1) & 1u, wc)) return false;
+        if (u == 0 && !first_item) {
+          if (!wait_bounded(o_empty, oeph, wc)) return false;
+          oeph ^= 1u;
+        }
+        tc_fence_after();
+        const bool stage_done = h == C::SUBS - 1 || u == nsub - 1;
+        if (lane == 0) {
+          issue_pv(pst, h, b, u > 0);
+          umma_commit(&pv_done[b]);
+          if (stage_done) umma_commit(&kv_empty[pst]);
+          if (u == nsub - 1) umma_commit(o_full);
+        }
+        __syncwarp();
+        if (stage_done && ++pst == C::NST) pst = 0;
+        return true;
+      };
+      for (int u = 0; ok && u < C::LOOKAHEAD && u < nsub; ++u) ok = qk(u);
+      for (int u = 0; ok && u < nsub; ++u) {
+        if (u + C::LOOKAHEAD < nsub && !qk(u + C::LOOKAHEAD)) ok = false;
+        else if (!pv(u)) ok = false;
       }
       if (!ok) break;
-      if (!wait_bounded(p_full, pph, wc)) break;
-      pph ^= 1u;
-      if (need_oe) {
-        if (!wait_bounded(o_empty, oeph, wc)) break;
-        oeph ^= 1u;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        issue_pv(prev_st, it.nkb > 1);
-        umma_commit(&kv_empty[prev_st]);
-        umma_commit(o_full);
-      }
-      __syncwarp();
+      g = g0 + nsub;
       first_item = false;
     }
   } else {
     // ------------------------------------------------------------ softmax + output (warps 0-3)
     const int r = warp * 32 + lane;  // query row within the block == TMEM lane
-    const uint32_t t_s = tmem_base + ((uint32_t)(warp * 32) << 16);
-    const uint32_t t_o = t_s + C::O_COL;
-    const uint32_t t_p = t_s + C::P_COL;
+    const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_o = t_row + C::O_COL;
     const float sl2 = args.scale_log2;
-    uint32_t sph = 0, oph = 0, itph = 0;
+    uint32_t oph = 0, itph = 0, g = 0;
     int ik = 0;
     uint8_t* xst = sX + warp * 4096;
-
-    // exponentials of one 64-key group against reference mref, packed as fp16
-    // pairs into this row's 32 P columns of group g; returns the group's sum in
-    // four partials and its max.  MASKED: keys past kmax get p = 0 and no max.
-    auto exp_group = [&](auto masked, const float* sv, int g, int kbase, int kmax, float mref, float* ls,
-                         float* bm) {
-      constexpr bool MASKED = decltype(masked)::value;
-      uint32_t pk[32];
-#pragma unroll
-      for (int e2 = 0; e2 < 32; ++e2) {
-        float p2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int idx = 2 * e2 + u;
-          const float v = sv[idx];
-          if constexpr (MASKED) {
-            const bool ok2 = kbase + idx <= kmax;
-            bm[idx & 3] = ok2 ? fmaxf(bm[idx & 3], v) : bm[idx & 3];
-            p2[u] = ok2 ? ex2(fmaf(v, sl2, -mref)) : 0.f;
-          } else {
-            bm[idx & 3] = fmaxf(bm[idx & 3], v);
-            p2[u] = ex2(fmaf(v, sl2, -mref));
-          }
-          ls[idx & 3] += p2[u];
-        }
-        const __half2 hp = __floats2half2_rn(p2[0], p2[1]);  // first key in the low half
-        pk[e2] = *reinterpret_cast<const uint32_t*>(&hp);
-      }
-      tmem_st32_u(t_p + g * 32, pk);
-    };
-    // one pass over S against reference mref: P into TMEM, partial sums and maxima
-    auto exp_block = [&](bool need_mask, int k0, int kmax, float mref, float* ls, float* bm) {
-#pragma unroll
-      for (int g = 0; g < BN / 64; ++g) {
-        float sv[64];
-        tmem_ld32(t_s + g * 64, sv);
-        tmem_ld32(t_s + g * 64 + 32, sv + 32);
-        tmem_wait_ld();
-        if (need_mask)
-          exp_group(std::true_type{}, sv, g, k0 + g * 64, kmax, mref, ls, bm);
-        else
-          exp_group(std::false_type{}, sv, g, k0 + g * 64, kmax, mref, ls, bm);
-      }
-    };
 
     while (true) {
       if (!wait_bounded(&it_full[ik], itph, wc)) break;
@@ -393,74 +382,137 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       if (i < 0) break;
       Item it;
       decode_item(i, args, nqb, BN, it);
+      const int nsub = item_subblocks(it, args.causal);
       const int qpos = it.qb * kAttnBM + r;
+      const int wq0 = it.qb * kAttnBM + warp * 32;       // first query row of this warp
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
-      for (int j = 0; j < it.nkb; ++j) {
-        if (!wait_bounded(s_full, sph, wc)) {
+      for (int u = 0; u < nsub; ++u, ++g) {
+        const uint32_t b = g & 1u;
+        const int k0 = u * C::SUB;
+        // How this warp's 32 rows meet the sub-block's 64 keys.  Causal: with
+        // d = (first row of the warp) - k0, d >= 63 is unmasked, d <= -32 is
+        // entirely above the diagonal (P = 0, nothing computed), and d = 0 / 32
+        // (the only other values: query blocks are 128-row and sub-blocks
+        // 64-key aligned) mask one 32-key half triangularly.  Key padding
+        // masks the keys at or past len_b, the same for every row.
+        int mode;
+        if (args.causal) {
+          const int d = wq0 - k0;
+          mode = d >= C::SUB - 1 ? kFull : d <= -32 ? kNone : d == 0 ? kTriLo : kTriHi;
+        } else {
+          mode = k0 + C::SUB > it.len ? kKeyPad : kFull;
+        }
+        if (!wait_bounded(&s_full[b], (g >> 1) & 1u, wc)) {
           ok = false;
           break;
         }
-        sph ^= 1u;
         tc_fence_after();
-        const int k0 = j * BN;
-        const bool need_mask = args.causal ? (k0 + BN - 1 > it.qb * kAttnBM) : (k0 + BN > it.len);
-        const int kmax = args.causal ? qpos : it.len - 1;  // last allowed key when masking
-        bool slow = (j == 0);
-        if (!slow) {
-          // fast path: exponentials against the running max, block max tracked alongside
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
-          float bm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          exp_block(need_mask, k0, kmax, m_run, ls, bm);
-          const float bmax = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
-          slow = __any_sync(0xffffffffu, bmax * sl2 > m_run + 8.0f);
-          if (!slow) l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        uint32_t pk[C::SUB / 2];
+        float sv[C::SUB];
+        const uint32_t t_s = t_row + C::S_COL + b * C::SUB;
+        if (mode != kNone) {
+          tmem_ld32(t_s, sv);
+          if (mode != kTriLo) tmem_ld32(t_s + 32, sv + 32);
+          tmem_wait_ld();
         }
-        if (slow) {
-          // pass 1: block max
-          float bm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-          for (int g = 0; g < BN / 64; ++g) {
-            float sv[64];
-            tmem_ld32(t_s + g * 64, sv);
-            tmem_ld32(t_s + g * 64 + 32, sv + 32);
-            tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[b]);  // S[b] may now take sub-block g + 2
+        if (mode == kNone) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-              const bool ok2 = !need_mask || (k0 + g * 64 + e <= kmax);
-              bm[e & 3] = ok2 ? fmaxf(bm[e & 3], sv[e]) : bm[e & 3];
+          for (int e = 0; e < C::SUB / 2; ++e) pk[e] = 0u;
+        } else {
+          if (mode == kTriLo) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[e] = e <= lane ? sv[e] : -INFINITY;
+          } else if (mode == kTriHi) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[32 + e] = e <= lane ? sv[32 + e] : -INFINITY;
+          } else if (mode == kKeyPad) {
+            const int lim = it.len - 1 - k0;
+#pragma unroll
+            for (int e = 0; e < C::SUB; ++e) sv[e] = e <= lim ? sv[e] : -INFINITY;
+          }
+          const int nv = mode == kTriLo ? 32 : C::SUB;  // values that can be non-zero
+          float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            bm0 = fmax3(bm0, sv[e], sv[e + 1]);
+            bm1 = fmax3(bm1, sv[e + 2], sv[e + 3]);
+          }
+          if (nv == C::SUB) {
+#pragma unroll
+            for (int e = 32; e < C::SUB; e += 4) {
+              bm0 = fmax3(bm0, sv[e], sv[e + 1]);
+              bm1 = fmax3(bm1, sv[e + 2], sv[e + 3]);
             }
           }
-          const float bmax = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
-          const float m_new = fmaxf(m_run, bmax * sl2);
+          const float m_new = fmaxf(m_run, fmaxf(bm0, bm1) * sl2);
           const bool resc = m_new > m_run + 8.0f;
-          if (j > 0 && __any_sync(0xffffffffu, resc)) {
-            // O holds PV of every earlier block (s_full(j) was committed after PV(j-1)).
-            const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
+          if (__any_sync(0xffffffffu, resc)) {
+            if (u > 0) {
+              // O must hold P V of every earlier sub-block of this item before it is rescaled
+              const uint32_t gp = g - 1;
+              if (!wait_bounded(&pv_done[gp & 1u], (gp >> 1) & 1u, wc)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
 #pragma unroll 1
-            for (int c = 0; c < HD / 32; ++c) {
-              float o[32];
-              tmem_ld32(t_o + c * 32, o);
-              tmem_wait_ld();
+              for (int c = 0; c < HD / 32; ++c) {
+                float o[32];
+                tmem_ld32(t_o + c * 32, o);
+                tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= alpha;
-              tmem_st32(t_o + c * 32, o);
+                for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                tmem_st32(t_o + c * 32, o);
+              }
+              tmem_wait_st();
+              l_run *= alpha;
             }
-            tmem_wait_st();
-            l_run *= alpha;
+            if (resc) m_run = m_new;
           }
-          if (resc) m_run = m_new;
+          // p = 2^(s * scale * log2(e) - m): pairs of scores scaled in one
+          // packed FMA, partial sums kept as four packed pairs
           const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-          // pass 2: exponentials
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
-          float bm2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          exp_block(need_mask, k0, kmax, mref, ls, bm2);
-          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mref, -mref);
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          auto exp_pairs = [&](int e2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sv[2 * e2], sv[2 * e2 + 1]), sl2x2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            acc[e2 & 3] = f2_add(acc[e2 & 3], f2_pack(p0, p1));
+            const __half2 hp = __floats2half2_rn(p0, p1);  // first key in the low half
+            pk[e2] = *reinterpret_cast<const uint32_t*>(&hp);
+          };
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) exp_pairs(e2);
+          if (nv == C::SUB) {
+#pragma unroll
+            for (int e2 = 16; e2 < C::SUB / 2; ++e2) exp_pairs(e2);
+          } else {
+#pragma unroll
+            for (int e2 = 16; e2 < C::SUB / 2; ++e2) pk[e2] = 0u;
+          }
+          float a0, a1;
+          f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+          l_run += a0 + a1;
         }
+        if (g >= 2) {
+          // P[b] is free once the P V of sub-block g - 2 has completed
+          if (!wait_bounded(&pv_done[b], ((g - 2) >> 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32_u(t_row + C::P_COL + b * (C::SUB / 2), pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[b]);
       }
       if (!ok) break;
       if (!wait_bounded(o_full, oph, wc)) break;

@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a waiting thread is parked by the
+// hardware until the phase completes or about `hint_ns` have passed, instead
+// of re-polling and taking issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_parked(uint32_t addr, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Control block for bounded waits: the kernel's status word in global memory,
 // the CTA's abort flag in shared memory, and the bound.
 struct WaitCtl {
@@ -66,6 +81,9 @@ struct WaitCtl {
                              // share a named barrier: they must all leave the same way)
 };
 
+// Longest a waiter stays parked before it re-checks the abort flag and the bound.
+constexpr uint32_t kParkNs = 20000;
+
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false (after flagging) if the bound ran out or another waiter of the CTA
 // already gave up.
@@ -73,15 +91,13 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (c.early_exit && *c.abort_flag) return false;
-      if ((int64_t)(globaltimer_ns() - t0) > c.timeout_ns) {
-        *c.abort_flag = 1;
-        atomicOr(c.status, TFL_DEV_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_parked(a, parity, kParkNs)) return true;
+    if (c.early_exit && *c.abort_flag) return false;
+    if ((int64_t)(globaltimer_ns() - t0) > c.timeout_ns) {
+      *c.abort_flag = 1;
+      atomicOr(c.status, TFL_DEV_TIMEOUT);
+      return false;
     }
   }
 }
@@ -235,6 +251,34 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---------------------------------------------------------------- packed fp32 pairs
+// sm_100-class FMA units execute two fp32 operations per lane in one
+// instruction (fma/add/mul .f32x2); a pair lives in one 64-bit register.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// three-input maximum (one instruction on sm_100-class GPUs)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // ---------------------------------------------------------------- rows

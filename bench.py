@@ -35,7 +35,9 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
-MUFU_PER_CLK_PER_SM = 16  # ex2 throughput of one SM per clock
+# ex2.approx.f32 results per clock per SM, measured on GB300 with
+# attention_qkv_gemm_gb300/ex2_rate.cu (32.0 at 8 and 32 warps per SM)
+MUFU_PER_CLK_PER_SM = 32
 
 
 def dist_env():
@@ -140,29 +142,31 @@ def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of the benchmark workload (summaries in profiles/), valid only while the
-# kernel's source file is unchanged (sha256 prefix); otherwise traffic is reported null.
+# capture of the benchmark workload (summaries in profiles/).  A figure is valid
+# only while every kernel source it was taken with is unchanged: the fingerprint is
+# the sha256 prefix over all files of the package's csrc/ directory; otherwise
+# traffic is reported null.
 NCU_TRAFFIC = {
-    ("postchain", "B64_S1024_D128_causal_ragged"):
-        ("attention_qkv_gemm_gb300/csrc/postchain.cu", "7b1481155367", 40.311296e6 + 10.486016e6),
-    ("attention", "B64_S1024_D128_causal_ragged"):
-        ("attention_qkv_gemm_gb300/csrc/attention.cu", "d63c1b8b8d1a", 41.476608e6 + 0.4736e6),
-    ("gemm_qkv", "B64_S1024_D128_causal_ragged"):
-        ("attention_qkv_gemm_gb300/csrc/gemm.cu", "fd2104ecbbcd", 27.823872e6 + 0.707328e6),
+    # (kernel, workload): (csrc fingerprint, bytes per launch)
 }
 
 
-def ncu_traffic(kernel: str, workload: str):
+def csrc_fingerprint() -> str:
     import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "attention_qkv_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, workload: str):
     e = NCU_TRAFFIC.get((kernel, workload))
     if e is None:
         return None
-    path, sha, nbytes = e
-    try:
-        cur = hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:12]
-    except OSError:
-        return None
-    return nbytes if cur == sha else None
+    sha, nbytes = e
+    return nbytes if csrc_fingerprint() == sha else None
 
 
 def run_oracle_sample(shape, prm, seed, n_seq):
@@ -312,7 +316,8 @@ def main():
         peak = MUFU_PER_CLK_PER_SM * 152 * peaks["sm_max_mhz"] * 1e6 / 1e9
         roof = {"kernel": "attention", "bound": "alu", "achieved": achieved, "peak": peak, "unit": "Gexp2/s",
                 "frac": achieved / peak, "traffic": ncu_traffic("attention", shape.name),
-                "note": "MUFU ex2 rate: 16/clk/SM x 152 SMs x max SM clock; per launch = causal pairs x heads",
+                "note": "MUFU ex2 rate: 32/clk/SM (measured) x 152 SMs x max SM clock; per launch = allowed "
+                        "(query, key) pairs x heads",
                 "tensor_tflops": alg["attn_flops_per_launch"] / (dom_ms_launch / 1e3) / 1e12}
     else:
         by = kernel_bytes(dom, shape, alg["valid_tokens"])
