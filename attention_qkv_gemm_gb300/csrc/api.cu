@@ -111,6 +111,9 @@ struct WsLayout {
   size_t h32, n16, n16lo, qkv16, o16, g16, g16lo, status, sched, total;
 };
 
+// Ints before the tile list in the scheduling area.
+inline size_t tile_list_offset(int n_layers) { return align_up((size_t)n_layers, 32); }
+
 // precision 2 adds the lo planes of the GEMM activations (normed rows, GELU output).
 WsLayout ws_layout(const tfl_shape& s, int precision) {
   const size_t M = (size_t)s.B * s.S, D = s.d_model, F = s.d_ff;
@@ -129,7 +132,8 @@ WsLayout ws_layout(const tfl_shape& s, int precision) {
   w.g16 = take(M * F * 2);
   w.g16lo = precision == 2 ? take(M * F * 2) : 0;
   w.status = take(256);
-  w.sched = take((size_t)s.n_layers * sizeof(int));  // attention work counters, one per layer
+  // attention work counters (one per layer), then the tile list
+  w.sched = take((size_t)(tile_list_offset(s.n_layers) + 2 + (M + kGemmBM - 1) / kGemmBM) * sizeof(int));
   w.total = off;
   return w;
 }
@@ -258,6 +262,8 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
   c.lengths = lengths;
   c.status = h->status;
   c.timeout_ns = h->opt.wait_timeout_ns;
+  int* tiles = h->sched + tile_list_offset(h->L);
+  c.tiles = tiles;
   const float eps = h->opt.ln_eps;
   const int D = h->D, F = h->F, L = h->L;
   auto maps = [](const CUtensorMap& a, const CUtensorMap& alo, const PackedW& w) {
@@ -270,7 +276,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
   };
 
   TFL_CUDA(cudaMemsetAsync(h->sched, 0, (size_t)L * sizeof(int), st), "work counter reset");
-  TFL_CUDA(launch_check_lengths(lengths, h->shape.B, h->shape.S, h->status, st), "length check launch");
+  TFL_CUDA(launch_prepare(lengths, h->shape.B, h->shape.S, h->M, h->status, tiles, st), "preparation launch");
 
   TFL_CUDA(rec_mark(rec, st, 0), "event");
   {

@@ -135,7 +135,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int M = args.c.M, S = args.c.S;
   const int* lengths = args.c.lengths;
   const int num_m = (M + kGemmBM - 1) / kGemmBM, num_n = args.N / BN, num_k = args.K / kGemmBK;
-  const int total = num_m * num_n;
+  // work item t: live tile t / num_n of the tile list, column block t % num_n
+  const int* tile_list = args.c.tiles;
+  const int n_live = tile_list[0];
+  const int total = n_live * num_n;
+  (void)num_m;
 
   uint32_t issued_mask = 0, issued_par = 0;  // producer: stages with loads in flight (abort path)
   bool mma_issued = false;
@@ -146,8 +150,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const int mb = t / num_n, nb = t - mb * num_n;
-        if (!rows_live(mb * kGemmBM, min(mb * kGemmBM + kGemmBM, M), S, lengths)) continue;
+        const int ti = t / num_n, nb = t - ti * num_n;
+        const int mb = tile_list[2 + ti];
         for (int kb = 0; kb < num_k; ++kb) {
           if (!wait_bounded(&empty[stage], phase ^ 1u, wc)) {
             ok = false;
@@ -176,8 +180,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const int mb = t / num_n;
-        if (!rows_live(mb * kGemmBM, min(mb * kGemmBM + kGemmBM, M), S, lengths)) continue;
         if (!wait_bounded(&acce[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
@@ -226,13 +228,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ewc.early_exit = false;  // the epilogue warps meet at a named barrier: leave only on their own bound
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int mb = t / num_n, nb = t - mb * num_n;
+    // the final row epilogue also zeroes the all-padding tiles, listed after the live ones
+    bool zero_dead = false;
+    if constexpr (EPI == EPI_BIAS_RES_ROW) zero_dead = (args.row.flags & ROW_FINAL) != 0;
+    const int all_work = (zero_dead ? tile_list[1] : n_live) * num_n;
+    for (int t = blockIdx.x; t < all_work; t += gridDim.x) {
+      const int ti = t / num_n, nb = t - ti * num_n;
+      const int mb = tile_list[2 + ti];
       const int m0w = mb * kGemmBM + q * 32;  // first row of this warp's 32 rows
       const int m = m0w + lane;
       const uint32_t in_rows = __ballot_sync(0xffffffffu, m < M);
       const uint32_t valid_rows = __ballot_sync(0xffffffffu, m < M && row_valid(m, S, lengths));
-      if (!rows_live(mb * kGemmBM, min(mb * kGemmBM + kGemmBM, M), S, lengths)) {
+      if (ti >= n_live) {
         if constexpr (EPI == EPI_BIAS_RES_ROW) {
           if (args.row.flags & ROW_FINAL) {
             float z[32];

@@ -44,6 +44,10 @@ struct Common {
   const int* lengths = nullptr;    // device [B] or null
   int* status = nullptr;           // device status word
   int64_t timeout_ns = 2000000000LL;
+  // 128-row tiles in processing order, written once per forward by the
+  // preparation kernel: [0] tiles holding a valid row, [1] all tiles, then the
+  // live tiles ascending followed by the dead ones ascending
+  const int* tiles = nullptr;
 };
 
 // GEMM: C[M, N] = A[M, K] (fp16, K-major) * W[N, K]^T (fp16, K-major), fp32 accumulate.
@@ -125,7 +129,8 @@ cudaError_t launch_attention(int hd, const CUtensorMap& tq, const CUtensorMap& t
 cudaError_t launch_rows(const RowArgs& a, cudaStream_t s);
 cudaError_t launch_postchain(const ChainMaps& mp, const ChainArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_gelu_selftest(int n, unsigned* out, cudaStream_t s);
-cudaError_t launch_check_lengths(const int* lengths, int B, int S, int* status, cudaStream_t s);
+// Checks the lengths (TFL_DEV_BAD_LENGTHS) and writes the tile list of Common::tiles.
+cudaError_t launch_prepare(const int* lengths, int B, int S, int M, int* status, int* tiles, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s);
 cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s);
 cudaError_t launch_split_f16(const float* src, __half* hi, __half* lo, size_t n, float scale, cudaStream_t s);

@@ -232,7 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int M = args.c.M, S = args.c.S;
   const int* lengths = args.c.lengths;
-  const int num_m = (M + kGemmBM - 1) / kGemmBM;
+  // tiles from the list: the live ones, then (last layer only) the all-padding
+  // ones, whose output rows the epilogue zeroes
+  const int* tile_list = args.c.tiles;
+  const int n_live = tile_list[0];
+  const int n_work = args.last ? tile_list[1] : n_live;
   const int nch = args.F / kFC;
 
   uint32_t issued_mask = 0, issued_par = 0;  // producer: ring stages in flight (abort path)
@@ -275,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(d + 16384, &tmW2Lo, b, f0, 0);
         });
       };
-      for (int t = blockIdx.x; t < num_m && ok; t += gridDim.x) {
-        if (!rows_live(t * kGemmBM, min(t * kGemmBM + kGemmBM, M), S, lengths)) continue;
+      for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x) {
+        const int t = tile_list[2 + ti];
         rot = t % nch;
         if (!wait_bounded(o_free, oph ^ 1u, wc)) break;
         mbar_arrive_expect_tx(o_full, kOBytes);
@@ -357,8 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&gp_free[c & 1]);
         return true;
       };
-      for (int t = blockIdx.x; t < num_m && ok; t += gridDim.x) {
-        if (!rows_live(t * kGemmBM, min(t * kGemmBM + kGemmBM, M), S, lengths)) continue;
+      for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x) {
         // o_proj into A1 (free once the previous tile's epilogue read OUT)
         if (!first) {
           if (!wait_bounded(out_read, orph, wc)) break;
@@ -434,21 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t afph = 0, ofph = 0, gfph[2] = {0, 0}, gffph[2] = {0, 0};
     int slot = 0;
     const float eps = args.eps;
-    for (int t = blockIdx.x; t < num_m; t += gridDim.x) {
+    for (int ti = blockIdx.x; ti < n_work; ti += gridDim.x) {
+      const int t = tile_list[2 + ti];
       const int m0w = t * kGemmBM + q * 32;
       const int m = m0w + lane;
       const uint32_t in_rows = __ballot_sync(0xffffffffu, m < M);
       const uint32_t valid_rows = __ballot_sync(0xffffffffu, m < M && row_valid(m, S, lengths));
       const bool valid = (valid_rows >> lane) & 1u;
-      if (!rows_live(t * kGemmBM, min(t * kGemmBM + kGemmBM, M), S, lengths)) {
-        if (args.last) {
-          float z[32];
+      if (ti >= n_live) {
+        float z[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0.f;
+        for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            xp_store_f32x32(st, lane, z, args.out32 + (size_t)m0w * kD + c0 + c * 32, kD, in_rows);
-        }
+        for (int c = 0; c < 2; ++c)
+          xp_store_f32x32(st, lane, z, args.out32 + (size_t)m0w * kD + c0 + c * 32, kD, in_rows);
         continue;
       }
       // ---- phase 1: t = o_proj + bias + residual
@@ -459,7 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tq + kColA1 + c0, tv);
       tmem_ld32(tq + kColA1 + c0 + 32, tv + 32);
       tmem_wait_ld();
-#pragma unroll
       scale_bias64(tv, args.scale_o, prm + kPBo + c0);
 #pragma unroll
       for (int c = 0; c < 2; ++c)

@@ -118,20 +118,63 @@ cudaError_t launch_rows(const RowArgs& a, cudaStream_t s) {
 }
 
 // Flags TFL_DEV_BAD_LENGTHS if any length is outside [0, S] (kernels clamp).
-__global__ void check_lengths_kernel(const int* lengths, int B, int S, int* status) {
-  if (lengths == nullptr) return;
+// One CTA: flags out-of-range lengths, then lists the 128-row tiles, the ones
+// holding a valid row first (ascending), the all-padding ones after.  The
+// persistent GEMM / chain kernels deal the live tiles round-robin, so every
+// CTA gets within one tile of the same share however the padding falls.
+__global__ void __launch_bounds__(1024) prepare_kernel(const int* lengths, int B, int S, int M, int* status,
+                                                       int* tiles) {
+  __shared__ int warp_tot[32];
   bool bad = false;
-  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
-    const int l = lengths[b];
-    bad |= (l < 0) || (l > S);
+  if (lengths != nullptr)
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      const int l = lengths[b];
+      bad |= (l < 0) || (l > S);
+    }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, TFL_DEV_BAD_LENGTHS);
+
+  const int num_m = (M + kGemmBM - 1) / kGemmBM;
+  const int per = (num_m + blockDim.x - 1) / blockDim.x;
+  const int t0 = min((int)threadIdx.x * per, num_m), t1 = min(t0 + per, num_m);
+  int cnt = 0;
+  for (int t = t0; t < t1; ++t) cnt += rows_live(t * kGemmBM, min(t * kGemmBM + kGemmBM, M), S, lengths) ? 1 : 0;
+  // exclusive scan of cnt over the block
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, TFL_DEV_BAD_LENGTHS);
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tot[lane] = w;  // inclusive prefix over warps
+  }
+  __syncthreads();
+  const int n_live = warp_tot[31];
+  const int excl = x - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
+  int li = excl, di = n_live + (t0 - excl);
+  for (int t = t0; t < t1; ++t) {
+    if (rows_live(t * kGemmBM, min(t * kGemmBM + kGemmBM, M), S, lengths))
+      tiles[2 + li++] = t;
+    else
+      tiles[2 + di++] = t;
+  }
+  if (threadIdx.x == 0) {
+    tiles[0] = n_live;
+    tiles[1] = num_m;
+  }
 }
 
-cudaError_t launch_check_lengths(const int* lengths, int B, int S, int* status, cudaStream_t s) {
-  int grid = (B + 255) / 256;
-  if (grid > 64) grid = 64;
-  check_lengths_kernel<<<grid, 256, 0, s>>>(lengths, B, S, status);
+cudaError_t launch_prepare(const int* lengths, int B, int S, int M, int* status, int* tiles, cudaStream_t s) {
+  prepare_kernel<<<1, 1024, 0, s>>>(lengths, B, S, M, status, tiles);
   return cudaGetLastError();
 }
 
