@@ -340,6 +340,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ca.scale_o = ly.wo.acc_scale;
       ca.scale_1 = ly.w1.acc_scale;
       ca.scale_2 = ly.w2.acc_scale;
+      ca.inv_scale_2 = 1.0f / ly.w2.acc_scale;  // exact: acc_scale is a power of two
       ca.bo = ly.bo;
       ca.b1 = ly.b1;
       ca.b2 = ly.b2;

@@ -101,6 +101,7 @@ struct ChainArgs {
   int post_ln = 0;  // 1: h = LN1(h + attn), h = LN2(h + FFN)
   int last = 0;     // 1: write the model tail (final LN + pad-mask) to out32
   float scale_o = 1.f, scale_1 = 1.f, scale_2 = 1.f;  // weight pre-scales undone
+  float inv_scale_2 = 1.f;                            // 1 / scale_2 (a power of two)
   const float *bo = nullptr, *b1 = nullptr, *b2 = nullptr;
   const float *ln1_g = nullptr, *ln1_b = nullptr, *ln2_g = nullptr, *ln2_b = nullptr;
   const float *lnn_g = nullptr, *lnn_b = nullptr;  // next layer's LN1 (pre-LN, not last)

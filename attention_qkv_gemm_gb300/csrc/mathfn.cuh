@@ -33,6 +33,30 @@ __device__ __forceinline__ float gelu_as7126(float x) {
   return x * (x >= 0.f ? 1.0f - half_erfc : half_erfc);
 }
 
+// The same approximation for a packed pair of fp32 values (one 64-bit
+// register), with the sign case folded: x Phi(x) = max(x, 0) - |x| erfc(|x|/sqrt2)/2.
+// FMA-pipe work runs two lanes per instruction; the two MUFU operations stay
+// per value.
+__device__ __forceinline__ uint64_t gelu2_as7126(uint64_t x) {
+  constexpr float p_s = 0.3275911f * 0.7071067811865476f;
+  constexpr float h1 = 0.5f * 0.254829592f, h2 = 0.5f * -0.284496736f, h3 = 0.5f * 1.421413741f,
+                  h4 = 0.5f * -1.453152027f, h5 = 0.5f * 1.061405429f;
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  const uint64_t nax = f2_pack(-fabsf(x0), -fabsf(x1));
+  float d0, d1;
+  f2_unpack(f2_fma(nax, f2_splat(-p_s), f2_splat(1.0f)), d0, d1);
+  const uint64_t t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  uint64_t poly = f2_fma(f2_splat(h5), t, f2_splat(h4));
+  poly = f2_fma(poly, t, f2_splat(h3));
+  poly = f2_fma(poly, t, f2_splat(h2));
+  poly = f2_fma(poly, t, f2_splat(h1));
+  float e0, e1;
+  f2_unpack(f2_mul(f2_mul(x, x), f2_splat(-0.7213475204444817f)), e0, e1);
+  const uint64_t half_erfc = f2_mul(f2_mul(t, poly), f2_pack(ex2(e0), ex2(e1)));
+  return f2_fma(nax, half_erfc, f2_pack(fmaxf(x0, 0.f), fmaxf(x1, 0.f)));
+}
+
 // Reference GELU on CUDA's erff (used only by the self-test).
 __device__ __forceinline__ float gelu_erff(float x) { return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f)); }
 

@@ -39,6 +39,8 @@
 //   [0,128) A1 / OUT   [128,192) N2 hi  [192,256) N2 lo
 //   [256,320) G0  [320,384) G1   [384,416) GP0 hi [416,448) GP0 lo
 //   [448,480) GP1 hi [480,512) GP1 lo
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "mathfn.cuh"
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id64 = idesc_f16(128, kFC, 0, 0);
       const uint32_t tA1 = tmem_base + kColA1;
       int rs = 0;
-      uint32_t rph = 0, oph = 0, orph = 0, arph = 0, gpr[2] = {0, 0}, grd[2] = {0, 0};
+      uint32_t rph = 0, oph = 0, orph = 0, arph = 0, gpr = 0, grd = 0;  // parity bit per buffer
       bool ok = true, first = true;
       auto take = [&]() -> uint32_t {  // wait for the next ring unit; returns its smem address
         if (!wait_bounded(&r_full[rs], rph, wc)) return 0;
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bh = sdesc(u + kk * 32, 16, 1024, kSw128);
           const uint64_t bl = sdesc(u + 16384 + kk * 32, 16, 1024, kSw128);
           const uint32_t ah = gp + kk * 8, al = gp + 32 + kk * 8;
-          umma_f16_ts(tA1, ah, bh, id128, (c > 0 || kk > 0) ? 1u : 0u);
+          umma_f16_ts(tA1, ah, bh, id128, 1u);  // onto t (written by the epilogue)
           umma_f16_ts(tA1, al, bh, id128, 1u);
           umma_f16_ts(tA1, ah, bl, id128, 1u);
         }
@@ -398,22 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nch > 1 && !ffn1(1)) break;
         for (int c = 0; c < nch && ok; ++c) {
           // FFN-in of chunk c+2 reuses G[c&1] as soon as the epilogue has read it
-          if (!wait_bounded(&g_read[c & 1], grd[c & 1], wc)) {
+          if (!wait_bounded(&g_read[c & 1], (grd >> (c & 1)) & 1u, wc)) {
             ok = false;
             break;
           }
-          grd[c & 1] ^= 1u;
+          grd ^= 1u << (c & 1);
           tc_fence_after();
           if (c + 2 < nch && !ffn1(c + 2)) {
             ok = false;
             break;
           }
           // FFN-out of chunk c once its GELU output is in TMEM
-          if (!wait_bounded(&gp_ready[c & 1], gpr[c & 1], wc)) {
+          if (!wait_bounded(&gp_ready[c & 1], (gpr >> (c & 1)) & 1u, wc)) {
             ok = false;
             break;
           }
-          gpr[c & 1] ^= 1u;
+          gpr ^= 1u << (c & 1);
           tc_fence_after();
           if (!ffn2(c)) {
             ok = false;
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* st = xpose + (warp - 2) * 4096;
     WaitCtl ewc = wc;
     ewc.early_exit = false;  // the epilogue warps meet at a named barrier: leave only on their own bound
-    uint32_t afph = 0, ofph = 0, gfph[2] = {0, 0}, gffph[2] = {0, 0};
+    uint32_t afph = 0, ofph = 0, gfph = 0, gffph = 0;  // parity bit per buffer
     int slot = 0;
     const float eps = args.eps;
     for (int ti = blockIdx.x; ti < n_work; ti += gridDim.x) {
@@ -453,21 +455,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           xp_store_f32x32(st, lane, z, args.out32 + (size_t)m0w * kD + c0 + c * 32, kD, in_rows);
         continue;
       }
-      // ---- phase 1: t = o_proj + bias + residual
+      // ---- phase 1: t = o_proj + bias + residual (post-LN: LN1 of it).  t goes
+      // back into the accumulator columns, scaled by 2^s2, and FFN-out then
+      // accumulates onto it, so t is not held in registers through the FFN.
       if (!wait_bounded(acc_full, afph, ewc)) break;
       afph ^= 1u;
       tc_fence_after();
-      float tv[64];
-      tmem_ld32(tq + kColA1 + c0, tv);
-      tmem_ld32(tq + kColA1 + c0 + 32, tv + 32);
-      tmem_wait_ld();
-      scale_bias64(tv, args.scale_o, prm + kPBo + c0);
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-        xp_add_f32x32(st, lane, tv + c * 32, args.res + (size_t)m0w * kD + c0 + c * 32, kD, valid_rows);
-      if (args.post_ln) layer_norm64(tv, eps, prm + kPLn1g, prm + kPLn1b, c0, red, slot, half, r);
-      // ---- normed input of the FFN, as fp16 hi/lo pairs in TMEM (16 columns at a time)
       {
+        float tv[64];
+        tmem_ld32(tq + kColA1 + c0, tv);
+        tmem_ld32(tq + kColA1 + c0 + 32, tv + 32);
+        tmem_wait_ld();
+        scale_bias64(tv, args.scale_o, prm + kPBo + c0);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          xp_add_f32x32(st, lane, tv + c * 32, args.res + (size_t)m0w * kD + c0 + c * 32, kD, valid_rows);
+        if (args.post_ln) layer_norm64(tv, eps, prm + kPLn1g, prm + kPLn1b, c0, red, slot, half, r);
+        // normed input of the FFN, as fp16 hi/lo pairs in TMEM (16 columns at a time)
         float mean = 0.f, rstd = 1.f;
         const float* g = prm + kPLn2g + c0;
         const float* bb = prm + kPLn2b + c0;
@@ -488,16 +492,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st8_u(tq + kColN2 + half * 32 + 8 * j, hi);
           tmem_st8_u(tq + kColN2 + 64 + half * 32 + 8 * j, lo);
         }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) tv[i] *= args.inv_scale_2;  // exact: a power of two
+        tmem_st32(tq + kColA1 + c0, tv);
+        tmem_st32(tq + kColA1 + c0 + 32, tv + 32);
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_read);
       // ---- phase 2: GELU of each FFN-in chunk, back into TMEM as hi/lo pairs
+      const uint64_t sc1 = f2_splat(args.scale_1);
       for (int c = 0; c < args.F / kFC; ++c) {
         const int b = c & 1;
-        if (!wait_bounded(&g_full[b], gfph[b], ewc)) break;
-        gfph[b] ^= 1u;
+        if (!wait_bounded(&g_full[b], (gfph >> b) & 1u, ewc)) break;
+        gfph ^= 1u << b;
         tc_fence_after();
         float gv[32];
         tmem_ld32(tq + kColG + b * 64 + half * 32, gv);
@@ -505,24 +514,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&g_read[b]);
-        const float4* b1 = reinterpret_cast<const float4*>(prm + kPB1 + ((c + t) % nch) * kFC + half * 32);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 q = b1[i];
-          gv[4 * i + 0] = gelu_as7126(fmaf(gv[4 * i + 0], args.scale_1, q.x));
-          gv[4 * i + 1] = gelu_as7126(fmaf(gv[4 * i + 1], args.scale_1, q.y));
-          gv[4 * i + 2] = gelu_as7126(fmaf(gv[4 * i + 2], args.scale_1, q.z));
-          gv[4 * i + 3] = gelu_as7126(fmaf(gv[4 * i + 3], args.scale_1, q.w));
-        }
-        uint32_t hi[16], lo[16];
-        pack_pairs<32>(gv, hi, lo);
+        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + ((c + t) % nch) * kFC + half * 32);
         if (c >= 2) {  // GP[b] is free once FFN-out of chunk c-2 has read it
-          if (!wait_bounded(&gp_free[b], gffph[b], ewc)) break;
-          gffph[b] ^= 1u;
+          if (!wait_bounded(&gp_free[b], (gffph >> b) & 1u, ewc)) break;
+          gffph ^= 1u << b;
           tc_fence_after();
         }
-        tmem_st16_u(tq + kColGP + b * 64 + half * 16, hi);
-        tmem_st16_u(tq + kColGP + b * 64 + 32 + half * 16, lo);
+        // 16 values (8 pairs) at a time: GELU, fp16 hi/lo split, into GP[b]
+        auto gelu_half = [&](auto hh_c) {
+          constexpr int HH = decltype(hh_c)::value;
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = 8 * HH + i;
+            const float2 bq = b1[e];
+            const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), sc1, f2_pack(bq.x, bq.y)));
+            float g0, g1;
+            f2_unpack(gl, g0, g1);
+            const __half2 h = __floats2half2_rn(g0, g1);  // first value in the low half
+            const float2 hf = __half22float2(h);
+            float l0, l1;
+            f2_unpack(f2_sub(gl, f2_pack(hf.x, hf.y)), l0, l1);
+            const __half2 l = __floats2half2_rn(l0, l1);
+            hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[i] = *reinterpret_cast<const uint32_t*>(&l);
+          }
+          tmem_st8_u(tq + kColGP + b * 64 + half * 16 + 8 * HH, hi);
+          tmem_st8_u(tq + kColGP + b * 64 + 32 + half * 16 + 8 * HH, lo);
+        };
+        gelu_half(std::integral_constant<int, 0>{});
+        gelu_half(std::integral_constant<int, 1>{});
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -531,31 +552,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // consume the gp_free completions of the last two chunks (keeps the phases aligned)
       for (int c = max(args.F / kFC - 2, 0); c < args.F / kFC; ++c) {
         const int b = c & 1;
-        if (!wait_bounded(&gp_free[b], gffph[b], ewc)) break;
-        gffph[b] ^= 1u;
+        if (!wait_bounded(&gp_free[b], (gffph >> b) & 1u, ewc)) break;
+        gffph ^= 1u << b;
       }
-      // ---- phase 3: t2 = t + FFN-out + bias, then the next LayerNorm or the tail
+      // ---- phase 3: t2 = (t 2^s2 + FFN-out) 2^-s2 + bias, then the next LayerNorm or the tail
       if (!wait_bounded(out_full, ofph, ewc)) break;
       ofph ^= 1u;
       tc_fence_after();
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float ov[32];
-        tmem_ld32(tq + kColA1 + c0 + 32 * h2, ov);
-        tmem_wait_ld();
-        const float4* p4 = reinterpret_cast<const float4*>(prm + kPB2 + c0 + 32 * h2);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 q = p4[i];
-          tv[32 * h2 + 4 * i + 0] += fmaf(ov[4 * i + 0], args.scale_2, q.x);
-          tv[32 * h2 + 4 * i + 1] += fmaf(ov[4 * i + 1], args.scale_2, q.y);
-          tv[32 * h2 + 4 * i + 2] += fmaf(ov[4 * i + 2], args.scale_2, q.z);
-          tv[32 * h2 + 4 * i + 3] += fmaf(ov[4 * i + 3], args.scale_2, q.w);
-        }
-      }
+      float tv[64];
+      tmem_ld32(tq + kColA1 + c0, tv);
+      tmem_ld32(tq + kColA1 + c0 + 32, tv + 32);
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(out_read);
+      scale_bias64(tv, args.scale_2, prm + kPB2 + c0);
       if (args.post_ln) layer_norm64(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, half, r);
       if (!args.last) {
 #pragma unroll

@@ -251,7 +251,12 @@ __global__ void gelu_selftest_kernel(int n, unsigned* out) {
   float m = 0.f;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const float x = -12.0f + 24.0f * (float)i / (float)(n - 1);
+    const float y = -12.0f + 24.0f * (float)(n - 1 - i) / (float)(n - 1);
+    float g0, g1;
+    f2_unpack(gelu2_as7126(f2_pack(x, y)), g0, g1);
+    // the scalar form (GEMM epilogue) and the packed form (fused chain)
     m = fmaxf(m, fabsf(gelu_as7126(x) - gelu_erff(x)));
+    m = fmaxf(m, fmaxf(fabsf(g0 - gelu_erff(x)), fabsf(g1 - gelu_erff(y))));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));

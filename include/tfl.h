@@ -178,8 +178,9 @@ int tfl_profile_forward(tfl_handle* h, const float* x, const int32_t* lengths,
 
 /*
  * Self-test of the epilogues' GELU (exact-erf form evaluated with erf from
- * Abramowitz & Stegun 7.1.26): writes the largest |difference| from a GELU
- * built on CUDA's erff over n >= 2 points evenly spaced on [-12, 12].
+ * Abramowitz & Stegun 7.1.26), both the scalar form and the packed fp32-pair
+ * form: writes the largest |difference| from a GELU built on CUDA's erff over
+ * n >= 2 points evenly spaced on [-12, 12].
  * Synchronizes `stream`.  Errors: INVALID_ARG, CUDA.
  */
 int tfl_selftest_gelu(int32_t n, float* max_abs_diff, tfl_stream stream);
