@@ -91,7 +91,6 @@ struct PackedW {
   __half* lo = nullptr;
   float acc_scale = 1.f;
   CUtensorMap tm_hi{}, tm_lo{};
-  CUtensorMap tm_hi64{}, tm_lo64{};  // 64-row boxes (the fused chain's FFN-in chunks)
 };
 
 struct LayerDev {
@@ -363,8 +362,8 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       cm.o = h->tm_o16;
       cm.wo = ly.wo.tm_hi;
       cm.wo_lo = ly.wo.tm_lo;
-      cm.w1 = ly.w1.tm_hi64;
-      cm.w1_lo = ly.w1.tm_lo64;
+      cm.w1 = ly.w1.tm_hi;  // 128-row boxes at d_model 128
+      cm.w1_lo = ly.w1.tm_lo;
       cm.w2 = ly.w2.tm_hi;
       cm.w2_lo = ly.w2.tm_lo;
       TFL_CUDA(launch_postchain(cm, ca, h->num_sms, st), "post-attention chain");
@@ -656,8 +655,6 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
       const int aw = o.precision == 2;
       bool ok = maps(d.wqkv, 3 * D, D, gemm_bn(3 * D, aw)) && maps(d.wo, D, D, D == 128 ? 128 : gemm_bn(D, 0)) &&
                 maps(d.w1, F, D, gemm_bn(F, aw)) && maps(d.w2, D, F, D == 128 ? 128 : gemm_bn(D, aw));
-      if (ok && use_chain(D, F, o.precision))
-        ok = make_map_2d(&d.w1.tm_hi64, d.w1.hi, F, D, 64) && make_map_2d(&d.w1.tm_lo64, d.w1.lo, F, D, 64);
       if (!ok) rc = fail(TFL_ERR_CUDA, "weight tensor map encoding failed");
     }
   }

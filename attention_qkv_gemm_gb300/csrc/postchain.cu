@@ -13,32 +13,36 @@
 //   A1  = O Wo^T                    O: TMA tile in SMEM;  Wo hi/lo: ring
 //   t   = A1 * 2^-s + bo + res      (registers, fp32; post-LN: LN1(t))
 //   N2  = LN2(t) as fp16 hi/lo pairs, written to TMEM        (pre-LN)
-//   per 64-wide chunk c of d_ff:
+//   per 128-wide chunk c of d_ff:
 //     G_c   = N2 W1_c^T             A from TMEM (hi, lo), W1_c hi/lo: ring
 //     GP_c  = GELU(G_c * 2^-s + b1_c) as fp16 hi/lo pairs, to TMEM
-//     OUT  += GP_c W2_c^T           A from TMEM (hi, lo), W2_c hi/lo: ring
-//   t2  = t + OUT * 2^-s + b2 -> residual / next LayerNorm / tail  (HBM)
+//     OUT  += GP_c W2_c^T           A from TMEM (hi, lo), W2_c hi/lo: ring;
+//                                   OUT starts as t * 2^s (written by the epilogue)
+//   t2  = OUT * 2^-s + b2 -> residual / next LayerNorm / tail  (HBM)
 //
 // The GELU output never leaves the SM: per token it saves the d_ff-wide
 // round trip (2 * 2 * d_ff bytes written and read with split planes) and the
 // normed-row round trip of the unfused path.
 //
 // Weight streaming: every tile re-reads the layer's weights from L2 through
-// the ring.  Tile t walks the d_ff chunks starting at chunk t mod (d_ff/64),
-// so CTAs running at the same time read different weight chunks instead of
-// all hitting the same L2 lines (the FFN-out sum order differs per tile but is
-// fixed for a given shape).
+// a two-slot ring of 128 x 128 blocks (hi and lo planes, 64 KB).  Tile t walks
+// the d_ff chunks starting at chunk t mod (d_ff/128), so CTAs running at the
+// same time read different weight blocks instead of all hitting the same L2
+// lines (the FFN-out sum order differs per tile but is fixed for a shape).
 //
-// Pipelining: the epilogue releases G[c&1] as soon as it has read it, so
-// FFN-in of chunk c+2 runs on the tensor core while chunk c's GELU is being
-// computed; FFN-out of chunk c waits for that GELU.
+// Pipelining: the d_ff chunks are 128 wide, so every MMA is M = N = 128 (a
+// 64-wide N runs the tensor core at about half rate).  G and GP are single
+// buffers: the epilogue releases G as soon as it has read it, so FFN-in of
+// chunk c+1 runs on the tensor core while chunk c's GELU is being computed,
+// and FFN-out of chunk c runs while the epilogue reads G of chunk c+1.
+// FFN-out accumulates onto t, which the epilogue writes into the
+// accumulator columns (scaled by 2^s2) after the o_proj epilogue.
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-9
 // epilogue (two warps per TMEM lane quarter; each owns 64 of the 128 columns
 // of its 32 rows).  Tensor memory (512 columns):
-//   [0,128) A1 / OUT   [128,192) N2 hi  [192,256) N2 lo
-//   [256,320) G0  [320,384) G1   [384,416) GP0 hi [416,448) GP0 lo
-//   [448,480) GP1 hi [480,512) GP1 lo
+//   [0,128) A1 / t / OUT   [128,192) N2 hi  [192,256) N2 lo
+//   [256,384) G (fp32)     [384,448) GP hi  [448,512) GP lo
 #include <type_traits>
 
 #include "kernels.h"
@@ -51,9 +55,10 @@ namespace tfl {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kFC = 64;             // d_ff chunk
-constexpr int kUnit = 32 * 1024;    // one ring unit: a weight block, hi + lo planes
-constexpr int kRing = 4;
+constexpr int kFC = 128;            // d_ff chunk
+constexpr int kUnit = 64 * 1024;    // one ring unit: a 128 x 128 weight block, hi + lo planes
+constexpr int kHalf = 16 * 1024;    // one 64-column (K) half of a plane: 128 rows x 128 B
+constexpr int kRing = 2;
 constexpr int kEpi = 8;
 constexpr int kThreads = 64 + 32 * kEpi;
 constexpr int kOBytes = kGemmBM * kD * 2;
@@ -67,7 +72,7 @@ constexpr int kPBo = 0, kPB2 = 128, kPLn1g = 256, kPLn1b = 384, kPLn2g = 512, kP
 constexpr int kParamBytes = (kPB1 + kMaxF) * 4;
 constexpr size_t kSmem = 1024 + kOBytes + (size_t)kRing * kUnit + kXpBytes + kRedBytes + kParamBytes + 512;
 
-constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;
+constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;  // GP: hi [384,448), lo [448,512)
 
 __device__ __forceinline__ void chain_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpi) : "memory"); }
 
@@ -174,11 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* out_full = bars + 4;
   uint64_t* out_read = bars + 5;
   uint64_t* drain = bars + 6;
-  uint64_t* g_full = bars + 7;     // [2]
-  uint64_t* gp_ready = bars + 9;   // [2]
-  uint64_t* gp_free = bars + 11;   // [2]
-  uint64_t* g_read = bars + 13;    // [2]
-  uint64_t* r_full = bars + 15;    // [kRing]
+  uint64_t* g_full = bars + 7;
+  uint64_t* gp_ready = bars + 8;
+  uint64_t* gp_free = bars + 9;
+  uint64_t* g_read = bars + 10;
+  uint64_t* r_full = bars + 11;    // [kRing]
   uint64_t* r_empty = r_full + kRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(r_empty + kRing);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -193,12 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(out_full, 1);
     mbar_init(out_read, kEpi);
     mbar_init(drain, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&g_full[i], 1);
-      mbar_init(&gp_ready[i], kEpi);
-      mbar_init(&gp_free[i], 1);
-      mbar_init(&g_read[i], kEpi);
-    }
+    mbar_init(g_full, 1);
+    mbar_init(gp_ready, kEpi);
+    mbar_init(gp_free, 1);
+    mbar_init(g_read, kEpi);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&r_full[i], 1);
       mbar_init(&r_empty[i], 1);
@@ -265,20 +268,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       int rot = 0;  // this tile's chunk rotation (see the header)
+      // a 128 x 128 block of a weight: hi plane (two 64-column halves), then lo
       auto w1 = [&](int c) {
         const int f0 = ((c + rot) % nch) * kFC;
         return unit([&](uint8_t* d, uint64_t* b) {
           tma_load_2d(d, &tmW1, b, 0, f0);
-          tma_load_2d(d + 8192, &tmW1, b, 64, f0);
-          tma_load_2d(d + 16384, &tmW1Lo, b, 0, f0);
-          tma_load_2d(d + 24576, &tmW1Lo, b, 64, f0);
+          tma_load_2d(d + kHalf, &tmW1, b, 64, f0);
+          tma_load_2d(d + 2 * kHalf, &tmW1Lo, b, 0, f0);
+          tma_load_2d(d + 3 * kHalf, &tmW1Lo, b, 64, f0);
         });
       };
       auto w2 = [&](int c) {
         const int f0 = ((c + rot) % nch) * kFC;
         return unit([&](uint8_t* d, uint64_t* b) {
           tma_load_2d(d, &tmW2, b, f0, 0);
-          tma_load_2d(d + 16384, &tmW2Lo, b, f0, 0);
+          tma_load_2d(d + kHalf, &tmW2, b, f0 + 64, 0);
+          tma_load_2d(d + 2 * kHalf, &tmW2Lo, b, f0, 0);
+          tma_load_2d(d + 3 * kHalf, &tmW2Lo, b, f0 + 64, 0);
         });
       };
       for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x) {
@@ -291,16 +297,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         o_issued = true;
         o_par = oph;
         oph ^= 1u;
-        for (int u = 0; u < 2 && ok; ++u)
-          ok = unit([&](uint8_t* d, uint64_t* b) {
-            tma_load_2d(d, &tmWo, b, u * 64, 0);
-            tma_load_2d(d + 16384, &tmWoLo, b, u * 64, 0);
-          });
+        // the order the MMA warp consumes them: Wo, FFN-in 0 and 1, then FFN-out c / FFN-in c+2
+        ok = unit([&](uint8_t* d, uint64_t* b) {
+          tma_load_2d(d, &tmWo, b, 0, 0);
+          tma_load_2d(d + kHalf, &tmWo, b, 64, 0);
+          tma_load_2d(d + 2 * kHalf, &tmWoLo, b, 0, 0);
+          tma_load_2d(d + 3 * kHalf, &tmWoLo, b, 64, 0);
+        });
         if (ok) ok = w1(0);
         if (ok && nch > 1) ok = w1(1);
         for (int c = 0; c < nch && ok; ++c) {
-          if (c + 2 < nch) ok = w1(c + 2);
-          if (ok) ok = w2(c);
+          ok = w2(c);
+          if (ok && c + 2 < nch) ok = w1(c + 2);
         }
       }
     }
@@ -308,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id128 = idesc_f16(128, 128, 0, 0);
-      constexpr uint32_t id64 = idesc_f16(128, kFC, 0, 0);
       const uint32_t tA1 = tmem_base + kColA1;
       int rs = 0;
       uint32_t rph = 0, oph = 0, orph = 0, arph = 0, gpr = 0, grd = 0;  // parity bit per buffer
@@ -325,42 +332,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           rph ^= 1u;
         }
       };
-      // FFN-in chunk c: G[c&1] = N2 (hi, lo in TMEM) * W1_c^T (hi, lo)
+      // k-step kk of a 128 x 128 ring block (plane base p): 16 columns of one 64-column half
+      auto kdesc = [](uint32_t p, int kk) { return sdesc(p + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kSw128); };
+      // FFN-in chunk c: G = N2 (hi, lo in TMEM) * W1_c^T (hi, lo)
       auto ffn1 = [&](int c) -> bool {
         const uint32_t u = take();
         if (!u) return false;
-        const uint32_t d = tmem_base + kColG + (c & 1) * 64;
+        const uint32_t d = tmem_base + kColG;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t boff = (kk >> 2) * 8192 + (kk & 3) * 32;
-          const uint64_t bh = sdesc(u + boff, 16, 1024, kSw128);
-          const uint64_t bl = sdesc(u + 16384 + boff, 16, 1024, kSw128);
+          const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
           const uint32_t ah = tmem_base + kColN2 + kk * 8, al = ah + 64;
-          umma_f16_ts(d, ah, bh, id64, kk > 0 ? 1u : 0u);
-          umma_f16_ts(d, al, bh, id64, 1u);
-          umma_f16_ts(d, ah, bl, id64, 1u);
+          umma_f16_ts(d, ah, bh, id128, kk > 0 ? 1u : 0u);
+          umma_f16_ts(d, al, bh, id128, 1u);
+          umma_f16_ts(d, ah, bl, id128, 1u);
         }
         mma_issued = true;
         give();
-        umma_commit(&g_full[c & 1]);
+        umma_commit(g_full);
+        (void)c;
         return true;
       };
       // FFN-out chunk c: OUT += GP_c (hi, lo in TMEM) * W2_c^T (hi, lo)
       auto ffn2 = [&](int c) -> bool {
         const uint32_t u = take();
         if (!u) return false;
-        const uint32_t gp = tmem_base + kColGP + (c & 1) * 64;
+        const uint32_t gp = tmem_base + kColGP;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bh = sdesc(u + kk * 32, 16, 1024, kSw128);
-          const uint64_t bl = sdesc(u + 16384 + kk * 32, 16, 1024, kSw128);
-          const uint32_t ah = gp + kk * 8, al = gp + 32 + kk * 8;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
+          const uint32_t ah = gp + kk * 8, al = gp + 64 + kk * 8;
           umma_f16_ts(tA1, ah, bh, id128, 1u);  // onto t (written by the epilogue)
           umma_f16_ts(tA1, al, bh, id128, 1u);
           umma_f16_ts(tA1, ah, bl, id128, 1u);
         }
         give();
-        umma_commit(&gp_free[c & 1]);
+        umma_commit(gp_free);
+        (void)c;
         return true;
       };
       for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x) {
@@ -373,49 +381,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bounded(o_full, oph, wc)) break;
         oph ^= 1u;
         tc_fence_after();
-        const uint32_t so = smem_u32(sO);
-        for (int u8 = 0; u8 < 2 && ok; ++u8) {
+        {
           const uint32_t u = take();
-          if (!u) {
-            ok = false;
-            break;
-          }
+          if (!u) break;
+          const uint32_t so = smem_u32(sO);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = sdesc(so + u8 * (kOBytes / 2) + k * 32, 16, 1024, kSw128);
-            umma_f16(tA1, a, sdesc(u + k * 32, 16, 1024, kSw128), id128, (u8 | k) != 0);
-            umma_f16(tA1, a, sdesc(u + 16384 + k * 32, 16, 1024, kSw128), id128, 1u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a = sdesc(so + (kk >> 2) * (kOBytes / 2) + (kk & 3) * 32, 16, 1024, kSw128);
+            umma_f16(tA1, a, kdesc(u, kk), id128, kk > 0 ? 1u : 0u);
+            umma_f16(tA1, a, kdesc(u + 2 * kHalf, kk), id128, 1u);
           }
           mma_issued = true;
           give();
         }
-        if (!ok) break;
         umma_commit(o_free);
         umma_commit(acc_full);
-        // FFN chunks, FFN-in running two chunks ahead of FFN-out
+        // FFN chunks: FFN-in of chunk c+1 runs while the epilogue computes GELU of chunk c
         if (!wait_bounded(acc_read, arph, wc)) break;
         arph ^= 1u;
         tc_fence_after();
         if (!ffn1(0)) break;
-        if (nch > 1 && !ffn1(1)) break;
         for (int c = 0; c < nch && ok; ++c) {
-          // FFN-in of chunk c+2 reuses G[c&1] as soon as the epilogue has read it
-          if (!wait_bounded(&g_read[c & 1], (grd >> (c & 1)) & 1u, wc)) {
+          // FFN-in of chunk c+1 reuses G as soon as the epilogue has read chunk c
+          if (!wait_bounded(g_read, grd, wc)) {
             ok = false;
             break;
           }
-          grd ^= 1u << (c & 1);
+          grd ^= 1u;
           tc_fence_after();
-          if (c + 2 < nch && !ffn1(c + 2)) {
+          if (c + 1 < nch && !ffn1(c + 1)) {
             ok = false;
             break;
           }
           // FFN-out of chunk c once its GELU output is in TMEM
-          if (!wait_bounded(&gp_ready[c & 1], (gpr >> (c & 1)) & 1u, wc)) {
+          if (!wait_bounded(gp_ready, gpr, wc)) {
             ok = false;
             break;
           }
-          gpr ^= 1u << (c & 1);
+          gpr ^= 1u;
           tc_fence_after();
           if (!ffn2(c)) {
             ok = false;
@@ -503,30 +506,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(acc_read);
       // ---- phase 2: GELU of each FFN-in chunk, back into TMEM as hi/lo pairs
       const uint64_t sc1 = f2_splat(args.scale_1);
-      for (int c = 0; c < args.F / kFC; ++c) {
-        const int b = c & 1;
-        if (!wait_bounded(&g_full[b], (gfph >> b) & 1u, ewc)) break;
-        gfph ^= 1u << b;
+      bool ok = true;
+      for (int c = 0; c < nch && ok; ++c) {
+        if (!wait_bounded(g_full, gfph, ewc)) {
+          ok = false;
+          break;
+        }
+        gfph ^= 1u;
         tc_fence_after();
-        float gv[32];
-        tmem_ld32(tq + kColG + b * 64 + half * 32, gv);
+        float gv[64];  // this warp's 64 of the chunk's 128 columns
+        tmem_ld32(tq + kColG + half * 64, gv);
+        tmem_ld32(tq + kColG + half * 64 + 32, gv + 32);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&g_read[b]);
-        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + ((c + t) % nch) * kFC + half * 32);
-        if (c >= 2) {  // GP[b] is free once FFN-out of chunk c-2 has read it
-          if (!wait_bounded(&gp_free[b], (gffph >> b) & 1u, ewc)) break;
-          gffph ^= 1u << b;
+        if (lane == 0) mbar_arrive(g_read);
+        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + ((c + t) % nch) * kFC + half * 64);
+        if (c >= 1) {  // GP is free once FFN-out of chunk c-1 has read it
+          if (!wait_bounded(gp_free, gffph, ewc)) {
+            ok = false;
+            break;
+          }
+          gffph ^= 1u;
           tc_fence_after();
         }
-        // 16 values (8 pairs) at a time: GELU, fp16 hi/lo split, into GP[b]
-        auto gelu_half = [&](auto hh_c) {
-          constexpr int HH = decltype(hh_c)::value;
+        // 16 values (8 pairs) at a time: GELU, fp16 hi/lo split, into GP
+        auto gelu16 = [&](auto q_c) {
+          constexpr int Q = decltype(q_c)::value;
           uint32_t hi[8], lo[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int e = 8 * HH + i;
+            const int e = 8 * Q + i;
             const float2 bq = b1[e];
             const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), sc1, f2_pack(bq.x, bq.y)));
             float g0, g1;
@@ -539,22 +549,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             hi[i] = *reinterpret_cast<const uint32_t*>(&h);
             lo[i] = *reinterpret_cast<const uint32_t*>(&l);
           }
-          tmem_st8_u(tq + kColGP + b * 64 + half * 16 + 8 * HH, hi);
-          tmem_st8_u(tq + kColGP + b * 64 + 32 + half * 16 + 8 * HH, lo);
+          tmem_st8_u(tq + kColGP + half * 32 + 8 * Q, hi);
+          tmem_st8_u(tq + kColGP + 64 + half * 32 + 8 * Q, lo);
         };
-        gelu_half(std::integral_constant<int, 0>{});
-        gelu_half(std::integral_constant<int, 1>{});
+        gelu16(std::integral_constant<int, 0>{});
+        gelu16(std::integral_constant<int, 1>{});
+        gelu16(std::integral_constant<int, 2>{});
+        gelu16(std::integral_constant<int, 3>{});
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&gp_ready[b]);
+        if (lane == 0) mbar_arrive(gp_ready);
       }
-      // consume the gp_free completions of the last two chunks (keeps the phases aligned)
-      for (int c = max(args.F / kFC - 2, 0); c < args.F / kFC; ++c) {
-        const int b = c & 1;
-        if (!wait_bounded(&gp_free[b], (gffph >> b) & 1u, ewc)) break;
-        gffph ^= 1u << b;
-      }
+      // consume the gp_free completion of the last chunk (keeps the phases aligned)
+      if (!ok || !wait_bounded(gp_free, gffph, ewc)) break;
+      gffph ^= 1u;
       // ---- phase 3: t2 = (t 2^s2 + FFN-out) 2^-s2 + bias, then the next LayerNorm or the tail
       if (!wait_bounded(out_full, ofph, ewc)) break;
       ofph ^= 1u;
