@@ -77,24 +77,45 @@ constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;  // GP: 
 __device__ __forceinline__ void chain_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpi) : "memory"); }
 
 // Row mean / rstd of a 128-wide row split over two warps (64 values each).
+// Sums run as four packed pairs (eight partial sums) to keep the dependent
+// chains short.
 __device__ __forceinline__ void stats64(const float* t, float eps, float* red, int slot, int half, int r,
                                         float& mean, float& rstd) {
-  float s = 0.f;
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-  for (int i = 0; i < 64; ++i) s += t[i];
-  red[(slot * 2 + half) * kGemmBM + r] = s;
+  for (int i = 0; i < 32; ++i) acc[i & 3] = f2_add(acc[i & 3], f2_pack(t[2 * i], t[2 * i + 1]));
+  float s0, s1;
+  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+  red[(slot * 2 + half) * kGemmBM + r] = s0 + s1;
   chain_bar();
   mean = (red[(slot * 2) * kGemmBM + r] + red[(slot * 2 + 1) * kGemmBM + r]) * (1.0f / kD);
-  float q = 0.f;
+  const uint64_t m2 = f2_splat(mean);
 #pragma unroll
-  for (int i = 0; i < 64; ++i) {
-    const float d = t[i] - mean;
-    q = fmaf(d, d, q);
+  for (int i = 0; i < 4; ++i) acc[i] = 0ull;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint64_t d = f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2);
+    acc[i & 3] = f2_fma(d, d, acc[i & 3]);
   }
-  red[((slot + 1) * 2 + half) * kGemmBM + r] = q;
+  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+  red[((slot + 1) * 2 + half) * kGemmBM + r] = s0 + s1;
   chain_bar();
   rstd = rsqrtf((red[((slot + 1) * 2) * kGemmBM + r] + red[((slot + 1) * 2 + 1) * kGemmBM + r]) * (1.0f / kD) +
                 eps);
+}
+
+// (t - mean) * rstd * g + b for 64 values in place; g, b: this warp's 64 columns in shared memory.
+__device__ __forceinline__ void normalize64(float* t, float mean, float rstd, const float* g, const float* b) {
+  const uint64_t m2 = f2_splat(mean), r2 = f2_splat(rstd);
+  const float2* g2 = reinterpret_cast<const float2*>(g);
+  const float2* b2 = reinterpret_cast<const float2*>(b);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float2 gg = g2[i], bb = b2[i];
+    const uint64_t y = f2_fma(f2_mul(f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2), r2), f2_pack(gg.x, gg.y),
+                              f2_pack(bb.x, bb.y));
+    f2_unpack(y, t[2 * i], t[2 * i + 1]);
+  }
 }
 
 // LayerNorm of a row split over two warps; g, b: shared-memory gamma / beta.
@@ -103,16 +124,7 @@ __device__ __forceinline__ void layer_norm64(float* t, float eps, const float* g
   float mean, rstd;
   stats64(t, eps, red, slot, half, r, mean, rstd);
   slot = (slot + 2) & 3;
-  const float4* g4 = reinterpret_cast<const float4*>(g + c0);
-  const float4* b4 = reinterpret_cast<const float4*>(b + c0);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 gg = g4[i], bb = b4[i];
-    t[4 * i + 0] = (t[4 * i + 0] - mean) * rstd * gg.x + bb.x;
-    t[4 * i + 1] = (t[4 * i + 1] - mean) * rstd * gg.y + bb.y;
-    t[4 * i + 2] = (t[4 * i + 2] - mean) * rstd * gg.z + bb.z;
-    t[4 * i + 3] = (t[4 * i + 3] - mean) * rstd * gg.w + bb.w;
-  }
+  normalize64(t, mean, rstd, g + c0, b + c0);
 }
 
 // v[i] = v[i] * scale + p[i] for 64 values, p in shared memory.
@@ -125,20 +137,6 @@ __device__ __forceinline__ void scale_bias64(float* v, float scale, const float*
     v[4 * i + 1] = fmaf(v[4 * i + 1], scale, q.y);
     v[4 * i + 2] = fmaf(v[4 * i + 2], scale, q.z);
     v[4 * i + 3] = fmaf(v[4 * i + 3], scale, q.w);
-  }
-}
-
-// Pack n values as fp16 pairs (first value in the low half): hi words and the
-// rounding residuals' words.
-template <int N>
-__device__ __forceinline__ void pack_pairs(const float* v, uint32_t* hi, uint32_t* lo) {
-#pragma unroll
-  for (int i = 0; i < N / 2; ++i) {
-    const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-    const float2 f = __half22float2(h);
-    const __half2 l = __floats2half2_rn(v[2 * i] - f.x, v[2 * i + 1] - f.y);
-    hi[i] = *reinterpret_cast<const uint32_t*>(&h);
-    lo[i] = *reinterpret_cast<const uint32_t*>(&l);
   }
 }
 
@@ -476,22 +474,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (args.post_ln) layer_norm64(tv, eps, prm + kPLn1g, prm + kPLn1b, c0, red, slot, half, r);
         // normed input of the FFN, as fp16 hi/lo pairs in TMEM (16 columns at a time)
         float mean = 0.f, rstd = 1.f;
-        const float* g = prm + kPLn2g + c0;
-        const float* bb = prm + kPLn2b + c0;
         if (!args.post_ln) {
           stats64(tv, eps, red, slot, half, r, mean, rstd);
           slot = (slot + 2) & 3;
         }
+        const uint64_t m2 = f2_splat(mean), r2 = f2_splat(rstd);
+        const float2* g2 = reinterpret_cast<const float2*>(prm + kPLn2g + c0);
+        const float2* b2 = reinterpret_cast<const float2*>(prm + kPLn2b + c0);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float nv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float v = tv[16 * j + i];
-            nv[i] = args.post_ln ? v : (v - mean) * rstd * g[16 * j + i] + bb[16 * j + i];
-          }
           uint32_t hi[8], lo[8];
-          pack_pairs<16>(nv, hi, lo);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = 8 * j + i;
+            uint64_t v = f2_pack(tv[2 * e], tv[2 * e + 1]);
+            if (!args.post_ln) {
+              const float2 gg = g2[e], bb = b2[e];
+              v = f2_fma(f2_mul(f2_sub(v, m2), r2), f2_pack(gg.x, gg.y), f2_pack(bb.x, bb.y));
+            }
+            float v0, v1;
+            f2_unpack(v, v0, v1);
+            const __half2 h = __floats2half2_rn(v0, v1);  // first value in the low half
+            const float2 hf = __half22float2(h);
+            float l0, l1;
+            f2_unpack(f2_sub(v, f2_pack(hf.x, hf.y)), l0, l1);
+            const __half2 l = __floats2half2_rn(l0, l1);
+            hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[i] = *reinterpret_cast<const uint32_t*>(&l);
+          }
           tmem_st8_u(tq + kColN2 + half * 32 + 8 * j, hi);
           tmem_st8_u(tq + kColN2 + 64 + half * 32 + 8 * j, lo);
         }
@@ -504,6 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_read);
+      // pull the next tile's residual rows into L2 while this tile's FFN runs
+      if (ti + (int)gridDim.x < n_live) {
+        const int mn = tile_list[2 + ti + gridDim.x] * kGemmBM + q * 32 + lane;
+        if (mn < M) {
+          const float* pr = args.res + (size_t)mn * kD + c0;
+          prefetch_l2(pr);
+          prefetch_l2(pr + 32);
+        }
+      }
       // ---- phase 2: GELU of each FFN-in chunk, back into TMEM as hi/lo pairs
       const uint64_t sc1 = f2_splat(args.scale_1);
       bool ok = true;
