@@ -38,9 +38,9 @@
 // FFN-out accumulates onto t, which the epilogue writes into the
 // accumulator columns (scaled by 2^s2) after the o_proj epilogue.
 //
-// Roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-9
-// epilogue (two warps per TMEM lane quarter; each owns 64 of the 128 columns
-// of its 32 rows).  Tensor memory (512 columns):
+// Roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-17
+// epilogue (four warps per TMEM lane quarter; each owns 32 of the 128 columns
+// of its 32 rows, so four warps per scheduler hide each other's latencies).  Tensor memory (512 columns):
 //   [0,128) A1 / t / OUT   [128,192) N2 hi  [192,256) N2 lo
 //   [256,384) G (fp32)     [384,448) GP hi  [448,512) GP lo
 #include <type_traits>
@@ -59,11 +59,13 @@ constexpr int kFC = 128;            // d_ff chunk
 constexpr int kUnit = 64 * 1024;    // one ring unit: a 128 x 128 weight block, hi + lo planes
 constexpr int kHalf = 16 * 1024;    // one 64-column (K) half of a plane: 128 rows x 128 B
 constexpr int kRing = 2;
-constexpr int kEpi = 8;
+constexpr int kEpi = 16;           // epilogue warps: four per TMEM lane quarter
+constexpr int kParts = 4;           // each owns 32 of a row's 128 columns
 constexpr int kThreads = 64 + 32 * kEpi;
 constexpr int kOBytes = kGemmBM * kD * 2;
-constexpr int kXpBytes = kEpi * 4096;
-constexpr int kRedBytes = 4 * 2 * kGemmBM * 4;
+constexpr int kXpWarp = 2048;       // per-warp transpose stage: 32 rows x 64 B
+constexpr int kXpBytes = kEpi * kXpWarp;
+constexpr int kRedBytes = 4 * kParts * kGemmBM * 4;
 // parameter vectors staged in shared memory once per CTA (floats):
 // bo, b2, ln1 g/b, ln2 g/b, next-layer ln1 g/b, final ln g/b (128 each), then b1 (d_ff <= kMaxF)
 constexpr int kMaxF = 2048;
@@ -76,41 +78,43 @@ constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;  // GP: 
 
 __device__ __forceinline__ void chain_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpi) : "memory"); }
 
-// Row mean / rstd of a 128-wide row split over two warps (64 values each).
+// Row mean / rstd of a 128-wide row split over four warps (32 values each).
 // Sums run as four packed pairs (eight partial sums) to keep the dependent
-// chains short.
-__device__ __forceinline__ void stats64(const float* t, float eps, float* red, int slot, int half, int r,
+// chains short; slots alternate so a fast warp never overwrites partial sums
+// a slow one still reads.
+__device__ __forceinline__ void stats32(const float* t, float eps, float* red, int slot, int part, int r,
                                         float& mean, float& rstd) {
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i & 3] = f2_add(acc[i & 3], f2_pack(t[2 * i], t[2 * i + 1]));
+  for (int i = 0; i < 16; ++i) acc[i & 3] = f2_add(acc[i & 3], f2_pack(t[2 * i], t[2 * i + 1]));
   float s0, s1;
   f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
-  red[(slot * 2 + half) * kGemmBM + r] = s0 + s1;
+  float* rs = red + slot * kParts * kGemmBM + r;
+  rs[part * kGemmBM] = s0 + s1;
   chain_bar();
-  mean = (red[(slot * 2) * kGemmBM + r] + red[(slot * 2 + 1) * kGemmBM + r]) * (1.0f / kD);
+  mean = ((rs[0] + rs[kGemmBM]) + (rs[2 * kGemmBM] + rs[3 * kGemmBM])) * (1.0f / kD);
   const uint64_t m2 = f2_splat(mean);
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = 0ull;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 16; ++i) {
     const uint64_t d = f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2);
     acc[i & 3] = f2_fma(d, d, acc[i & 3]);
   }
   f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
-  red[((slot + 1) * 2 + half) * kGemmBM + r] = s0 + s1;
+  float* rq = rs + kParts * kGemmBM;
+  rq[part * kGemmBM] = s0 + s1;
   chain_bar();
-  rstd = rsqrtf((red[((slot + 1) * 2) * kGemmBM + r] + red[((slot + 1) * 2 + 1) * kGemmBM + r]) * (1.0f / kD) +
-                eps);
+  rstd = rsqrtf(((rq[0] + rq[kGemmBM]) + (rq[2 * kGemmBM] + rq[3 * kGemmBM])) * (1.0f / kD) + eps);
 }
 
-// (t - mean) * rstd * g + b for 64 values in place; g, b: this warp's 64 columns in shared memory.
-__device__ __forceinline__ void normalize64(float* t, float mean, float rstd, const float* g, const float* b) {
+// (t - mean) * rstd * g + b for 32 values in place; g, b: this warp's 32 columns in shared memory.
+__device__ __forceinline__ void normalize32(float* t, float mean, float rstd, const float* g, const float* b) {
   const uint64_t m2 = f2_splat(mean), r2 = f2_splat(rstd);
   const float2* g2 = reinterpret_cast<const float2*>(g);
   const float2* b2 = reinterpret_cast<const float2*>(b);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 16; ++i) {
     const float2 gg = g2[i], bb = b2[i];
     const uint64_t y = f2_fma(f2_mul(f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2), r2), f2_pack(gg.x, gg.y),
                               f2_pack(bb.x, bb.y));
@@ -118,25 +122,38 @@ __device__ __forceinline__ void normalize64(float* t, float mean, float rstd, co
   }
 }
 
-// LayerNorm of a row split over two warps; g, b: shared-memory gamma / beta.
-__device__ __forceinline__ void layer_norm64(float* t, float eps, const float* g, const float* b, int c0,
-                                             float* red, int& slot, int half, int r) {
+// LayerNorm of a row split over four warps; g, b: shared-memory gamma / beta of the whole row.
+__device__ __forceinline__ void layer_norm32(float* t, float eps, const float* g, const float* b, int c0,
+                                             float* red, int& slot, int part, int r) {
   float mean, rstd;
-  stats64(t, eps, red, slot, half, r, mean, rstd);
+  stats32(t, eps, red, slot, part, r, mean, rstd);
   slot = (slot + 2) & 3;
-  normalize64(t, mean, rstd, g + c0, b + c0);
+  normalize32(t, mean, rstd, g + c0, b + c0);
 }
 
-// v[i] = v[i] * scale + p[i] for 64 values, p in shared memory.
-__device__ __forceinline__ void scale_bias64(float* v, float scale, const float* p) {
-  const float4* p4 = reinterpret_cast<const float4*>(p);
+// v[i] = v[i] * scale + p[i] for 32 values, p in shared memory.
+__device__ __forceinline__ void scale_bias32(float* v, float scale, const float* p) {
+  const float2* p2 = reinterpret_cast<const float2*>(p);
+  const uint64_t s2 = f2_splat(scale);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float4 q = p4[i];
-    v[4 * i + 0] = fmaf(v[4 * i + 0], scale, q.x);
-    v[4 * i + 1] = fmaf(v[4 * i + 1], scale, q.y);
-    v[4 * i + 2] = fmaf(v[4 * i + 2], scale, q.z);
-    v[4 * i + 3] = fmaf(v[4 * i + 3], scale, q.w);
+    const float2 q = p2[i];
+    f2_unpack(f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), s2, f2_pack(q.x, q.y)), v[2 * i], v[2 * i + 1]);
+  }
+}
+
+// fp16 hi/lo pairs of 16 values (first value of a pair in the low half): v = hi + lo + O(2^-22 |v|).
+__device__ __forceinline__ void split_pairs16(const float* v, uint32_t* hi, uint32_t* lo) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t x = f2_pack(v[2 * i], v[2 * i + 1]);
+    const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+    const float2 hf = __half22float2(h);
+    float l0, l1;
+    f2_unpack(f2_sub(x, f2_pack(hf.x, hf.y)), l0, l1);
+    const __half2 l = __floats2half2_rn(l0, l1);
+    hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+    lo[i] = *reinterpret_cast<const uint32_t*>(&l);
   }
 }
 
@@ -428,18 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (8 warps)
-    const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int c0 = half * 64;  // this warp's 64 of the 128 columns
+    // ------------------------------------------------------------ epilogue (16 warps)
+    const int q = warp & 3;             // TMEM lane quarter this warp may access
+    const int part = (warp - 2) >> 2;   // which 32 of the 128 columns it owns
+    const int c0 = part * 32;
     const int r = q * 32 + lane;
     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
-    uint8_t* st = xpose + (warp - 2) * 4096;
+    uint8_t* st = xpose + (warp - 2) * kXpWarp;
     WaitCtl ewc = wc;
     ewc.early_exit = false;  // the epilogue warps meet at a named barrier: leave only on their own bound
-    uint32_t afph = 0, ofph = 0, gfph = 0, gffph = 0;  // parity bit per buffer
+    uint32_t afph = 0, ofph = 0, gfph = 0, gffph = 0;
+    bool gp_written = false;  // GP holds an earlier chunk that FFN-out must have consumed before a rewrite
     int slot = 0;
     const float eps = args.eps;
+    const uint64_t sc1 = f2_splat(args.scale_1);
     for (int ti = blockIdx.x; ti < n_work; ti += gridDim.x) {
       const int t = tile_list[2 + ti];
       const int m0w = t * kGemmBM + q * 32;
@@ -447,68 +466,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t in_rows = __ballot_sync(0xffffffffu, m < M);
       const uint32_t valid_rows = __ballot_sync(0xffffffffu, m < M && row_valid(m, S, lengths));
       const bool valid = (valid_rows >> lane) & 1u;
-      if (ti >= n_live) {
-        float z[32];
+      if (ti >= n_live) {  // all-padding tile (last layer only): zero output rows
+        float z[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = 0.f;
+        for (int i = 0; i < 16; ++i) z[i] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          xp_store_f32x32(st, lane, z, args.out32 + (size_t)m0w * kD + c0 + c * 32, kD, in_rows);
+        for (int h = 0; h < 2; ++h)
+          xp_store_f32x16(st, lane, z, args.out32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
         continue;
       }
       // ---- phase 1: t = o_proj + bias + residual (post-LN: LN1 of it).  t goes
       // back into the accumulator columns, scaled by 2^s2, and FFN-out then
       // accumulates onto it, so t is not held in registers through the FFN.
+      uint4 res0[4], res1[4];  // this warp's 32 residual columns, fetched before the accumulator wait
+      XStage<64>::fetch_rows(lane, reinterpret_cast<const uint8_t*>(args.res + (size_t)m0w * kD + c0), kD * 4,
+                             valid_rows, res0);
+      XStage<64>::fetch_rows(lane, reinterpret_cast<const uint8_t*>(args.res + (size_t)m0w * kD + c0 + 16), kD * 4,
+                             valid_rows, res1);
       if (!wait_bounded(acc_full, afph, ewc)) break;
       afph ^= 1u;
       tc_fence_after();
       {
-        float tv[64];
+        float tv[32];
         tmem_ld32(tq + kColA1 + c0, tv);
-        tmem_ld32(tq + kColA1 + c0 + 32, tv + 32);
         tmem_wait_ld();
-        scale_bias64(tv, args.scale_o, prm + kPBo + c0);
+        scale_bias32(tv, args.scale_o, prm + kPBo + c0);
+        xp_add_fetched_f32x16(st, lane, tv, res0);
+        xp_add_fetched_f32x16(st, lane, tv + 16, res1);
+        if (args.post_ln) layer_norm32(tv, eps, prm + kPLn1g, prm + kPLn1b, c0, red, slot, part, r);
+        // t * 2^s2 into the accumulator columns (exact: a power of two), then t back
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          xp_add_f32x32(st, lane, tv + c * 32, args.res + (size_t)m0w * kD + c0 + c * 32, kD, valid_rows);
-        if (args.post_ln) layer_norm64(tv, eps, prm + kPLn1g, prm + kPLn1b, c0, red, slot, half, r);
-        // normed input of the FFN, as fp16 hi/lo pairs in TMEM (16 columns at a time)
-        float mean = 0.f, rstd = 1.f;
-        if (!args.post_ln) {
-          stats64(tv, eps, red, slot, half, r, mean, rstd);
-          slot = (slot + 2) & 3;
-        }
-        const uint64_t m2 = f2_splat(mean), r2 = f2_splat(rstd);
-        const float2* g2 = reinterpret_cast<const float2*>(prm + kPLn2g + c0);
-        const float2* b2 = reinterpret_cast<const float2*>(prm + kPLn2b + c0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t hi[8], lo[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = 8 * j + i;
-            uint64_t v = f2_pack(tv[2 * e], tv[2 * e + 1]);
-            if (!args.post_ln) {
-              const float2 gg = g2[e], bb = b2[e];
-              v = f2_fma(f2_mul(f2_sub(v, m2), r2), f2_pack(gg.x, gg.y), f2_pack(bb.x, bb.y));
-            }
-            float v0, v1;
-            f2_unpack(v, v0, v1);
-            const __half2 h = __floats2half2_rn(v0, v1);  // first value in the low half
-            const float2 hf = __half22float2(h);
-            float l0, l1;
-            f2_unpack(f2_sub(v, f2_pack(hf.x, hf.y)), l0, l1);
-            const __half2 l = __floats2half2_rn(l0, l1);
-            hi[i] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[i] = *reinterpret_cast<const uint32_t*>(&l);
-          }
-          tmem_st8_u(tq + kColN2 + half * 32 + 8 * j, hi);
-          tmem_st8_u(tq + kColN2 + 64 + half * 32 + 8 * j, lo);
-        }
-#pragma unroll
-        for (int i = 0; i < 64; ++i) tv[i] *= args.inv_scale_2;  // exact: a power of two
+        for (int i = 0; i < 32; ++i) tv[i] *= args.inv_scale_2;
         tmem_st32(tq + kColA1 + c0, tv);
-        tmem_st32(tq + kColA1 + c0 + 32, tv + 32);
+        tmem_wait_st();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tv[i] *= args.scale_2;
+        // normed input of the FFN, as fp16 hi/lo pairs in TMEM
+        if (!args.post_ln) layer_norm32(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, part, r);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t hi[8], lo[8];
+          split_pairs16(tv + 16 * j, hi, lo);
+          tmem_st8_u(tq + kColN2 + part * 16 + 8 * j, hi);
+          tmem_st8_u(tq + kColN2 + 64 + part * 16 + 8 * j, lo);
+        }
         tmem_wait_st();
       }
       tc_fence_before();
@@ -517,14 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pull the next tile's residual rows into L2 while this tile's FFN runs
       if (ti + (int)gridDim.x < n_live) {
         const int mn = tile_list[2 + ti + gridDim.x] * kGemmBM + q * 32 + lane;
-        if (mn < M) {
-          const float* pr = args.res + (size_t)mn * kD + c0;
-          prefetch_l2(pr);
-          prefetch_l2(pr + 32);
-        }
+        if (mn < M) prefetch_l2(args.res + (size_t)mn * kD + c0);
       }
       // ---- phase 2: GELU of each FFN-in chunk, back into TMEM as hi/lo pairs
-      const uint64_t sc1 = f2_splat(args.scale_1);
       bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
         if (!wait_bounded(g_full, gfph, ewc)) {
@@ -533,15 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         gfph ^= 1u;
         tc_fence_after();
-        float gv[64];  // this warp's 64 of the chunk's 128 columns
-        tmem_ld32(tq + kColG + half * 64, gv);
-        tmem_ld32(tq + kColG + half * 64 + 32, gv + 32);
+        float gv[32];  // this warp's 32 of the chunk's 128 columns
+        tmem_ld32(tq + kColG + c0, gv);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(g_read);
-        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + ((c + t) % nch) * kFC + half * 64);
-        if (c >= 1) {  // GP is free once FFN-out of chunk c-1 has read it
+        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + ((c + t) % nch) * kFC + c0);
+        if (gp_written) {  // GP is free once FFN-out of the previous chunk has read it
           if (!wait_bounded(gp_free, gffph, ewc)) {
             ok = false;
             break;
@@ -550,12 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
         }
         // 16 values (8 pairs) at a time: GELU, fp16 hi/lo split, into GP
-        auto gelu16 = [&](auto q_c) {
-          constexpr int Q = decltype(q_c)::value;
+        auto gelu16 = [&](auto h_c) {
+          constexpr int HH = decltype(h_c)::value;
           uint32_t hi[8], lo[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int e = 8 * Q + i;
+            const int e = 8 * HH + i;
             const float2 bq = b1[e];
             const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), sc1, f2_pack(bq.x, bq.y)));
             float g0, g1;
@@ -568,48 +563,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             hi[i] = *reinterpret_cast<const uint32_t*>(&h);
             lo[i] = *reinterpret_cast<const uint32_t*>(&l);
           }
-          tmem_st8_u(tq + kColGP + half * 32 + 8 * Q, hi);
-          tmem_st8_u(tq + kColGP + 64 + half * 32 + 8 * Q, lo);
+          tmem_st8_u(tq + kColGP + part * 16 + 8 * HH, hi);
+          tmem_st8_u(tq + kColGP + 64 + part * 16 + 8 * HH, lo);
         };
         gelu16(std::integral_constant<int, 0>{});
         gelu16(std::integral_constant<int, 1>{});
-        gelu16(std::integral_constant<int, 2>{});
-        gelu16(std::integral_constant<int, 3>{});
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(gp_ready);
+        gp_written = true;
       }
-      // consume the gp_free completion of the last chunk (keeps the phases aligned)
-      if (!ok || !wait_bounded(gp_free, gffph, ewc)) break;
-      gffph ^= 1u;
+      if (!ok) break;
       // ---- phase 3: t2 = (t 2^s2 + FFN-out) 2^-s2 + bias, then the next LayerNorm or the tail
       if (!wait_bounded(out_full, ofph, ewc)) break;
       ofph ^= 1u;
       tc_fence_after();
-      float tv[64];
+      float tv[32];
       tmem_ld32(tq + kColA1 + c0, tv);
-      tmem_ld32(tq + kColA1 + c0 + 32, tv + 32);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(out_read);
-      scale_bias64(tv, args.scale_2, prm + kPB2 + c0);
-      if (args.post_ln) layer_norm64(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, half, r);
+      scale_bias32(tv, args.scale_2, prm + kPB2 + c0);
+      if (args.post_ln) layer_norm32(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, part, r);
       if (!args.last) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          xp_store_f32x32(st, lane, tv + c * 32, args.h32 + (size_t)m0w * kD + c0 + c * 32, kD, in_rows);
-        if (!args.post_ln) layer_norm64(tv, eps, prm + kPLnng, prm + kPLnnb, c0, red, slot, half, r);
+        for (int h = 0; h < 2; ++h)
+          xp_store_f32x16(st, lane, tv + 16 * h, args.h32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
+        if (!args.post_ln) layer_norm32(tv, eps, prm + kPLnng, prm + kPLnnb, c0, red, slot, part, r);
         const size_t off = (size_t)m0w * kD + c0;
-        xp_store_f16<64>(st, lane, tv, args.n16 + off, args.n16lo + off, kD, in_rows);
+        xp_store_f16<32>(st, lane, tv, args.n16 + off, args.n16lo + off, kD, in_rows);
       } else {
-        layer_norm64(tv, eps, prm + kPLnfg, prm + kPLnfb, c0, red, slot, half, r);
+        layer_norm32(tv, eps, prm + kPLnfg, prm + kPLnfb, c0, red, slot, part, r);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) tv[i] = valid ? tv[i] : 0.f;
+        for (int i = 0; i < 32; ++i) tv[i] = valid ? tv[i] : 0.f;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          xp_store_f32x32(st, lane, tv + c * 32, args.out32 + (size_t)m0w * kD + c0 + c * 32, kD, in_rows);
+        for (int h = 0; h < 2; ++h)
+          xp_store_f32x16(st, lane, tv + 16 * h, args.out32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
       }
     }
   }

@@ -147,4 +147,40 @@ __device__ __forceinline__ void xp_add_f32x32(uint8_t* st, int lane, float* v, c
   xp_add_fetched_f32x32(st, lane, v, f);
 }
 
+// 16 fp32 values -> 4 x 16 bytes.
+__device__ __forceinline__ void pack_f32x16(const float* v, uint4* o) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    o[q] = make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                      __float_as_uint(v[4 * q + 3]));
+}
+
+// Store 16 fp32 columns of the warp's 32 rows through a 2 KB stage.
+__device__ __forceinline__ void xp_store_f32x16(uint8_t* st, int lane, const float* v, float* row0,
+                                                size_t pitch_elems, uint32_t rows) {
+  uint4 o[4];
+  pack_f32x16(v, o);
+  XStage<64>::put_row(st, lane, o);
+  __syncwarp();
+  XStage<64>::store_rows(st, lane, reinterpret_cast<uint8_t*>(row0), pitch_elems * 4, rows);
+  __syncwarp();
+}
+
+// Add 16 fp32 columns of the warp's 32 rows, already fetched into `f` by
+// XStage<64>::fetch_rows, into v (thread = row) through a 2 KB stage.
+__device__ __forceinline__ void xp_add_fetched_f32x16(uint8_t* st, int lane, float* v, const uint4* f) {
+  using X = XStage<64>;
+  X::put_fetched(st, lane, f);
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 o = *reinterpret_cast<const uint4*>(st + X::off(lane, q));
+    v[4 * q] += __uint_as_float(o.x);
+    v[4 * q + 1] += __uint_as_float(o.y);
+    v[4 * q + 2] += __uint_as_float(o.z);
+    v[4 * q + 3] += __uint_as_float(o.w);
+  }
+  __syncwarp();
+}
+
 }  // namespace tfl
