@@ -38,7 +38,8 @@
 // FFN-out accumulates onto t, which the epilogue writes into the
 // accumulator columns (scaled by 2^s2) after the o_proj epilogue.
 //
-// Roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-17
+// Roles: warp 0 TMA producer, warp 1 o_proj / FFN-out MMA issuer + TMEM
+// owner, warp 18 FFN-in MMA issuer, warps 2-17
 // epilogue (four warps per TMEM lane quarter; each owns 32 of the 128 columns
 // of its 32 rows, so four warps per scheduler hide each other's latencies).  Tensor memory (512 columns):
 //   [0,128) A1 / t / OUT   [128,192) N2 hi  [192,256) N2 lo
@@ -61,7 +62,8 @@ constexpr int kHalf = 16 * 1024;    // one 64-column (K) half of a plane: 128 ro
 constexpr int kRing = 2;
 constexpr int kEpi = 16;           // epilogue warps: four per TMEM lane quarter
 constexpr int kParts = 4;           // each owns 32 of a row's 128 columns
-constexpr int kThreads = 64 + 32 * kEpi;
+constexpr int kFfn1Warp = 2 + kEpi;  // the FFN-in MMA issuer (scheduler 2; o_proj / FFN-out issue from warp 1)
+constexpr int kThreads = 32 * (kFfn1Warp + 1);
 constexpr int kOBytes = kGemmBM * kD * 2;
 constexpr int kXpWarp = 2048;       // per-warp transpose stage: 32 rows x 64 B
 constexpr int kXpBytes = kEpi * kXpWarp;
@@ -193,12 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_read = bars + 3;
   uint64_t* out_full = bars + 4;
   uint64_t* out_read = bars + 5;
-  uint64_t* drain = bars + 6;
-  uint64_t* g_full = bars + 7;
-  uint64_t* gp_ready = bars + 8;
-  uint64_t* gp_free = bars + 9;
-  uint64_t* g_read = bars + 10;
-  uint64_t* r_full = bars + 11;    // [kRing]
+  uint64_t* drain = bars + 6;      // [2]: one per MMA issuer (abort path)
+  uint64_t* g_full = bars + 8;
+  uint64_t* gp_ready = bars + 9;
+  uint64_t* gp_free = bars + 10;
+  uint64_t* g_read = bars + 11;
+  uint64_t* r_full = bars + 12;    // [kRing]
   uint64_t* r_empty = r_full + kRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(r_empty + kRing);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -212,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acc_read, kEpi);
     mbar_init(out_full, 1);
     mbar_init(out_read, kEpi);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(g_full, 1);
     mbar_init(gp_ready, kEpi);
     mbar_init(gp_free, 1);
@@ -327,124 +330,132 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kFfn1Warp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads on different schedulers issue the MMAs, so neither starves
+    // behind the epilogue warps sharing its scheduler: warp 1 o_proj and
+    // FFN-out (accumulator A1 / OUT), warp kFfn1Warp FFN-in (accumulator G).
+    // Both walk the producer's ring sequence by unit index: per tile Wo,
+    // W1_0, W1_1, then W2_c, W1_(c+2) for each chunk c.
     if (lane == 0) {
       constexpr uint32_t id128 = idesc_f16(128, 128, 0, 0);
       const uint32_t tA1 = tmem_base + kColA1;
-      int rs = 0;
-      uint32_t rph = 0, oph = 0, orph = 0, arph = 0, gpr = 0, grd = 0;  // parity bit per buffer
-      bool ok = true, first = true;
-      auto take = [&]() -> uint32_t {  // wait for the next ring unit; returns its smem address
-        if (!wait_bounded(&r_full[rs], rph, wc)) return 0;
+      const int units = 1 + 2 * nch;  // ring units per tile
+      auto idx_w1 = [&](int k) { return k == 0 ? 1 : (k == 1 ? 2 : 2 * k); };
+      auto idx_w2 = [&](int c) { return c <= nch - 2 ? 3 + 2 * c : 2 * nch; };
+      // wait for ring unit g (counted over all tiles of this CTA); returns its smem address
+      auto take = [&](uint32_t g) -> uint32_t {
+        if (!wait_bounded(&r_full[g % kRing], (g / kRing) & 1u, wc)) return 0;
         tc_fence_after();
-        return smem_u32(ring + (size_t)rs * kUnit);
+        return smem_u32(ring + (size_t)(g % kRing) * kUnit);
       };
-      auto give = [&]() {
-        umma_commit(&r_empty[rs]);
-        if (++rs == kRing) {
-          rs = 0;
-          rph ^= 1u;
-        }
-      };
+      auto give = [&](uint32_t g) { umma_commit(&r_empty[g % kRing]); };
       // k-step kk of a 128 x 128 ring block (plane base p): 16 columns of one 64-column half
       auto kdesc = [](uint32_t p, int kk) { return sdesc(p + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kSw128); };
-      // FFN-in chunk c: G = N2 (hi, lo in TMEM) * W1_c^T (hi, lo)
-      auto ffn1 = [&](int c) -> bool {
-        const uint32_t u = take();
-        if (!u) return false;
-        const uint32_t d = tmem_base + kColG;
+      bool ok = true;
+      uint32_t tile_seq = 0;
+      if (warp == 1) {
+        uint32_t oph = 0, orph = 0, gpr = 0;
+        for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x, ++tile_seq) {
+          const uint32_t g0 = tile_seq * units;
+          // o_proj into A1 (free once the previous tile's epilogue read OUT)
+          if (tile_seq > 0) {
+            if (!wait_bounded(out_read, orph, wc)) break;
+            orph ^= 1u;
+          }
+          if (!wait_bounded(o_full, oph, wc)) break;
+          oph ^= 1u;
+          tc_fence_after();
+          {
+            const uint32_t u = take(g0);
+            if (!u) break;
+            const uint32_t so = smem_u32(sO);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
-          const uint32_t ah = tmem_base + kColN2 + kk * 8, al = ah + 64;
-          umma_f16_ts(d, ah, bh, id128, kk > 0 ? 1u : 0u);
-          umma_f16_ts(d, al, bh, id128, 1u);
-          umma_f16_ts(d, ah, bl, id128, 1u);
-        }
-        mma_issued = true;
-        give();
-        umma_commit(g_full);
-        (void)c;
-        return true;
-      };
-      // FFN-out chunk c: OUT += GP_c (hi, lo in TMEM) * W2_c^T (hi, lo)
-      auto ffn2 = [&](int c) -> bool {
-        const uint32_t u = take();
-        if (!u) return false;
-        const uint32_t gp = tmem_base + kColGP;
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t a = sdesc(so + (kk >> 2) * (kOBytes / 2) + (kk & 3) * 32, 16, 1024, kSw128);
+              umma_f16(tA1, a, kdesc(u, kk), id128, kk > 0 ? 1u : 0u);
+              umma_f16(tA1, a, kdesc(u + 2 * kHalf, kk), id128, 1u);
+            }
+            mma_issued = true;
+            give(g0);
+          }
+          umma_commit(o_free);
+          umma_commit(acc_full);
+          // FFN-out of chunk c once its GELU output is in TMEM:
+          // OUT += GP_c (hi, lo in TMEM) * W2_c^T (hi, lo), onto t (written by the epilogue)
+          for (int c = 0; c < nch; ++c) {
+            if (!wait_bounded(gp_ready, gpr, wc)) {
+              ok = false;
+              break;
+            }
+            gpr ^= 1u;
+            tc_fence_after();
+            const uint32_t g = g0 + idx_w2(c);
+            const uint32_t u = take(g);
+            if (!u) {
+              ok = false;
+              break;
+            }
+            const uint32_t gp = tmem_base + kColGP;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
-          const uint32_t ah = gp + kk * 8, al = gp + 64 + kk * 8;
-          umma_f16_ts(tA1, ah, bh, id128, 1u);  // onto t (written by the epilogue)
-          umma_f16_ts(tA1, al, bh, id128, 1u);
-          umma_f16_ts(tA1, ah, bl, id128, 1u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
+              const uint32_t ah = gp + kk * 8, al = gp + 64 + kk * 8;
+              umma_f16_ts(tA1, ah, bh, id128, 1u);
+              umma_f16_ts(tA1, al, bh, id128, 1u);
+              umma_f16_ts(tA1, ah, bl, id128, 1u);
+            }
+            give(g);
+            umma_commit(gp_free);
+          }
+          if (!ok) break;
+          umma_commit(out_full);
         }
-        give();
-        umma_commit(gp_free);
-        (void)c;
-        return true;
-      };
-      for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x) {
-        // o_proj into A1 (free once the previous tile's epilogue read OUT)
-        if (!first) {
-          if (!wait_bounded(out_read, orph, wc)) break;
-          orph ^= 1u;
-        }
-        first = false;
-        if (!wait_bounded(o_full, oph, wc)) break;
-        oph ^= 1u;
-        tc_fence_after();
-        {
-          const uint32_t u = take();
-          if (!u) break;
-          const uint32_t so = smem_u32(sO);
+      } else {
+        uint32_t arph = 0, grd = 0;
+        // FFN-in chunk k: G = N2 (hi, lo in TMEM) * W1_k^T (hi, lo)
+        auto ffn1 = [&](uint32_t g0, int k) -> bool {
+          const uint32_t g = g0 + idx_w1(k);
+          const uint32_t u = take(g);
+          if (!u) return false;
+          const uint32_t d = tmem_base + kColG;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t a = sdesc(so + (kk >> 2) * (kOBytes / 2) + (kk & 3) * 32, 16, 1024, kSw128);
-            umma_f16(tA1, a, kdesc(u, kk), id128, kk > 0 ? 1u : 0u);
-            umma_f16(tA1, a, kdesc(u + 2 * kHalf, kk), id128, 1u);
+            const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
+            const uint32_t ah = tmem_base + kColN2 + kk * 8, al = ah + 64;
+            umma_f16_ts(d, ah, bh, id128, kk > 0 ? 1u : 0u);
+            umma_f16_ts(d, al, bh, id128, 1u);
+            umma_f16_ts(d, ah, bl, id128, 1u);
           }
           mma_issued = true;
-          give();
-        }
-        umma_commit(o_free);
-        umma_commit(acc_full);
-        // FFN chunks: FFN-in of chunk c+1 runs while the epilogue computes GELU of chunk c
-        if (!wait_bounded(acc_read, arph, wc)) break;
-        arph ^= 1u;
-        tc_fence_after();
-        if (!ffn1(0)) break;
-        for (int c = 0; c < nch && ok; ++c) {
-          // FFN-in of chunk c+1 reuses G as soon as the epilogue has read chunk c
-          if (!wait_bounded(g_read, grd, wc)) {
-            ok = false;
-            break;
-          }
-          grd ^= 1u;
+          give(g);
+          umma_commit(g_full);
+          return true;
+        };
+        for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x, ++tile_seq) {
+          const uint32_t g0 = tile_seq * units;
+          // N2 of this tile is in TMEM (the previous tile's last G read was awaited below)
+          if (!wait_bounded(acc_read, arph, wc)) break;
+          arph ^= 1u;
           tc_fence_after();
-          if (c + 1 < nch && !ffn1(c + 1)) {
-            ok = false;
-            break;
-          }
-          // FFN-out of chunk c once its GELU output is in TMEM
-          if (!wait_bounded(gp_ready, gpr, wc)) {
-            ok = false;
-            break;
-          }
-          gpr ^= 1u;
-          tc_fence_after();
-          if (!ffn2(c)) {
-            ok = false;
-            break;
+          if (!ffn1(g0, 0)) break;
+          for (int c = 0; c < nch; ++c) {
+            // FFN-in of chunk c+1 reuses G as soon as the epilogue has read chunk c
+            if (!wait_bounded(g_read, grd, wc)) {
+              ok = false;
+              break;
+            }
+            grd ^= 1u;
+            tc_fence_after();
+            if (c + 1 < nch && !ffn1(g0, c + 1)) {
+              ok = false;
+              break;
+            }
           }
         }
-        if (!ok) break;
-        umma_commit(out_full);
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kEpi) {
     // ------------------------------------------------------------ epilogue (16 warps)
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int part = (warp - 2) >> 2;   // which 32 of the 128 columns it owns
@@ -459,13 +470,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int slot = 0;
     const float eps = args.eps;
     const uint64_t sc1 = f2_splat(args.scale_1);
+    int t_next = (int)blockIdx.x < n_work ? tile_list[2 + blockIdx.x] : 0;  // loaded one tile ahead
     for (int ti = blockIdx.x; ti < n_work; ti += gridDim.x) {
-      const int t = tile_list[2 + ti];
+      const int t = t_next;
+      if (ti + (int)gridDim.x < n_work) t_next = tile_list[2 + ti + gridDim.x];
       const int m0w = t * kGemmBM + q * 32;
       const int m = m0w + lane;
       const uint32_t in_rows = __ballot_sync(0xffffffffu, m < M);
-      const uint32_t valid_rows = __ballot_sync(0xffffffffu, m < M && row_valid(m, S, lengths));
-      const bool valid = (valid_rows >> lane) & 1u;
       if (ti >= n_live) {  // all-padding tile (last layer only): zero output rows
         float z[16];
 #pragma unroll
@@ -478,11 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- phase 1: t = o_proj + bias + residual (post-LN: LN1 of it).  t goes
       // back into the accumulator columns, scaled by 2^s2, and FFN-out then
       // accumulates onto it, so t is not held in registers through the FFN.
-      uint4 res0[4], res1[4];  // this warp's 32 residual columns, fetched before the accumulator wait
+      // this warp's 32 residual columns, fetched before the accumulator wait; padding
+      // rows are fetched too (finite values whose results no valid token reads)
+      uint4 res0[4], res1[4];
       XStage<64>::fetch_rows(lane, reinterpret_cast<const uint8_t*>(args.res + (size_t)m0w * kD + c0), kD * 4,
-                             valid_rows, res0);
+                             in_rows, res0);
       XStage<64>::fetch_rows(lane, reinterpret_cast<const uint8_t*>(args.res + (size_t)m0w * kD + c0 + 16), kD * 4,
-                             valid_rows, res1);
+                             in_rows, res1);
       if (!wait_bounded(acc_full, afph, ewc)) break;
       afph ^= 1u;
       tc_fence_after();
@@ -517,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(acc_read);
       // pull the next tile's residual rows into L2 while this tile's FFN runs
       if (ti + (int)gridDim.x < n_live) {
-        const int mn = tile_list[2 + ti + gridDim.x] * kGemmBM + q * 32 + lane;
+        const int mn = t_next * kGemmBM + q * 32 + lane;
         if (mn < M) prefetch_l2(args.res + (size_t)mn * kD + c0);
       }
       // ---- phase 2: GELU of each FFN-in chunk, back into TMEM as hi/lo pairs
@@ -536,6 +549,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(g_read);
         const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + ((c + t) % nch) * kFC + c0);
+        // GELU and fp16 hi/lo split of the 32 values in registers, then into GP once
+        // FFN-out of the previous chunk has read it (the GELU overlaps that MMA)
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 bq = b1[e];
+          const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), sc1, f2_pack(bq.x, bq.y)));
+          float g0, g1;
+          f2_unpack(gl, g0, g1);
+          const __half2 h = __floats2half2_rn(g0, g1);  // first value in the low half
+          const float2 hf = __half22float2(h);
+          float l0, l1;
+          f2_unpack(f2_sub(gl, f2_pack(hf.x, hf.y)), l0, l1);
+          const __half2 l = __floats2half2_rn(l0, l1);
+          hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+          lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+        }
         if (gp_written) {  // GP is free once FFN-out of the previous chunk has read it
           if (!wait_bounded(gp_free, gffph, ewc)) {
             ok = false;
@@ -544,30 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           gffph ^= 1u;
           tc_fence_after();
         }
-        // 16 values (8 pairs) at a time: GELU, fp16 hi/lo split, into GP
-        auto gelu16 = [&](auto h_c) {
-          constexpr int HH = decltype(h_c)::value;
-          uint32_t hi[8], lo[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = 8 * HH + i;
-            const float2 bq = b1[e];
-            const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), sc1, f2_pack(bq.x, bq.y)));
-            float g0, g1;
-            f2_unpack(gl, g0, g1);
-            const __half2 h = __floats2half2_rn(g0, g1);  // first value in the low half
-            const float2 hf = __half22float2(h);
-            float l0, l1;
-            f2_unpack(f2_sub(gl, f2_pack(hf.x, hf.y)), l0, l1);
-            const __half2 l = __floats2half2_rn(l0, l1);
-            hi[i] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[i] = *reinterpret_cast<const uint32_t*>(&l);
-          }
-          tmem_st8_u(tq + kColGP + part * 16 + 8 * HH, hi);
-          tmem_st8_u(tq + kColGP + 64 + part * 16 + 8 * HH, lo);
-        };
-        gelu16(std::integral_constant<int, 0>{});
-        gelu16(std::integral_constant<int, 1>{});
+        tmem_st16_u(tq + kColGP + part * 16, hi);
+        tmem_st16_u(tq + kColGP + 64 + part * 16, lo);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -596,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         xp_store_f16<32>(st, lane, tv, args.n16 + off, args.n16lo + off, kD, in_rows);
       } else {
         layer_norm32(tv, eps, prm + kPLnfg, prm + kPLnfb, c0, red, slot, part, r);
+        const bool valid = m < M && row_valid(m, S, lengths);
 #pragma unroll
         for (int i = 0; i < 32; ++i) tv[i] = valid ? tv[i] : 0.f;
 #pragma unroll
@@ -616,9 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kRing; ++s)
         if (issued_mask & (1u << s)) wait_bounded(&r_full[s], (issued_par >> s) & 1u, dc);
     }
-    if (warp == 1 && lane == 0 && mma_issued) {
-      umma_commit(drain);
-      wait_bounded(drain, 0, dc);
+    if ((warp == 1 || warp == kFfn1Warp) && lane == 0 && mma_issued) {
+      uint64_t* db = &drain[warp == 1 ? 0 : 1];
+      umma_commit(db);
+      wait_bounded(db, 0, dc);
     }
     __syncthreads();
   }
