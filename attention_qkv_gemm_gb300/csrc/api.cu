@@ -169,6 +169,11 @@ struct tfl_handle {
 };
 
 namespace {
+// The fused chain (d_model 128) also computes the next layer's QKV projection in its tail.
+bool chain_fuses_qkv(const tfl_handle* h) { return use_chain(h->D, h->F, h->opt.precision); }
+}  // namespace
+
+namespace {
 
 int check_shape(const tfl_shape* s) {
   if (!s) return fail(TFL_ERR_INVALID_ARG, "shape is NULL");
@@ -300,8 +305,9 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
   for (int l = 0; l < L; ++l) {
     const LayerDev& ly = h->layers[l];
     const bool last = l == L - 1;
-    // QKV projection: [q | k | v] = normed [Wq; Wk; Wv]^T + b
-    {
+    // QKV projection: [q | k | v] = normed [Wq; Wk; Wv]^T + b (from layer 1 on, the fused
+    // chain of the previous layer computes it in its tail)
+    if (!(l > 0 && chain_fuses_qkv(h))) {
       GemmArgs g;
       g.c = c;
       g.N = 3 * D;
@@ -359,6 +365,18 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ca.n16lo = h->n16lo;
       ca.out32 = out;
       ChainMaps cm;
+      if (!last && chain_fuses_qkv(h)) {
+        const LayerDev& nx = h->layers[l + 1];
+        ca.fuse_qkv = 1;
+        ca.scale_qkv = nx.wqkv.acc_scale;
+        ca.bqkv = nx.bqkv;
+        ca.qkv16 = h->qkv16;
+        cm.wqkv = nx.wqkv.tm_hi;  // 128-row boxes at d_model 128
+        cm.wqkv_lo = nx.wqkv.tm_lo;
+      } else {
+        cm.wqkv = ly.wqkv.tm_hi;  // unused
+        cm.wqkv_lo = ly.wqkv.tm_lo;
+      }
       cm.o = h->tm_o16;
       cm.wo = ly.wo.tm_hi;
       cm.wo_lo = ly.wo.tm_lo;
@@ -505,6 +523,7 @@ const char* tfl_last_error(void) { return g_err.c_str(); }
 int tfl_launch_count(const tfl_handle* h, int causal) {
   (void)causal;
   if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (chain_fuses_qkv(h)) return 2 + 1 + 2 * h->L;  // layer 0's QKV GEMM, then attention + chain per layer
   const int per_layer = use_chain(h->D, h->F, h->opt.precision) ? 3 : (h->D == 128 ? 5 : 7);
   return 2 + per_layer * h->L;
 }

@@ -108,12 +108,19 @@ struct ChainArgs {
   const float *lnf_g = nullptr, *lnf_b = nullptr;  // final LN (last)
   const float* res = nullptr;                      // residual in: x (layer 0) or h32
   float* h32 = nullptr;                            // residual out (not last)
-  __half *n16 = nullptr, *n16lo = nullptr;         // next layer's QKV input, hi/lo (not last)
+  __half *n16 = nullptr, *n16lo = nullptr;         // next layer's QKV input, hi/lo (not last, not fused)
   float* out32 = nullptr;                          // model output (last)
+  // fuse_qkv (not last): the next layer's QKV projection runs in the tail on its
+  // normed rows, writing qkv16 directly (n16 is not written)
+  int fuse_qkv = 0;
+  float scale_qkv = 1.f;                           // next layer's W_qkv pre-scale undone
+  const float* bqkv = nullptr;                     // next layer's [bq | bk | bv]
+  __half* qkv16 = nullptr;                         // [M, 3 * 128]
 };
 
 struct ChainMaps {
   CUtensorMap o, wo, wo_lo, w1, w1_lo, w2, w2_lo;
+  CUtensorMap wqkv, wqkv_lo;  // next layer's W_qkv (fuse_qkv)
 };
 
 // TMA descriptors of one GEMM: A (and its lo plane), W (and its lo part).

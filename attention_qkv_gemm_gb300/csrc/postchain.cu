@@ -73,7 +73,8 @@ constexpr int kRedBytes = 4 * kParts * kGemmBM * 4;
 constexpr int kMaxF = 2048;
 constexpr int kPBo = 0, kPB2 = 128, kPLn1g = 256, kPLn1b = 384, kPLn2g = 512, kPLn2b = 640, kPLnng = 768,
               kPLnnb = 896, kPLnfg = 1024, kPLnfb = 1152, kPB1 = 1280;
-constexpr int kParamBytes = (kPB1 + kMaxF) * 4;
+constexpr int kPBqkv = kPB1 + kMaxF;  // next layer's [bq | bk | bv] (fuse_qkv)
+constexpr int kParamBytes = (kPBqkv + 3 * kD) * 4;
 constexpr size_t kSmem = 1024 + kOBytes + (size_t)kRing * kUnit + kXpBytes + kRedBytes + kParamBytes + 512;
 
 constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;  // GP: hi [384,448), lo [448,512)
@@ -117,6 +118,20 @@ __device__ __forceinline__ void normalize32(float* t, float mean, float rstd, co
   const float2* b2 = reinterpret_cast<const float2*>(b);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
+    const float2 gg = g2[i], bb = b2[i];
+    const uint64_t y = f2_fma(f2_mul(f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2), r2), f2_pack(gg.x, gg.y),
+                              f2_pack(bb.x, bb.y));
+    f2_unpack(y, t[2 * i], t[2 * i + 1]);
+  }
+}
+
+// (t - mean) * rstd * g + b for 16 values in place.
+__device__ __forceinline__ void normalize16(float* t, float mean, float rstd, const float* g, const float* b) {
+  const uint64_t m2 = f2_splat(mean), r2 = f2_splat(rstd);
+  const float2* g2 = reinterpret_cast<const float2*>(g);
+  const float2* b2 = reinterpret_cast<const float2*>(b);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
     const float2 gg = g2[i], bb = b2[i];
     const uint64_t y = f2_fma(f2_mul(f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2), r2), f2_pack(gg.x, gg.y),
                               f2_pack(bb.x, bb.y));
@@ -180,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     postchain_kernel(const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmWo,
                      const __grid_constant__ CUtensorMap tmWoLo, const __grid_constant__ CUtensorMap tmW1,
                      const __grid_constant__ CUtensorMap tmW1Lo, const __grid_constant__ CUtensorMap tmW2,
-                     const __grid_constant__ CUtensorMap tmW2Lo, const ChainArgs args) {
+                     const __grid_constant__ CUtensorMap tmW2Lo, const __grid_constant__ CUtensorMap tmWq,
+                     const __grid_constant__ CUtensorMap tmWqLo, const ChainArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sO = smem;
@@ -200,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* gp_ready = bars + 9;
   uint64_t* gp_free = bars + 10;
   uint64_t* g_read = bars + 11;
-  uint64_t* r_full = bars + 12;    // [kRing]
+  uint64_t* n_ready = bars + 12;   // fuse_qkv: the next layer's normed rows are in TMEM
+  uint64_t* qkv_full = bars + 13;  // fuse_qkv: the QKV accumulators are complete
+  uint64_t* r_full = bars + 14;    // [kRing]
   uint64_t* r_empty = r_full + kRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(r_empty + kRing);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -220,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(gp_ready, kEpi);
     mbar_init(gp_free, 1);
     mbar_init(g_read, kEpi);
+    mbar_init(n_ready, kEpi);
+    mbar_init(qkv_full, 1);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&r_full[i], 1);
       mbar_init(&r_empty[i], 1);
@@ -236,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmW1Lo);
     tma_prefetch_desc(&tmW2);
     tma_prefetch_desc(&tmW2Lo);
+    if (args.fuse_qkv) {
+      tma_prefetch_desc(&tmWq);
+      tma_prefetch_desc(&tmWqLo);
+    }
   }
   {
     const float* src[10] = {args.bo,    args.b2,    args.ln1_g, args.ln1_b, args.ln2_g,
@@ -245,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prm[i] = p ? __ldg(p + (i % kD)) : 0.f;
     }
     for (int i = threadIdx.x; i < args.F; i += blockDim.x) prm[kPB1 + i] = __ldg(args.b1 + i);
+    for (int i = threadIdx.x; i < 3 * kD; i += blockDim.x) prm[kPBqkv + i] = args.fuse_qkv ? __ldg(args.bqkv + i) : 0.f;
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -328,6 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = w2(c);
           if (ok && c + 2 < nch) ok = w1(c + 2);
         }
+        // fuse_qkv: the next layer's W_qkv, one 128-row block (q, k, v) per unit
+        for (int j = 0; j < 3 && ok && args.fuse_qkv; ++j)
+          ok = unit([&](uint8_t* d, uint64_t* b) {
+            tma_load_2d(d, &tmWq, b, 0, 128 * j);
+            tma_load_2d(d + kHalf, &tmWq, b, 64, 128 * j);
+            tma_load_2d(d + 2 * kHalf, &tmWqLo, b, 0, 128 * j);
+            tma_load_2d(d + 3 * kHalf, &tmWqLo, b, 64, 128 * j);
+          });
       }
     }
   } else if (warp == 1 || warp == kFfn1Warp) {
@@ -340,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id128 = idesc_f16(128, 128, 0, 0);
       const uint32_t tA1 = tmem_base + kColA1;
-      const int units = 1 + 2 * nch;  // ring units per tile
+      const int units = 1 + 2 * nch + (args.fuse_qkv ? 3 : 0);  // ring units per tile
       auto idx_w1 = [&](int k) { return k == 0 ? 1 : (k == 1 ? 2 : 2 * k); };
       auto idx_w2 = [&](int c) { return c <= nch - 2 ? 3 + 2 * c : 2 * nch; };
       // wait for ring unit g (counted over all tiles of this CTA); returns its smem address
@@ -355,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t tile_seq = 0;
       if (warp == 1) {
-        uint32_t oph = 0, orph = 0, gpr = 0;
+        uint32_t oph = 0, orph = 0, gpr = 0, nrph = 0, qbph = 0;
         for (int ti = blockIdx.x; ti < n_live && ok; ti += gridDim.x, ++tile_seq) {
           const uint32_t g0 = tile_seq * units;
           // o_proj into A1 (free once the previous tile's epilogue read OUT)
@@ -410,6 +443,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           umma_commit(out_full);
+          if (args.fuse_qkv) {
+            // the next layer's [q | k | v] = N W_qkv^T into [128, 512), N (hi, lo) in [0, 128).
+            // This thread's o_proj of the next tile, which rewrites [0, 128), issues after these.
+            if (!wait_bounded(n_ready, nrph, wc)) break;
+            nrph ^= 1u;
+            tc_fence_after();
+            for (int j = 0; j < 3 && ok; ++j) {
+              const uint32_t g = g0 + 1 + 2 * nch + j;
+              const uint32_t u = take(g);
+              if (!u) {
+                ok = false;
+                break;
+              }
+              const uint32_t d = tmem_base + 128 + 128 * j;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
+                const uint32_t ah = tmem_base + kk * 8, al = ah + 64;
+                umma_f16_ts(d, ah, bh, id128, kk > 0 ? 1u : 0u);
+                umma_f16_ts(d, al, bh, id128, 1u);
+                umma_f16_ts(d, ah, bl, id128, 1u);
+              }
+              give(g);
+            }
+            if (!ok) break;
+            umma_commit(qkv_full);
+            // the next tile's o_proj overwrites N: let these MMAs finish reading it first
+            if (!wait_bounded(qkv_full, qbph, wc)) break;
+            qbph ^= 1u;
+          }
         }
       } else {
         uint32_t arph = 0, grd = 0;
@@ -465,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* st = xpose + (warp - 2) * kXpWarp;
     WaitCtl ewc = wc;
     ewc.early_exit = false;  // the epilogue warps meet at a named barrier: leave only on their own bound
-    uint32_t afph = 0, ofph = 0, gfph = 0, gffph = 0;
+    uint32_t afph = 0, ofph = 0, gfph = 0, gffph = 0, qfph = 0;
     bool gp_written = false;  // GP holds an earlier chunk that FFN-out must have consumed before a rewrite
     int slot = 0;
     const float eps = args.eps;
@@ -595,7 +658,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(out_read);
       scale_bias32(tv, args.scale_2, prm + kPB2 + c0);
       if (args.post_ln) layer_norm32(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, part, r);
-      if (!args.last) {
+      if (!args.last && args.fuse_qkv) {
+        // the next layer's normed rows (pre-LN: its LN1 of t2; post-LN: t2 itself) as fp16
+        // hi/lo pairs into [0, 128), so its QKV MMAs run while t2 is stored as the residual.
+        // Every epilogue warp has read its OUT columns before the LayerNorm barriers.
+        float mean = 0.f, rstd = 1.f;
+        if (!args.post_ln) {
+          stats32(tv, eps, red, slot, part, r, mean, rstd);
+          slot = (slot + 2) & 3;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float nv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) nv[i] = tv[16 * j + i];
+          if (!args.post_ln) normalize16(nv, mean, rstd, prm + kPLnng + c0 + 16 * j, prm + kPLnnb + c0 + 16 * j);
+          uint32_t hi[8], lo[8];
+          split_pairs16(nv, hi, lo);
+          tmem_st8_u(tq + part * 16 + 8 * j, hi);
+          tmem_st8_u(tq + 64 + part * 16 + 8 * j, lo);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(n_ready);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          xp_store_f32x16(st, lane, tv + 16 * h, args.h32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
+        if (!wait_bounded(qkv_full, qfph, ewc)) break;
+        qfph ^= 1u;
+        tc_fence_after();
+        // qkv = acc 2^-s + b, fp16, this warp's 32 columns of each of q, k, v
+#pragma unroll 1
+        for (int j = 0; j < 3; ++j) {
+          float qv[32];
+          tmem_ld32(tq + 128 + 128 * j + c0, qv);
+          tmem_wait_ld();
+          scale_bias32(qv, args.scale_qkv, prm + kPBqkv + 128 * j + c0);
+          xp_store_f16<32>(st, lane, qv, args.qkv16 + (size_t)m0w * (3 * kD) + 128 * j + c0, nullptr, 3 * kD,
+                           in_rows);
+        }
+      } else if (!args.last) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           xp_store_f32x16(st, lane, tv + 16 * h, args.h32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
@@ -647,7 +750,8 @@ cudaError_t launch_postchain(const ChainMaps& mp, const ChainArgs& a, int num_sm
   const int tiles = (a.c.M + kGemmBM - 1) / kGemmBM;
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  postchain_kernel<<<grid, kThreads, kSmem, s>>>(mp.o, mp.wo, mp.wo_lo, mp.w1, mp.w1_lo, mp.w2, mp.w2_lo, a);
+  postchain_kernel<<<grid, kThreads, kSmem, s>>>(mp.o, mp.wo, mp.wo_lo, mp.w1, mp.w1_lo, mp.w2, mp.w2_lo, mp.wqkv,
+                                                 mp.wqkv_lo, a);
   return cudaGetLastError();
 }
 

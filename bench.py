@@ -127,17 +127,20 @@ def algorithmic(shape: synth.Shape, lens: np.ndarray, causal: bool):
 
 
 def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
-    """Algorithmic HBM bytes per launch of the row-streaming kernels (valid rows only)."""
-    D, F = shape.d_model, shape.d_ff
+    """Algorithmic HBM bytes per launch of the row-streaming kernels (valid rows only;
+    default precision: GEMM activations carry fp16 hi and lo planes)."""
+    D, F, L = shape.d_model, shape.d_ff, shape.n_layers
+    # the fused chain (d_model 128), averaged over the forward's L launches: attention output
+    # in, residual in, then either residual out + the next layer's qkv (fp16; its QKV
+    # projection runs in the chain's tail) or, for the last layer, the fp32 model output
+    chain = (L - 1) * (D * 2 + D * 4 + D * 4 + 3 * D * 2) + (D * 2 + D * 4 + D * 4)
     return {
-        "gemm_qkv": valid * (D * 2 + 3 * D * 2),
+        "gemm_qkv": valid * (2 * D * 2 + 3 * D * 2),
         "gemm_ffn1": valid * (D * 2 + F * 2),
         "gemm_oproj": valid * (D * 2 + D * 4 + D * 4 + D * 2),
         "gemm_ffn2": valid * (F * 2 + D * 4 + D * 4 + D * 2),
         "rownorm": valid * (D * 4 + D * 2),
-        # o_proj .. FFN-out fused (d_model 128): attention output in, residual in/out,
-        # next layer's normed rows out as fp16 hi/lo planes
-        "postchain": valid * (D * 2 + D * 4 + D * 4 + 2 * D * 2),
+        "postchain": valid * chain / L,
     }.get(kind)
 
 

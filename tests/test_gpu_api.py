@@ -97,7 +97,9 @@ def test_profile_forward_reports_every_launch():
             kinds = [k for k, _ in prof]
             # every launch except the length check is timed
             assert len(kinds) == pkg.tfl_launch_count(m.handle, 1) - 1
-            assert kinds.count("attention") == 2 and kinds.count("gemm_qkv") == 2
+            assert kinds.count("attention") == 2
+            # at d_model 128 the fused chain computes layer 1's QKV projection itself
+            assert kinds.count("gemm_qkv") == (1 if D == 128 else 2)
             assert all(ms > 0 for _, ms in prof)
         finally:
             m.close()
