@@ -28,9 +28,9 @@
 // q, k, v are strided views of the fused QKV output [B, S, 3D] (section 1.A,
 // head-split copies removed); O is written straight into [B, S, H*hd].
 //
-// Warp roles: warps 0-3 softmax + output (thread = query row), warp 4 TMA
-// producer (Q once per work item, K/V blocks into an NST-deep ring), warp 5
-// MMA issuer and TMEM owner.  Persistent CTAs claim work items from a global
+// Warp roles: warp 0 MMA issuer and TMEM owner, warp 1 TMA producer (Q once
+// per work item, K/V blocks into an NST-deep ring), warps 2-5 softmax +
+// output (thread = query row of TMEM lane quarter warp % 4).  Persistent CTAs claim work items from a global
 // atomic counter, heaviest first (causal: the last query blocks have the most
 // keys); the producer publishes each claimed item to the other warps through
 // a small shared-memory ring.
@@ -51,8 +51,12 @@ struct AttnCfg {
   static constexpr int ROWB = ATOM_C * 2;           // bytes of one row inside an atom
   static constexpr uint32_t SWZ = ROWB == 64 ? kSw64 : kSw128;
   static constexpr int Q_BYTES = BM * HD * 2;
+  // Q tiles: two at head_dim <= 64, so the next work item's Q loads while the
+  // current item runs (its load would otherwise wait for the last QK^T)
+  static constexpr int NQ = HD <= 64 ? 2 : 1;
   static constexpr int KV_BYTES = BN * HD * 2;      // one K (or V) block
-  static constexpr int XP_BYTES = 4 * 32 * 128;     // output transpose stage, one per softmax warp
+  static constexpr int XPW = HD == 64 ? 2048 : 4096;  // output transpose stage per softmax warp
+  static constexpr int XP_BYTES = 4 * XPW;
   static constexpr int NST = HD == 32 ? 4 : 2;
   static constexpr int CTAS_PER_SM = HD <= 64 ? 2 : 1;
   // Keys are taken 64 at a time (a sub-block; a K/V stage holds BN / 64 of
@@ -68,7 +72,7 @@ struct AttnCfg {
   static constexpr int LOOKAHEAD = NST * SUBS >= 3 ? 2 : 1;
   static constexpr int O_COL = HD <= 64 ? 192 : 256;
   static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
-  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)NST * 2 * KV_BYTES + XP_BYTES + 384;
+  static constexpr size_t SMEM = 1024 + (size_t)NQ * Q_BYTES + (size_t)NST * 2 * KV_BYTES + XP_BYTES + 384;
 };
 
 size_t attn_smem_bytes(int hd) {
@@ -119,20 +123,20 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + C::Q_BYTES;
+  uint8_t* sK = sQ + C::NQ * C::Q_BYTES;
   uint8_t* sV = sK + (size_t)C::NST * C::KV_BYTES;
   uint8_t* sX = sV + (size_t)C::NST * C::KV_BYTES;  // output transpose stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(sX + C::XP_BYTES);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* o_full = bars + 2;
-  uint64_t* o_empty = bars + 3;
-  uint64_t* drain = bars + 4;
-  uint64_t* s_full = bars + 5;   // [2] MMA -> softmax: S[b] computed
-  uint64_t* s_free = bars + 7;   // [2] softmax -> MMA: S[b] read
-  uint64_t* p_full = bars + 9;   // [2] softmax -> MMA: P[b] written
-  uint64_t* pv_done = bars + 11; // [2] MMA -> softmax: P[b] V done (P[b] free, O current)
-  uint64_t* kv_full = bars + 13;
+  uint64_t* q_full = bars + 0;   // [NQ] (bars 0 and 1)
+  uint64_t* q_empty = bars + 2;  // [NQ] (bars 2 and 3)
+  uint64_t* o_full = bars + 4;
+  uint64_t* o_empty = bars + 5;
+  uint64_t* drain = bars + 6;
+  uint64_t* s_full = bars + 7;   // [2] MMA -> softmax: S[b] computed
+  uint64_t* s_free = bars + 9;   // [2] softmax -> MMA: S[b] read
+  uint64_t* p_full = bars + 11;  // [2] softmax -> MMA: P[b] written
+  uint64_t* pv_done = bars + 13; // [2] MMA -> softmax: P[b] V done (P[b] free, O current)
+  uint64_t* kv_full = bars + 15;
   uint64_t* kv_empty = kv_full + C::NST;
   uint64_t* it_full = kv_empty + C::NST;
   uint64_t* it_empty = it_full + kItemRing;
@@ -143,8 +147,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int b = 0; b < C::NQ; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&s_free[b], 4);
@@ -166,11 +172,15 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     *never_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  // Warp 0 issues the MMAs: the oldest warp is the one the scheduler prefers
+  // when the running warp stalls, which keeps the MMA issue from being starved
+  // by the softmax warps sharing its scheduler.
+  constexpr int kMmaWarp = 0, kProdWarp = 1;
+  if (warp == kProdWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmKV);
   }
-  if (warp == 5) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -182,15 +192,15 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   const int items = args.B * args.H * nqb;
 
   uint32_t issued_mask = 0, issued_par = 0;  // producer: stages with loads in flight (abort path)
-  bool q_issued = false;
-  uint32_t q_par = 0;
+  uint32_t q_issued = 0, q_par = 0;  // producer: Q buffers with loads in flight, and their parities
   bool mma_issued = false;
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     // ------------------------------------------------------------ TMA producer + scheduler
     if (lane == 0) {
       int st = 0, ik = 0;
-      uint32_t kvph = 0, qph = 0, itph = 0;
+      uint32_t kvph = 0, qph = 0, itph = 0;  // qph: parity bit per Q buffer
+      int qb_i = 0;                          // Q buffer of the next item
       bool ok = true;
       while (ok) {
         // claim the next work item that holds a valid query (heaviest first)
@@ -208,14 +218,18 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           itph ^= 1u;
         }
         if (i < 0) break;
-        if (!wait_bounded(q_empty, qph ^ 1u, wc)) break;
-        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+        const uint32_t qpar = (qph >> qb_i) & 1u;
+        if (!wait_bounded(&q_empty[qb_i], qpar ^ 1u, wc)) break;
+        mbar_arrive_expect_tx(&q_full[qb_i], C::Q_BYTES);
+        uint8_t* sq = sQ + (size_t)qb_i * C::Q_BYTES;
 #pragma unroll
         for (int a = 0; a < C::NATOM; ++a)
-          tma_load_3d(sQ + a * (kAttnBM * C::ROWB), &tmQ, q_full, it.h * HD + a * C::ATOM_C, it.qb * kAttnBM, it.b);
-        q_issued = true;
-        q_par = qph;
-        qph ^= 1u;
+          tma_load_3d(sq + a * (kAttnBM * C::ROWB), &tmQ, &q_full[qb_i], it.h * HD + a * C::ATOM_C, it.qb * kAttnBM,
+                      it.b);
+        q_issued |= 1u << qb_i;
+        q_par = (q_par & ~(1u << qb_i)) | (qpar << qb_i);
+        qph ^= 1u << qb_i;
+        if (++qb_i == C::NQ) qb_i = 0;
         for (int j = 0; j < it.nkb; ++j) {
           if (!wait_bounded(&kv_empty[st], kvph ^ 1u, wc)) {
             ok = false;
@@ -239,18 +253,22 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         }
       }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer (whole warp)
+  } else if (warp == kMmaWarp) {
+   if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (one thread)
+    // Key rows at or past len_b hold exact zeros (the QKV producers write padding rows
+    // as zeros; rows past S are zero-filled by the TMA), so whole key blocks are used.
     constexpr uint32_t idesc_qk = idesc_f16(128, C::SUB, 0, 0);
     constexpr uint32_t idesc_pv = idesc_f16(128, HD, 0, 1);
     const uint32_t d_o = tmem_base + C::O_COL;
     int st = 0, pst = 0, ik = 0;  // stage of the next QK / of the next PV
-    uint32_t kvph = 0, qph = 0, oeph = 0, itph = 0;
+    uint32_t kvph = 0, qph = 0, oeph = 0, itph = 0;  // qph: parity bit per Q buffer
+    int qb_i = 0;    // Q buffer of the current item
     uint32_t g = 0;  // sub-blocks of all earlier items: sub-block g uses S/P buffer g & 1
     bool first_item = true, ok = true;
     // S[b] = Q K^T for the keys of half h of stage s
     auto issue_qk = [&](int s, int h, uint32_t b) {
-      const uint32_t sq = smem_u32(sQ);
+      const uint32_t sq = smem_u32(sQ + (size_t)qb_i * C::Q_BYTES);
       const uint32_t sk = smem_u32(sK + (size_t)s * C::KV_BYTES) + h * C::SUB * C::ROWB;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
@@ -273,8 +291,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     while (ok) {
       if (!wait_bounded(&it_full[ik], itph, wc)) break;
       const int i = it_slot[ik];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&it_empty[ik]);
+      mbar_arrive(&it_empty[ik]);
       if (++ik == kItemRing) {
         ik = 0;
         itph ^= 1u;
@@ -283,8 +300,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       Item it;
       decode_item(i, args, nqb, BN, it);
       const int nsub = item_subblocks(it, args.causal);
-      if (!wait_bounded(q_full, qph, wc)) break;
-      qph ^= 1u;
+      if (!wait_bounded(&q_full[qb_i], (qph >> qb_i) & 1u, wc)) break;
+      qph ^= 1u << qb_i;
       tc_fence_after();
       const uint32_t g0 = g;
       // QK^T of sub-block u, once its keys are resident and its S buffer has been read
@@ -294,34 +311,15 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         if (h == 0) {
           if (!wait_bounded(&kv_full[st], kvph, wc)) return false;
           tc_fence_after();
-          // Keys at or past len_b in this stage: clear their V rows so stale
-          // workspace contents can never reach O through a zero probability.
-          const int vrow0 = it.len - (u / C::SUBS) * BN;
-          if (vrow0 < BN) {
-            uint8_t* v = sV + (size_t)st * C::KV_BYTES;
-            for (int rr = max(vrow0, 0) + lane; rr < BN; rr += 32) {
-#pragma unroll
-              for (int a = 0; a < C::NATOM; ++a) {
-                uint4* row = reinterpret_cast<uint4*>(v + a * (BN * C::ROWB) + rr * C::ROWB);
-#pragma unroll
-                for (int c = 0; c < C::ROWB / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
-              }
-            }
-            fence_async_smem();
-            __syncwarp();
-          }
         }
         if (gg >= 2) {
           if (!wait_bounded(&s_free[b], ((gg - 2) >> 1) & 1u, wc)) return false;
           tc_fence_after();
         }
-        if (lane == 0) {
-          issue_qk(st, h, b);
-          mma_issued = true;
-          umma_commit(&s_full[b]);
-          if (u == nsub - 1) umma_commit(q_empty);
-        }
-        __syncwarp();
+        issue_qk(st, h, b);
+        mma_issued = true;
+        umma_commit(&s_full[b]);
+        if (u == nsub - 1) umma_commit(&q_empty[qb_i]);
         if (h == C::SUBS - 1 || u == nsub - 1) {
           if (++st == C::NST) {
             st = 0;
@@ -341,13 +339,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         }
         tc_fence_after();
         const bool stage_done = h == C::SUBS - 1 || u == nsub - 1;
-        if (lane == 0) {
-          issue_pv(pst, h, b, u > 0);
-          umma_commit(&pv_done[b]);
-          if (stage_done) umma_commit(&kv_empty[pst]);
-          if (u == nsub - 1) umma_commit(o_full);
-        }
-        __syncwarp();
+        issue_pv(pst, h, b, u > 0);
+        umma_commit(&pv_done[b]);
+        if (stage_done) umma_commit(&kv_empty[pst]);
+        if (u == nsub - 1) umma_commit(o_full);
         if (stage_done && ++pst == C::NST) pst = 0;
         return true;
       };
@@ -359,16 +354,19 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       if (!ok) break;
       g = g0 + nsub;
       first_item = false;
+      if (++qb_i == C::NQ) qb_i = 0;
     }
+   }
   } else {
-    // ------------------------------------------------------------ softmax + output (warps 0-3)
-    const int r = warp * 32 + lane;  // query row within the block == TMEM lane
-    const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16);
+    // ------------------------------------------------------------ softmax + output (warps 2-5)
+    const int q = warp & 3;          // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;     // query row within the block == TMEM lane
+    const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16);
     const uint32_t t_o = t_row + C::O_COL;
     const float sl2 = args.scale_log2;
     uint32_t oph = 0, itph = 0, g = 0;
     int ik = 0;
-    uint8_t* xst = sX + warp * 4096;
+    uint8_t* xst = sX + (warp - 2) * C::XPW;
 
     while (true) {
       if (!wait_bounded(&it_full[ik], itph, wc)) break;
@@ -384,7 +382,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       decode_item(i, args, nqb, BN, it);
       const int nsub = item_subblocks(it, args.causal);
       const int qpos = it.qb * kAttnBM + r;
-      const int wq0 = it.qb * kAttnBM + warp * 32;       // first query row of this warp
+      const int wq0 = it.qb * kAttnBM + q * 32;          // first query row of this warp
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int u = 0; u < nsub; ++u, ++g) {
@@ -519,14 +517,17 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       oph ^= 1u;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      const int q0 = it.qb * kAttnBM + warp * 32;  // first query row of this warp
+      const int q0 = it.qb * kAttnBM + q * 32;  // first query row of this warp
       const uint32_t rows = __ballot_sync(0xffffffffu, qpos < S);
       __half* orow0 = args.o16 + ((size_t)it.b * S + q0) * D + it.h * HD;
-      if constexpr (HD == 32) {
-        float o[32];
-        tmem_ld32(t_o, o);
-        tmem_wait_ld();
-        xp_store_f16<32>(xst, lane, o, orow0, nullptr, D, rows, inv);
+      if constexpr (HD <= 64) {
+#pragma unroll 1
+        for (int c = 0; c < HD; c += 32) {
+          float o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
+          xp_store_f16<32>(xst, lane, o, orow0 + c, nullptr, D, rows, inv);
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < HD / 64; ++c) {
@@ -549,18 +550,19 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   __syncthreads();
   if (*abort_flag) {
     const WaitCtl dc{args.c.status, never_flag, 100000000LL};
-    if (warp == 4 && lane == 0) {
-      if (q_issued) wait_bounded(q_full, q_par, dc);
+    if (warp == kProdWarp && lane == 0) {
+      for (int b = 0; b < C::NQ; ++b)
+        if (q_issued & (1u << b)) wait_bounded(&q_full[b], (q_par >> b) & 1u, dc);
       for (int s = 0; s < C::NST; ++s)
         if (issued_mask & (1u << s)) wait_bounded(&kv_full[s], (issued_par >> s) & 1u, dc);
     }
-    if (warp == 5 && lane == 0 && mma_issued) {
+    if (warp == kMmaWarp && lane == 0 && mma_issued) {
       umma_commit(drain);
       wait_bounded(drain, 0, dc);
     }
     __syncthreads();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }

@@ -280,6 +280,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if constexpr (EPI == EPI_BIAS_GELU_F16) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) v[i] = gelu_as7126(v[i]);
+          } else {
+            // q, k, v of padding rows are written as exact zeros, so attention can take
+            // whole key blocks (a zero probability times a zero value row) whatever the
+            // padding positions of the input held
+            if (!((valid_rows >> lane) & 1u)) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) v[i] = 0.f;
+            }
           }
           const size_t off = (size_t)m0w * args.N + n0;
           xp_store_f16<64>(st, lane, v, args.c16 + off, args.c16lo ? args.c16lo + off : nullptr, args.N, in_rows);

@@ -180,14 +180,6 @@ __device__ __forceinline__ void tmem_st8_u(uint32_t taddr, const uint32_t* r) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16_u(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
 
 }  // namespace
 
@@ -688,13 +680,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bounded(qkv_full, qfph, ewc)) break;
         qfph ^= 1u;
         tc_fence_after();
-        // qkv = acc 2^-s + b, fp16, this warp's 32 columns of each of q, k, v
+        // qkv = acc 2^-s + b, fp16, this warp's 32 columns of each of q, k, v; padding rows
+        // as exact zeros (attention takes whole key blocks: zero probability times zero value)
+        const bool valid = m < M && row_valid(m, S, lengths);
 #pragma unroll 1
         for (int j = 0; j < 3; ++j) {
           float qv[32];
           tmem_ld32(tq + 128 + 128 * j + c0, qv);
           tmem_wait_ld();
           scale_bias32(qv, args.scale_qkv, prm + kPBqkv + 128 * j + c0);
+          if (!valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) qv[i] = 0.f;
+          }
           xp_store_f16<32>(st, lane, qv, args.qkv16 + (size_t)m0w * (3 * kD) + 128 * j + c0, nullptr, 3 * kD,
                            in_rows);
         }
