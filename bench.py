@@ -139,9 +139,22 @@ def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
         "gemm_ffn1": valid * (D * 2 + F * 2),
         "gemm_oproj": valid * (D * 2 + D * 4 + D * 4 + D * 2),
         "gemm_ffn2": valid * (F * 2 + D * 4 + D * 4 + D * 2),
-        "rownorm": valid * (D * 4 + D * 2),
+        "rownorm": valid * (D * 4 + 2 * D * 2),
         "postchain": valid * chain / L,
     }.get(kind)
+
+
+def forward_bytes(shape: synth.Shape, valid: float):
+    """Algorithmic HBM bytes of one forward under this implementation's kernel split
+    (each intermediate written once and read once at its stored width, valid rows only)."""
+    D, L = shape.d_model, shape.n_layers
+    attn = valid * (3 * D * 2 + D * 2)  # q, k, v in; o out
+    if D == 128:  # input LN, layer 0's QKV GEMM, then attention + fused chain per layer
+        return (kernel_bytes("rownorm", shape, valid) + kernel_bytes("gemm_qkv", shape, valid)
+                + L * (attn + kernel_bytes("postchain", shape, valid)))
+    per_layer = (kernel_bytes("gemm_qkv", shape, valid) + attn + kernel_bytes("gemm_oproj", shape, valid)
+                 + kernel_bytes("gemm_ffn1", shape, valid) + kernel_bytes("gemm_ffn2", shape, valid))
+    return kernel_bytes("rownorm", shape, valid) + L * per_layer
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
@@ -364,6 +377,15 @@ def main():
             pg.destroy_process_group()
         return 0
 
+    # whole forward against its own bound: t_bound = max(HBM bytes / copy bandwidth,
+    # algorithmic FLOPs / dense fp16 tensor peak), both measured peaks
+    fb = forward_bytes(shape, alg["valid_tokens"])
+    flops = alg["linear_flops"] + alg["attn_flops"]
+    t_hbm, t_tc = fb / (peaks["hbm_gbs"] * 1e9), flops / (peaks["tc_tflops"] * 1e12)
+    fwd_roof = {"bytes": fb, "flops": flops, "t_bound_ms": max(t_hbm, t_tc) * 1e3,
+                "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": max(t_hbm, t_tc) / (ms / 1e3),
+                "peak_source": peaks["source"]}
+
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         dt, tok = run_oracle_sample(shape, prm, seed, min(shape.B, args.ref_seqs))
@@ -376,7 +398,9 @@ def main():
         "dtype": "f16", "data": "synthetic", "config": config_dict(shape), "roofline": roof, "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "algorithmic": {"valid_tokens": alg["valid_tokens"], "gflop": (alg["linear_flops"] + alg["attn_flops"]) / 1e9,
-                        "tflops_achieved": (alg["linear_flops"] + alg["attn_flops"]) / (ms / 1e3) / 1e12},
+                        "tflops_achieved": (alg["linear_flops"] + alg["attn_flops"]) / (ms / 1e3) / 1e12,
+                        "valid_tokens_per_s": alg["valid_tokens"] * world / (ms / 1e3)},
+        "forward_roofline": fwd_roof,
     }
     print(json.dumps(line), flush=True)
     if pg:
