@@ -4,8 +4,11 @@
 // O = softmax(Q K^T / sqrt(hd) + mask) V without materialising the score
 // matrix ("TikTok TechJam 2026 -- Problem 3", section 2.1):
 //   * Keys are taken in sub-blocks of 64.  S = Q K_u^T of sub-block u goes to
-//     tensor memory (fp32), in one of two buffers, so the tensor cores compute
-//     S of sub-block u + 2 while the softmax warps still work on u.
+//     tensor memory (fp32), in one of two buffers: once the softmax warps have
+//     turned S of sub-block u into P, the MMA thread issues P V of u and then
+//     Q K^T of u + 2, which runs while the softmax works on u + 1.  One barrier
+//     each way per sub-block: s_full (S ready; also certifies that the P V
+//     which last read the P buffer is done) and p_full (P written, S read).
 //   * Online softmax in fp32, one query row per thread (the row's TMEM lane):
 //     running max m, running sum l, O rescaled by exp(m_old - m_new)
 //     (section 2.1, the running-max recurrence).  The row max of a sub-block
@@ -66,10 +69,9 @@ struct AttnCfg {
   static constexpr int SUBS = BN / SUB;
   static constexpr int S_COL = 0;
   static constexpr int P_COL = 128;
-  // QK^T runs this many sub-blocks ahead of P V: at most 2 (two S buffers)
-  // and below the sub-blocks the K/V ring holds, since the ring slot of
-  // sub-block u + LOOKAHEAD is freed by a P V issued before it.
-  static constexpr int LOOKAHEAD = NST * SUBS >= 3 ? 2 : 1;
+  // QK^T of sub-block u + LOOKAHEAD is issued right after P V of sub-block u:
+  // at most 2 (two S buffers) and at most the sub-blocks the K/V ring holds.
+  static constexpr int LOOKAHEAD = NST * SUBS >= 2 ? 2 : 1;
   static constexpr int O_COL = HD <= 64 ? 192 : 256;
   static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
   static constexpr size_t SMEM = 1024 + (size_t)NQ * Q_BYTES + (size_t)NST * 2 * KV_BYTES + XP_BYTES + 384;
@@ -132,11 +134,12 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   uint64_t* o_full = bars + 4;
   uint64_t* o_empty = bars + 5;
   uint64_t* drain = bars + 6;
+  // s_full(g) completes once QK^T of sub-block g and every earlier MMA (so P V of
+  // sub-block g - 2, the previous user of P[g & 1]) are done
   uint64_t* s_full = bars + 7;   // [2] MMA -> softmax: S[b] computed
-  uint64_t* s_free = bars + 9;   // [2] softmax -> MMA: S[b] read
-  uint64_t* p_full = bars + 11;  // [2] softmax -> MMA: P[b] written
-  uint64_t* pv_done = bars + 13; // [2] MMA -> softmax: P[b] V done (P[b] free, O current)
-  uint64_t* kv_full = bars + 15;
+  uint64_t* p_full = bars + 9;   // [2] softmax -> MMA: P[b] written (S[b] read)
+  uint64_t* pv_done = bars + 11; // [2] MMA -> softmax: P[b] V done (O current; the rescale path)
+  uint64_t* kv_full = bars + 13;
   uint64_t* kv_empty = kv_full + C::NST;
   uint64_t* it_full = kv_empty + C::NST;
   uint64_t* it_empty = it_full + kItemRing;
@@ -153,7 +156,6 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 4);
       mbar_init(&p_full[b], 4);
       mbar_init(&pv_done[b], 1);
     }
@@ -312,10 +314,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           if (!wait_bounded(&kv_full[st], kvph, wc)) return false;
           tc_fence_after();
         }
-        if (gg >= 2) {
-          if (!wait_bounded(&s_free[b], ((gg - 2) >> 1) & 1u, wc)) return false;
-          tc_fence_after();
-        }
+        // S[b] was last read by sub-block gg - 2, whose P this thread has already waited for
         issue_qk(st, h, b);
         mma_issued = true;
         umma_commit(&s_full[b]);
@@ -348,8 +347,8 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       };
       for (int u = 0; ok && u < C::LOOKAHEAD && u < nsub; ++u) ok = qk(u);
       for (int u = 0; ok && u < nsub; ++u) {
-        if (u + C::LOOKAHEAD < nsub && !qk(u + C::LOOKAHEAD)) ok = false;
-        else if (!pv(u)) ok = false;
+        if (!pv(u)) ok = false;
+        else if (u + C::LOOKAHEAD < nsub && !qk(u + C::LOOKAHEAD)) ok = false;
       }
       if (!ok) break;
       g = g0 + nsub;
@@ -414,9 +413,6 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           if (mode != kTriLo) tmem_ld32(t_s + 32, sv + 32);
           tmem_wait_ld();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[b]);  // S[b] may now take sub-block g + 2
         if (mode == kNone) {
 #pragma unroll
           for (int e = 0; e < C::SUB / 2; ++e) pk[e] = 0u;
@@ -498,14 +494,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
           l_run += a0 + a1;
         }
-        if (g >= 2) {
-          // P[b] is free once the P V of sub-block g - 2 has completed
-          if (!wait_bounded(&pv_done[b], ((g - 2) >> 1) & 1u, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
+        // P[b] is free: s_full(g) completed after P V of sub-block g - 2
         tmem_st32_u(t_row + C::P_COL + b * (C::SUB / 2), pk);
         tmem_wait_st();
         tc_fence_before();
