@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* gp_free = bars + 10;
   uint64_t* g_read = bars + 11;
   uint64_t* n_ready = bars + 12;   // fuse_qkv: the next layer's normed rows are in TMEM
-  uint64_t* qkv_full = bars + 13;  // fuse_qkv: the QKV accumulators are complete
-  uint64_t* r_full = bars + 14;    // [kRing]
+  uint64_t* qkv_full = bars + 13;  // [3] fuse_qkv: the q, k, v accumulators are complete
+  uint64_t* r_full = bars + 16;    // [kRing]
   uint64_t* r_empty = r_full + kRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(r_empty + kRing);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(gp_free, 1);
     mbar_init(g_read, kEpi);
     mbar_init(n_ready, kEpi);
-    mbar_init(qkv_full, 1);
+    for (int j = 0; j < 3; ++j) mbar_init(&qkv_full[j], 1);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&r_full[i], 1);
       mbar_init(&r_empty[i], 1);
@@ -458,11 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_f16_ts(d, ah, bl, id128, 1u);
               }
               give(g);
+              // the epilogue drains q while k and v are computed
+              umma_commit(&qkv_full[j]);
             }
             if (!ok) break;
-            umma_commit(qkv_full);
             // the next tile's o_proj overwrites N: let these MMAs finish reading it first
-            if (!wait_bounded(qkv_full, qbph, wc)) break;
+            if (!wait_bounded(&qkv_full[2], qbph, wc)) break;
             qbph ^= 1u;
           }
         }
@@ -677,14 +678,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           xp_store_f32x16(st, lane, tv + 16 * h, args.h32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
-        if (!wait_bounded(qkv_full, qfph, ewc)) break;
-        qfph ^= 1u;
-        tc_fence_after();
         // qkv = acc 2^-s + b, fp16, this warp's 32 columns of each of q, k, v; padding rows
         // as exact zeros (attention takes whole key blocks: zero probability times zero value)
         const bool valid = m < M && row_valid(m, S, lengths);
+        bool qkv_ok = true;
 #pragma unroll 1
         for (int j = 0; j < 3; ++j) {
+          if (!wait_bounded(&qkv_full[j], qfph, ewc)) {
+            qkv_ok = false;
+            break;
+          }
+          tc_fence_after();
           float qv[32];
           tmem_ld32(tq + 128 + 128 * j + c0, qv);
           tmem_wait_ld();
@@ -696,6 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           xp_store_f16<32>(st, lane, qv, args.qkv16 + (size_t)m0w * (3 * kD) + 128 * j + c0, nullptr, 3 * kD,
                            in_rows);
         }
+        if (!qkv_ok) break;
+        qfph ^= 1u;
       } else if (!args.last) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)

@@ -333,10 +333,15 @@ __device__ __forceinline__ int seq_len(const int* lengths, int b, int S) {
 }
 
 // Does the row range [m0, m1) of the flattened [B*S] token axis hold any valid token?
+// True if rows [m0, m1) hold a valid row or a padding row that attention reads
+// as a key: attention takes keys in 64-key sub-blocks, so rows up to len_b
+// rounded up to 64 (at most S) must be written, as zeros past len_b.  With S a
+// multiple of 64 no 128-row tile holds only such rows.
 __device__ __forceinline__ bool rows_live(int m0, int m1, int S, const int* lengths) {
   if (lengths == nullptr) return m0 < m1;
   for (int b = m0 / S; b * S < m1; ++b) {
-    const int lo = max(m0, b * S), hi = min(m1, b * S + seq_len(lengths, b, S));
+    const int kr = min(S, (seq_len(lengths, b, S) + 63) & ~63);
+    const int lo = max(m0, b * S), hi = min(m1, b * S + kr);
     if (lo < hi) return true;
   }
   return false;

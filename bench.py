@@ -164,8 +164,8 @@ def forward_bytes(shape: synth.Shape, valid: float):
 # traffic is reported null.
 NCU_TRAFFIC = {
     # (kernel, workload): (csrc fingerprint, bytes per launch)
-    ("postchain", "B64_S1024_D128_causal_ragged"): ("c5b86c172990", 42.388480e6 + 17.843456e6),
-    ("attention", "B64_S1024_D128_causal_ragged"): ("c5b86c172990", 41.436672e6 + 0.574976e6),
+    ("postchain", "B64_S1024_D128_causal_ragged"): ("271d9629eda6", 42.613760e6 + 27.968000e6),
+    ("attention", "B64_S1024_D128_causal_ragged"): ("271d9629eda6", 41.432064e6 + 0.535552e6),
     ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("c5b86c172990", 27.821056e6 + 0.539392e6),
 }
 
