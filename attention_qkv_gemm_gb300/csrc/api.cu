@@ -83,6 +83,21 @@ bool make_map_qkv(CUtensorMap* m, const void* base, uint64_t B, uint64_t S, uint
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D map for 32-row tile stores of 64-byte row pieces (fp16: 32 columns, fp32: 16)
+// over a row-major [rows, cols] matrix, 64-byte swizzle.
+bool make_map_store64(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, bool f32) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const uint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {(cuuint32_t)(64 / es), 32};
+  cuuint32_t ess[2] = {1, 1};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, ess, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // One packed weight matrix: fp16 hi (and lo) parts of W * 2^s, and the 2^-s the GEMM applies.
@@ -373,9 +388,14 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
         ca.qkv16 = h->qkv16;
         cm.wqkv = nx.wqkv.tm_hi;  // 128-row boxes at d_model 128
         cm.wqkv_lo = nx.wqkv.tm_lo;
+        if (!make_map_store64(&cm.h32_st, h->h32, (uint64_t)h->M, h->D, true) ||
+            !make_map_store64(&cm.qkv_st, h->qkv16, (uint64_t)h->M, 3 * h->D, false))
+          return fail(TFL_ERR_CUDA, "chain store tensor map encoding failed");
       } else {
         cm.wqkv = ly.wqkv.tm_hi;  // unused
         cm.wqkv_lo = ly.wqkv.tm_lo;
+        cm.h32_st = h->tm_o16;  // unused
+        cm.qkv_st = h->tm_o16;
       }
       cm.o = h->tm_o16;
       cm.wo = ly.wo.tm_hi;

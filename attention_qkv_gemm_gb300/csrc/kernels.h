@@ -121,6 +121,9 @@ struct ChainArgs {
 struct ChainMaps {
   CUtensorMap o, wo, wo_lo, w1, w1_lo, w2, w2_lo;
   CUtensorMap wqkv, wqkv_lo;  // next layer's W_qkv (fuse_qkv)
+  // fuse_qkv: stores of the residual h32 [M, D] fp32 and q, k, v [M, 3D] fp16,
+  // box 64 B x 32 rows, 64-byte swizzle
+  CUtensorMap h32_st, qkv_st;
 };
 
 // TMA descriptors of one GEMM: A (and its lo plane), W (and its lo part).

@@ -183,12 +183,30 @@ __device__ __forceinline__ void tmem_st8_u(uint32_t taddr, const uint32_t* r) {
 
 }  // namespace
 
+// One warp's 32 rows x 64 bytes (v: this thread's row, four 16-byte pieces) into
+// its stage in the 64-byte-swizzled order of a SWIZZLE_64B map, then stored by
+// TMA at (x, y).  The stage is reused only after the previous store has read it.
+__device__ __forceinline__ void stage_tma_store(uint8_t* st, int lane, const uint4* v, const CUtensorMap* m, int x,
+                                                int y) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(st + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = v[c];
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(m, st, x, y);
+    bulk_commit();
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     postchain_kernel(const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmWo,
                      const __grid_constant__ CUtensorMap tmWoLo, const __grid_constant__ CUtensorMap tmW1,
                      const __grid_constant__ CUtensorMap tmW1Lo, const __grid_constant__ CUtensorMap tmW2,
                      const __grid_constant__ CUtensorMap tmW2Lo, const __grid_constant__ CUtensorMap tmWq,
-                     const __grid_constant__ CUtensorMap tmWqLo, const ChainArgs args) {
+                     const __grid_constant__ CUtensorMap tmWqLo, const __grid_constant__ CUtensorMap tmH32St,
+                     const __grid_constant__ CUtensorMap tmQkvSt, const ChainArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sO = smem;
@@ -533,6 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0w = t * kGemmBM + q * 32;
       const int m = m0w + lane;
       const uint32_t in_rows = __ballot_sync(0xffffffffu, m < M);
+      if (args.fuse_qkv) {  // the stage's last tensor store must have read it
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
       if (ti >= n_live) {  // all-padding tile (last layer only): zero output rows
         float z[16];
 #pragma unroll
@@ -676,8 +698,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(n_ready);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          xp_store_f32x16(st, lane, tv + 16 * h, args.h32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
+        for (int h = 0; h < 2; ++h) {
+          uint4 pk[4];
+          pack_f32x16(tv + 16 * h, pk);
+          stage_tma_store(st, lane, pk, &tmH32St, c0 + 16 * h, m0w);
+        }
         // qkv = acc 2^-s + b, fp16, this warp's 32 columns of each of q, k, v; padding rows
         // as exact zeros (attention takes whole key blocks: zero probability times zero value)
         const bool valid = m < M && row_valid(m, S, lengths);
@@ -697,8 +722,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) qv[i] = 0.f;
           }
-          xp_store_f16<32>(st, lane, qv, args.qkv16 + (size_t)m0w * (3 * kD) + 128 * j + c0, nullptr, 3 * kD,
-                           in_rows);
+          uint4 pk[4];
+          pack_f16<32>(qv, pk, false, 1.0f);
+          stage_tma_store(st, lane, pk, &tmQkvSt, 128 * j + c0, m0w);
         }
         if (!qkv_ok) break;
         qfph ^= 1u;
@@ -722,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  if (warp >= 2 && warp < 2 + kEpi && lane == 0) bulk_wait<0>();  // tensor stores complete
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -755,7 +782,7 @@ cudaError_t launch_postchain(const ChainMaps& mp, const ChainArgs& a, int num_sm
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
   postchain_kernel<<<grid, kThreads, kSmem, s>>>(mp.o, mp.wo, mp.wo_lo, mp.w1, mp.w1_lo, mp.w2, mp.w2_lo, mp.wqkv,
-                                                 mp.wqkv_lo, a);
+                                                 mp.wqkv_lo, mp.h32_st, mp.qkv_st, a);
   return cudaGetLastError();
 }
 
