@@ -269,25 +269,37 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     uint32_t g = 0;  // sub-blocks of all earlier items: sub-block g uses S/P buffer g & 1
     bool first_item = true, ok = true;
     // S[b] = Q K^T for the keys of half h of stage s
+    // Operand descriptors: built once; a buffer / stage / half only moves the
+    // start-address field (shared-memory byte offset / 16, which stays below 2^14).
+    const uint64_t qd0 = sdesc(smem_u32(sQ), 16, 8 * C::ROWB, C::SWZ);
+    const uint64_t kd0 = sdesc(smem_u32(sK), 16, 8 * C::ROWB, C::SWZ);
+    const uint64_t vd0 = sdesc(smem_u32(sV), BN * C::ROWB, 8 * C::ROWB, C::SWZ);
     auto issue_qk = [&](int s, int h, uint32_t b) {
-      const uint32_t sq = smem_u32(sQ + (size_t)qb_i * C::Q_BYTES);
-      const uint32_t sk = smem_u32(sK + (size_t)s * C::KV_BYTES) + h * C::SUB * C::ROWB;
+      const uint64_t ad0 = qd0 + (uint32_t)((qb_i * C::Q_BYTES) >> 4);
+      const uint64_t bd0 = kd0 + (uint32_t)((s * C::KV_BYTES + h * C::SUB * C::ROWB) >> 4);
+      const uint32_t d = tmem_base + C::S_COL + b * C::SUB;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
         const int a = kk / (C::ATOM_C / 16), w = kk % (C::ATOM_C / 16);
-        const uint64_t ad = sdesc(sq + a * (kAttnBM * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
-        const uint64_t bd = sdesc(sk + a * (BN * C::ROWB) + w * 32, 16, 8 * C::ROWB, C::SWZ);
-        umma_f16(tmem_base + C::S_COL + b * C::SUB, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        const uint64_t ad = ad0 + (uint32_t)((a * (kAttnBM * C::ROWB) + w * 32) >> 4);
+        const uint64_t bd = bd0 + (uint32_t)((a * (BN * C::ROWB) + w * 32) >> 4);
+        if (kk == 0)
+          umma_f16_k<0>(d, ad, bd, idesc_qk);
+        else
+          umma_f16_k<1>(d, ad, bd, idesc_qk);
       }
     };
     // O += P[b] V for the keys of half h of stage s (P from tensor memory)
     auto issue_pv = [&](int s, int h, uint32_t b, bool accumulate) {
-      const uint32_t sv = smem_u32(sV + (size_t)s * C::KV_BYTES) + h * C::SUB * C::ROWB;
+      const uint64_t bd0 = vd0 + (uint32_t)((s * C::KV_BYTES + h * C::SUB * C::ROWB) >> 4);
+      const uint32_t pa = tmem_base + C::P_COL + b * (C::SUB / 2);
 #pragma unroll
       for (int kk = 0; kk < C::SUB / 16; ++kk) {
-        const uint64_t bd = sdesc(sv + kk * 16 * C::ROWB, BN * C::ROWB, 8 * C::ROWB, C::SWZ);
-        umma_f16_ts(d_o, tmem_base + C::P_COL + b * (C::SUB / 2) + kk * 8, bd, idesc_pv,
-                    (accumulate || kk > 0) ? 1u : 0u);
+        const uint64_t bd = bd0 + (uint32_t)((kk * 16 * C::ROWB) >> 4);
+        if (kk == 0)
+          umma_f16_ts(d_o, pa, bd, idesc_pv, accumulate ? 1u : 0u);
+        else
+          umma_f16_ts_k<1>(d_o, pa + kk * 8, bd, idesc_pv);
       }
     };
     while (ok) {
