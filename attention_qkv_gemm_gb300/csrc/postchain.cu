@@ -87,28 +87,36 @@ __device__ __forceinline__ void chain_bar() { asm volatile("bar.sync 1, %0;" ::"
 // a slow one still reads.
 __device__ __forceinline__ void stats32(const float* t, float eps, float* red, int slot, int part, int r,
                                         float& mean, float& rstd) {
+  // This warp's 32 values: their sum and their sum of squares about their own mean;
+  // the four partial results of a row then combine in one exchange (Chan, Golub and
+  // LeVeque's pairwise update: M2 = sum M2_p + 32 sum (mean_p - mean)^2).
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i & 3] = f2_add(acc[i & 3], f2_pack(t[2 * i], t[2 * i + 1]));
   float s0, s1;
   f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
-  float* rs = red + slot * kParts * kGemmBM + r;
-  rs[part * kGemmBM] = s0 + s1;
-  chain_bar();
-  mean = ((rs[0] + rs[kGemmBM]) + (rs[2 * kGemmBM] + rs[3 * kGemmBM])) * (1.0f / kD);
-  const uint64_t m2 = f2_splat(mean);
+  const float sp = s0 + s1;
+  const uint64_t mp2 = f2_splat(sp * (1.0f / 32));
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = 0ull;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const uint64_t d = f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2);
+    const uint64_t d = f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), mp2);
     acc[i & 3] = f2_fma(d, d, acc[i & 3]);
   }
   f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+  float* rs = red + slot * kParts * kGemmBM + r;
   float* rq = rs + kParts * kGemmBM;
+  rs[part * kGemmBM] = sp;
   rq[part * kGemmBM] = s0 + s1;
   chain_bar();
-  rstd = rsqrtf(((rq[0] + rq[kGemmBM]) + (rq[2 * kGemmBM] + rq[3 * kGemmBM])) * (1.0f / kD) + eps);
+  const float a0 = rs[0], a1 = rs[kGemmBM], a2 = rs[2 * kGemmBM], a3 = rs[3 * kGemmBM];
+  mean = ((a0 + a1) + (a2 + a3)) * (1.0f / kD);
+  const float d0 = a0 * (1.0f / 32) - mean, d1 = a1 * (1.0f / 32) - mean, d2 = a2 * (1.0f / 32) - mean,
+              d3 = a3 * (1.0f / 32) - mean;
+  const float m2 = ((rq[0] + rq[kGemmBM]) + (rq[2 * kGemmBM] + rq[3 * kGemmBM])) +
+                   32.0f * ((d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3));
+  rstd = rsqrtf(m2 * (1.0f / kD) + eps);
 }
 
 // (t - mean) * rstd * g + b for 32 values in place; g, b: this warp's 32 columns in shared memory.
