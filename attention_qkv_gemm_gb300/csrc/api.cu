@@ -111,6 +111,8 @@ struct PackedW {
 struct LayerDev {
   PackedW wqkv, wo, w1, w2;
   float *bqkv, *bo, *b1, *b2, *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+  // fused chain, pre-LN: row sums of the LN-folded W1 and W_qkv (zeros otherwise)
+  float *u1, *uqkv;
 };
 
 struct GraphEntry {
@@ -166,6 +168,9 @@ struct tfl_handle {
   tfl_options opt{};
   int device = 0, num_sms = 0;
   int M = 0, D = 0, H = 0, hd = 0, F = 0, L = 0;
+  // pre-LN fused chain: W1 carries LN2's affine, and W_qkv of layers >= 1 carries
+  // LN1's (layer 0's QKV GEMM reads rows the input LayerNorm already normalised)
+  bool fold = false;
   void* wmem = nullptr;
   void* ws = nullptr;
   WsLayout lay{};
@@ -217,18 +222,9 @@ int stage_f32(const float* src, size_t n, float* tmp, const char* name) {
 // Pack `count` float32 matrices (consecutive rows of one GEMM operand) into
 // hi (and lo) fp16 parts of W * 2^s, s chosen from the largest |w| so that
 // the lo parts sit well inside the normal fp16 range.
-int pack_weights(const float* const* src, const size_t* n, int count, float* tmp, unsigned* dmax, PackedW& w,
-                 bool split, const char* name) {
-  size_t off = 0, total = 0;
-  for (int i = 0; i < count; ++i) total += n[i];
-  (void)total;
+int pack_staged(const float* tmp, size_t off, unsigned* dmax, PackedW& w, bool split, const char* name) {
   TFL_CUDA(cudaMemset(dmax, 0, sizeof(unsigned)), name);
-  for (int i = 0; i < count; ++i) {
-    int rc = stage_f32(src[i], n[i], tmp + off, name);
-    if (rc) return rc;
-    TFL_CUDA(launch_absmax(tmp + off, n[i], dmax, 0), name);
-    off += n[i];
-  }
+  TFL_CUDA(launch_absmax(tmp, off, dmax, 0), name);
   unsigned bits = 0;
   TFL_CUDA(cudaMemcpy(&bits, dmax, sizeof(unsigned), cudaMemcpyDeviceToHost), name);
   float amax;
@@ -244,6 +240,26 @@ int pack_weights(const float* const* src, const size_t* n, int count, float* tmp
   TFL_CUDA(launch_split_f16(tmp, w.hi, split ? w.lo : nullptr, off, scale, 0), name);
   TFL_CUDA(cudaDeviceSynchronize(), name);
   return TFL_OK;
+}
+
+// Stage `count` float32 matrices (consecutive rows of one GEMM operand) into tmp.
+int stage_weights(const float* const* src, const size_t* n, int count, float* tmp, size_t* total,
+                  const char* name) {
+  size_t off = 0;
+  for (int i = 0; i < count; ++i) {
+    const int rc = stage_f32(src[i], n[i], tmp + off, name);
+    if (rc) return rc;
+    off += n[i];
+  }
+  *total = off;
+  return TFL_OK;
+}
+
+int pack_weights(const float* const* src, const size_t* n, int count, float* tmp, unsigned* dmax, PackedW& w,
+                 bool split, const char* name) {
+  size_t total = 0;
+  const int rc = stage_weights(src, n, count, tmp, &total, name);
+  return rc ? rc : pack_staged(tmp, total, dmax, w, split, name);
 }
 
 int copy_f32(const float* src, size_t n, float* dst, const char* name) {
@@ -363,6 +379,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ca.inv_scale_2 = 1.0f / ly.w2.acc_scale;  // exact: acc_scale is a power of two
       ca.bo = ly.bo;
       ca.b1 = ly.b1;
+      ca.u1 = ly.u1;
       ca.b2 = ly.b2;
       ca.ln1_g = ly.ln1_g;
       ca.ln1_b = ly.ln1_b;
@@ -385,6 +402,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
         ca.fuse_qkv = 1;
         ca.scale_qkv = nx.wqkv.acc_scale;
         ca.bqkv = nx.bqkv;
+        ca.uqkv = nx.uqkv;
         ca.qkv16 = h->qkv16;
         cm.wqkv = nx.wqkv.tm_hi;  // 128-row boxes at d_model 128
         cm.wqkv_lo = nx.wqkv.tm_lo;
@@ -580,7 +598,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   const bool wsplit = o.precision >= 1;
   // weights block: per layer (1 or 2) x (3D*D + D*D + F*D + D*F) halves, 3D + D + F + D + 4D floats; + final LN
   const size_t wl_half = (wsplit ? 2 : 1) * ((size_t)3 * D * D + (size_t)D * D + 2 * (size_t)F * D);
-  const size_t wl_float = (size_t)3 * D + D + F + D + 4 * (size_t)D;
+  const size_t wl_float = (size_t)3 * D + D + F + D + 4 * (size_t)D + F + 3 * (size_t)D;
   const size_t per_layer = align_up(wl_half * 2, 1024) + align_up(wl_float * 4, 1024);
   const size_t wbytes = per_layer * L + align_up((size_t)2 * D * 4, 1024);
   if (o.max_workspace_bytes > 0 && (int64_t)(lay.total + wbytes) > o.max_workspace_bytes)
@@ -599,6 +617,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   h->F = F;
   h->L = L;
   h->lay = lay;
+  h->fold = use_chain(D, F, o.precision) && shape->norm_placement == 0;
   auto bail = [&](int code) {
     tfl_destroy(h);
     return code;
@@ -665,15 +684,9 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
     d.ln1_b = d.ln1_g + D;
     d.ln2_g = d.ln1_b + D;
     d.ln2_b = d.ln2_g + D;
+    d.u1 = d.ln2_b + D;
+    d.uqkv = d.u1 + F;
     const size_t DD = (size_t)D * D, FD = (size_t)F * D;
-    {
-      const float* qkv[3] = {src.wq, src.wk, src.wv};
-      const size_t nq[3] = {DD, DD, DD};
-      if (!rc) rc = pack_weights(qkv, nq, 3, tmp, dmax, d.wqkv, wsplit, "wq/wk/wv");
-    }
-    if (!rc) rc = pack_weights(&src.wo, &DD, 1, tmp, dmax, d.wo, wsplit, "wo");
-    if (!rc) rc = pack_weights(&src.w1, &FD, 1, tmp, dmax, d.w1, wsplit, "w1");
-    if (!rc) rc = pack_weights(&src.w2, &FD, 1, tmp, dmax, d.w2, wsplit, "w2");
     if (!rc) rc = copy_f32(src.bq, D, d.bqkv, "bq");
     if (!rc) rc = copy_f32(src.bk, D, d.bqkv + D, "bk");
     if (!rc) rc = copy_f32(src.bv, D, d.bqkv + 2 * D, "bv");
@@ -684,6 +697,27 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
     if (!rc) rc = copy_f32(src.ln1_b, D, d.ln1_b, "ln1_b");
     if (!rc) rc = copy_f32(src.ln2_g, D, d.ln2_g, "ln2_g");
     if (!rc) rc = copy_f32(src.ln2_b, D, d.ln2_b, "ln2_b");
+    if (!rc && cudaMemset(d.u1, 0, (size_t)(F + 3 * D) * sizeof(float)) != cudaSuccess)
+      rc = fail(TFL_ERR_CUDA, "weight row-sum init failed");
+    {
+      const float* qkv[3] = {src.wq, src.wk, src.wv};
+      const size_t nq[3] = {DD, DD, DD};
+      size_t n = 0;
+      if (!rc) rc = stage_weights(qkv, nq, 3, tmp, &n, "wq/wk/wv");
+      if (!rc && h->fold && l > 0 &&
+          launch_fold_ln(tmp, 3 * D, D, d.ln1_g, d.ln1_b, d.bqkv, d.uqkv, 0) != cudaSuccess)
+        rc = fail(TFL_ERR_CUDA, "LayerNorm fold of W_qkv failed");
+      if (!rc) rc = pack_staged(tmp, n, dmax, d.wqkv, wsplit, "wq/wk/wv");
+    }
+    if (!rc) rc = pack_weights(&src.wo, &DD, 1, tmp, dmax, d.wo, wsplit, "wo");
+    {
+      size_t n = 0;
+      if (!rc) rc = stage_weights(&src.w1, &FD, 1, tmp, &n, "w1");
+      if (!rc && h->fold && launch_fold_ln(tmp, F, D, d.ln2_g, d.ln2_b, d.b1, d.u1, 0) != cudaSuccess)
+        rc = fail(TFL_ERR_CUDA, "LayerNorm fold of W1 failed");
+      if (!rc) rc = pack_staged(tmp, n, dmax, d.w1, wsplit, "w1");
+    }
+    if (!rc) rc = pack_weights(&src.w2, &FD, 1, tmp, dmax, d.w2, wsplit, "w2");
     if (!rc) {
       auto maps = [&](PackedW& pw, uint64_t rows, uint64_t cols, uint32_t box_rows) {
         bool ok = make_map_2d(&pw.tm_hi, pw.hi, rows, cols, box_rows);

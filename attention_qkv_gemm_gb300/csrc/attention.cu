@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   using C = AttnCfg<HD>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
+  grid_launch_dependents();  // the next kernel may set itself up meanwhile
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::NQ * C::Q_BYTES;
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{args.c.status, abort_flag, args.c.timeout_ns};
+  grid_wait_prior();  // everything below reads or writes what earlier kernels use
 
   const int S = args.c.S, D = args.D;
   const int nqb = (S + kAttnBM - 1) / kAttnBM;
@@ -578,8 +580,7 @@ static cudaError_t launch_attn_hd(const CUtensorMap& tq, const CUtensorMap& tkv,
   const int cap = num_sms * C::CTAS_PER_SM;
   const int grid = items < cap ? items : cap;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, 192, C::SMEM, s>>>(tq, tkv, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, 192, C::SMEM, s, tq, tkv, a);
 }
 
 cudaError_t prepare_attention_kernels() {

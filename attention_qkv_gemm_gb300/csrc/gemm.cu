@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const GemmArgs args) {
   using C = GemmCfg<BN, AS, WS>;
   extern __shared__ uint8_t smem_raw[];
+  grid_launch_dependents();  // the next kernel may set itself up meanwhile
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red = reinterpret_cast<float*>(smem + (size_t)C::STAGES * C::STAGE);
   uint8_t* xpose = smem + (size_t)C::STAGES * C::STAGE + C::RED_BYTES;
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{args.c.status, abort_flag, args.c.timeout_ns};
+  grid_wait_prior();  // everything below reads or writes what earlier kernels use
 
   const int M = args.c.M, S = args.c.S;
   const int* lengths = args.c.lengths;
@@ -419,8 +421,8 @@ static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int num_sms
   const int tiles = ((a.c.M + kGemmBM - 1) / kGemmBM) * (a.N / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  gemm_kernel<BN, EPI, AS, WS><<<grid, kGemmThreads, C::SMEM, s>>>(mp.a, mp.alo, mp.b, mp.blo, a);
-  return cudaGetLastError();
+  return launch_dependent(gemm_kernel<BN, EPI, AS, WS>, grid, kGemmThreads, C::SMEM, s, mp.a, mp.alo, mp.b, mp.blo,
+                          a);
 }
 
 template <int BN, int EPI, int AS, int WS>

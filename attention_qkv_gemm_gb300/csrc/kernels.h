@@ -102,7 +102,11 @@ struct ChainArgs {
   int last = 0;     // 1: write the model tail (final LN + pad-mask) to out32
   float scale_o = 1.f, scale_1 = 1.f, scale_2 = 1.f;  // weight pre-scales undone
   float inv_scale_2 = 1.f;                            // 1 / scale_2 (a power of two)
+  // Pre-LN: the LayerNorm affines that feed FFN-in and the next layer's QKV are
+  // folded into those weights (b1, bqkv are the folded biases); u1, uqkv are the
+  // row sums of the folded weights, so LN(t) W^T + b = rstd (t W'^T) - rstd mean u + b'.
   const float *bo = nullptr, *b1 = nullptr, *b2 = nullptr;
+  const float *u1 = nullptr, *uqkv = nullptr;
   const float *ln1_g = nullptr, *ln1_b = nullptr, *ln2_g = nullptr, *ln2_b = nullptr;
   const float *lnn_g = nullptr, *lnn_b = nullptr;  // next layer's LN1 (pre-LN, not last)
   const float *lnf_g = nullptr, *lnf_b = nullptr;  // final LN (last)
@@ -131,6 +135,24 @@ struct GemmMaps {
   CUtensorMap a, alo, b, blo;
 };
 
+// Launch with programmatic dependent launch allowed (the kernel waits on the
+// device for the previous kernel of the stream before using its results).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launchers (return cudaError_t of the launch).
 // as: A carries a lo plane; ws: W carries a lo part (as requires ws).
 cudaError_t launch_gemm(int bn, int epi, int as, int ws, const GemmMaps& mp, const GemmArgs& a, int num_sms,
@@ -144,6 +166,9 @@ cudaError_t launch_gelu_selftest(int n, unsigned* out, cudaStream_t s);
 cudaError_t launch_prepare(const int* lengths, int B, int S, int M, int* status, int* tiles, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s);
 cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s);
+// In place: w [rows, cols] <- w * gamma (per column), bias += w beta, u = row sums of the result.
+cudaError_t launch_fold_ln(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias,
+                           float* u, cudaStream_t s);
 cudaError_t launch_split_f16(const float* src, __half* hi, __half* lo, size_t n, float scale, cudaStream_t s);
 cudaError_t launch_probe_wait(int* status, int64_t timeout_ns, cudaStream_t s);
 

@@ -74,7 +74,9 @@ constexpr int kMaxF = 2048;
 constexpr int kPBo = 0, kPB2 = 128, kPLn1g = 256, kPLn1b = 384, kPLn2g = 512, kPLn2b = 640, kPLnng = 768,
               kPLnnb = 896, kPLnfg = 1024, kPLnfb = 1152, kPB1 = 1280;
 constexpr int kPBqkv = kPB1 + kMaxF;  // next layer's [bq | bk | bv] (fuse_qkv)
-constexpr int kParamBytes = (kPBqkv + 3 * kD) * 4;
+constexpr int kPU1 = kPBqkv + 3 * kD;   // row sums of the LN-folded W1 (pre-LN; else zeros)
+constexpr int kPUqkv = kPU1 + kMaxF;   // row sums of the next layer's LN-folded W_qkv
+constexpr int kParamBytes = (kPUqkv + 3 * kD) * 4;
 constexpr size_t kSmem = 1024 + kOBytes + (size_t)kRing * kUnit + kXpBytes + kRedBytes + kParamBytes + 512;
 
 constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;  // GP: hi [384,448), lo [448,512)
@@ -167,6 +169,21 @@ __device__ __forceinline__ void scale_bias32(float* v, float scale, const float*
   }
 }
 
+// v[i] = v[i] * a + (u[i] * b + p[i]) for 32 values, u and p in shared memory: the
+// output of a linear layer whose input LayerNorm (per-row statistics folded into
+// a = rstd * 2^-s, b = -rstd * mean) is applied after the product.
+__device__ __forceinline__ void fold_bias32(float* v, float a, float b, const float* u, const float* p) {
+  const float2* u2 = reinterpret_cast<const float2*>(u);
+  const float2* p2 = reinterpret_cast<const float2*>(p);
+  const uint64_t a2 = f2_splat(a), b2 = f2_splat(b);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 uu = u2[i], q = p2[i];
+    const uint64_t c = f2_fma(f2_pack(uu.x, uu.y), b2, f2_pack(q.x, q.y));
+    f2_unpack(f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), a2, c), v[2 * i], v[2 * i + 1]);
+  }
+}
+
 // fp16 hi/lo pairs of 16 values (first value of a pair in the low half): v = hi + lo + O(2^-22 |v|).
 __device__ __forceinline__ void split_pairs16(const float* v, uint32_t* hi, uint32_t* lo) {
 #pragma unroll
@@ -216,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmWqLo, const __grid_constant__ CUtensorMap tmH32St,
                      const __grid_constant__ CUtensorMap tmQkvSt, const ChainArgs args) {
   extern __shared__ uint8_t smem_raw[];
+  grid_launch_dependents();  // the next kernel may set itself up meanwhile
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sO = smem;
   uint8_t* ring = sO + kOBytes;
@@ -280,14 +298,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   {
+    // every thread issues all of its loads before any store, so the staging costs
+    // one global-memory round trip rather than one per loop iteration
     const float* src[10] = {args.bo,    args.b2,    args.ln1_g, args.ln1_b, args.ln2_g,
                             args.ln2_b, args.lnn_g, args.lnn_b, args.lnf_g, args.lnf_b};
-    for (int i = threadIdx.x; i < 10 * kD; i += blockDim.x) {
-      const float* p = src[i / kD];
-      prm[i] = p ? __ldg(p + (i % kD)) : 0.f;
+    constexpr int kPrm = kParamBytes / 4, kPer = (kPrm + kThreads - 1) / kThreads;
+    auto source = [&](int i) -> const float* {
+      if (i < kPB1) return src[i / kD] ? src[i / kD] + (i % kD) : nullptr;
+      if (i < kPBqkv) return i - kPB1 < args.F ? args.b1 + (i - kPB1) : nullptr;
+      if (i < kPU1) return args.fuse_qkv ? args.bqkv + (i - kPBqkv) : nullptr;
+      if (i < kPUqkv) return (args.u1 && i - kPU1 < args.F) ? args.u1 + (i - kPU1) : nullptr;
+      return (args.fuse_qkv && args.uqkv) ? args.uqkv + (i - kPUqkv) : nullptr;
+    };
+    float pv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      const float* a = i < kPrm ? source(i) : nullptr;
+      pv[k] = a ? __ldg(a) : 0.f;
     }
-    for (int i = threadIdx.x; i < args.F; i += blockDim.x) prm[kPB1 + i] = __ldg(args.b1 + i);
-    for (int i = threadIdx.x; i < 3 * kD; i += blockDim.x) prm[kPBqkv + i] = args.fuse_qkv ? __ldg(args.bqkv + i) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      if (i < kPrm) prm[i] = pv[k];
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -295,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{args.c.status, abort_flag, args.c.timeout_ns};
+  grid_wait_prior();  // everything below reads or writes what earlier kernels use
 
   const int M = args.c.M, S = args.c.S;
   const int* lengths = args.c.lengths;
@@ -462,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           umma_commit(out_full);
           if (args.fuse_qkv) {
-            // the next layer's [q | k | v] = N W_qkv^T into [128, 512), N (hi, lo) in [0, 128).
+            // the next layer's [q | k | v] = N W_qkv^T into [128, 512), N (hi, lo pairs per
+            // 32-column part) in [0, 128).
             // This thread's o_proj of the next tile, which rewrites [0, 128), issues after these.
             if (!wait_bounded(n_ready, nrph, wc)) break;
             nrph ^= 1u;
@@ -478,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t bh = kdesc(u, kk), bl = kdesc(u + 2 * kHalf, kk);
-                const uint32_t ah = tmem_base + kk * 8, al = ah + 64;
+                // k-step kk: values 16 kk .. +15, written by epilogue part kk / 2
+                const uint32_t ah = tmem_base + 32 * (kk >> 1) + 8 * (kk & 1), al = ah + 16;
                 umma_f16_ts(d, ah, bh, id128, kk > 0 ? 1u : 0u);
                 umma_f16_ts(d, al, bh, id128, 1u);
                 umma_f16_ts(d, ah, bl, id128, 1u);
@@ -551,7 +588,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool gp_written = false;  // GP holds an earlier chunk that FFN-out must have consumed before a rewrite
     int slot = 0;
     const float eps = args.eps;
-    const uint64_t sc1 = f2_splat(args.scale_1);
     int t_next = (int)blockIdx.x < n_work ? tile_list[2 + blockIdx.x] : 0;  // loaded one tile ahead
     for (int ti = blockIdx.x; ti < n_work; ti += gridDim.x) {
       const int t = t_next;
@@ -585,6 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bounded(acc_full, afph, ewc)) break;
       afph ^= 1u;
       tc_fence_after();
+      // FFN-in input row statistics: GELU input = acc a1 + (u1 b1v + b1)
+      float a1 = args.scale_1, b1v = 0.f;
       {
         float tv[32];
         tmem_ld32(tq + kColA1 + c0, tv);
@@ -600,8 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
 #pragma unroll
         for (int i = 0; i < 32; ++i) tv[i] *= args.scale_2;
-        // normed input of the FFN, as fp16 hi/lo pairs in TMEM
-        if (!args.post_ln) layer_norm32(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, part, r);
+        // the FFN's input as fp16 hi/lo pairs in TMEM: t itself.  Pre-LN, LN2's
+        // affine is folded into W1 and its row statistics, computed while FFN-in
+        // runs, enter the GELU input (post-LN the FFN reads t unnormalised).
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint32_t hi[8], lo[8];
@@ -610,10 +649,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st8_u(tq + kColN2 + 64 + part * 16 + 8 * j, lo);
         }
         tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_read);
+        if (!args.post_ln) {
+          float mean, rstd;
+          stats32(tv, eps, red, slot, part, r, mean, rstd);
+          slot = (slot + 2) & 3;
+          a1 = rstd * args.scale_1;
+          b1v = -rstd * mean;
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_read);
+      const uint64_t a1x2 = f2_splat(a1), b1x2 = f2_splat(b1v);
       // pull the next tile's residual rows into L2 while this tile's FFN runs
       if (ti + (int)gridDim.x < n_live) {
         const int mn = t_next * kGemmBM + q * 32 + lane;
@@ -634,14 +681,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(g_read);
-        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + ((c + t) % nch) * kFC + c0);
+        const int f0 = ((c + t) % nch) * kFC + c0;
+        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + f0);
+        const float2* u1 = reinterpret_cast<const float2*>(prm + kPU1 + f0);
         // GELU and fp16 hi/lo split of the 32 values in registers, then into GP once
         // FFN-out of the previous chunk has read it (the GELU overlaps that MMA)
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 bq = b1[e];
-          const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), sc1, f2_pack(bq.x, bq.y)));
+          const float2 bq = b1[e], uq = u1[e];
+          const uint64_t x0 = f2_fma(f2_pack(uq.x, uq.y), b1x2, f2_pack(bq.x, bq.y));
+          const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), a1x2, x0));
           float g0, g1;
           f2_unpack(gl, g0, g1);
           const __half2 h = __floats2half2_rn(g0, g1);  // first value in the low half
@@ -682,29 +732,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       scale_bias32(tv, args.scale_2, prm + kPB2 + c0);
       if (args.post_ln) layer_norm32(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, part, r);
       if (!args.last && args.fuse_qkv) {
-        // the next layer's normed rows (pre-LN: its LN1 of t2; post-LN: t2 itself) as fp16
-        // hi/lo pairs into [0, 128), so its QKV MMAs run while t2 is stored as the residual.
-        // Every epilogue warp has read its OUT columns before the LayerNorm barriers.
-        float mean = 0.f, rstd = 1.f;
-        if (!args.post_ln) {
-          stats32(tv, eps, red, slot, part, r, mean, rstd);
-          slot = (slot + 2) & 3;
-        }
+        // the next layer's QKV input, t2 itself, as fp16 hi/lo pairs into this warp's own
+        // 32 OUT columns of [0, 128) (values c0 + 16 j .. +15: hi at 32 part + 8 j, lo 16
+        // further), so no other warp's OUT read is overtaken.  Pre-LN, the next LN1's
+        // affine is folded into W_qkv and its row statistics, computed while the QKV MMAs
+        // run, enter the drains below; post-LN, t2 is the normalised residual already.
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          float nv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) nv[i] = tv[16 * j + i];
-          if (!args.post_ln) normalize16(nv, mean, rstd, prm + kPLnng + c0 + 16 * j, prm + kPLnnb + c0 + 16 * j);
           uint32_t hi[8], lo[8];
-          split_pairs16(nv, hi, lo);
-          tmem_st8_u(tq + part * 16 + 8 * j, hi);
-          tmem_st8_u(tq + 64 + part * 16 + 8 * j, lo);
+          split_pairs16(tv + 16 * j, hi, lo);
+          tmem_st8_u(tq + 32 * part + 8 * j, hi);
+          tmem_st8_u(tq + 32 * part + 16 + 8 * j, lo);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(n_ready);
+        float aq = args.scale_qkv, bqv = 0.f;
+        if (!args.post_ln) {
+          float mean, rstd;
+          stats32(tv, eps, red, slot, part, r, mean, rstd);
+          slot = (slot + 2) & 3;
+          aq = rstd * args.scale_qkv;
+          bqv = -rstd * mean;
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint4 pk[4];
@@ -725,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float qv[32];
           tmem_ld32(tq + 128 + 128 * j + c0, qv);
           tmem_wait_ld();
-          scale_bias32(qv, args.scale_qkv, prm + kPBqkv + 128 * j + c0);
+          fold_bias32(qv, aq, bqv, prm + kPUqkv + 128 * j + c0, prm + kPBqkv + 128 * j + c0);
           if (!valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) qv[i] = 0.f;
@@ -789,9 +840,8 @@ cudaError_t launch_postchain(const ChainMaps& mp, const ChainArgs& a, int num_sm
   const int tiles = (a.c.M + kGemmBM - 1) / kGemmBM;
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  postchain_kernel<<<grid, kThreads, kSmem, s>>>(mp.o, mp.wo, mp.wo_lo, mp.w1, mp.w1_lo, mp.w2, mp.w2_lo, mp.wqkv,
-                                                 mp.wqkv_lo, mp.h32_st, mp.qkv_st, a);
-  return cudaGetLastError();
+  return launch_dependent(postchain_kernel, grid, kThreads, kSmem, s, mp.o, mp.wo, mp.wo_lo, mp.w1, mp.w1_lo, mp.w2,
+                          mp.w2_lo, mp.wqkv, mp.wqkv_lo, mp.h32_st, mp.qkv_st, a);
 }
 
 }  // namespace tfl

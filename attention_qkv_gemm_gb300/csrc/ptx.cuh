@@ -107,6 +107,17 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
 
+// ---------------------------------------------------------------- dependent launch
+// The forward's kernels are launched with programmatic dependent launch allowed:
+// each one lets the next start launching at once, and the next one waits for this
+// one's completion (and memory) before it touches anything produced earlier in the
+// stream, so only its set-up (barriers, tensor memory, constant parameters)
+// overlaps the previous kernel's tail.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

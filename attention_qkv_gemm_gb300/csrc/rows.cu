@@ -65,6 +65,8 @@ __device__ __forceinline__ void store_h4(__half* p, __half* lo, float4 v) {
 
 template <int V>
 __global__ void __launch_bounds__(256) rows_kernel(const RowArgs a) {
+  grid_launch_dependents();
+  grid_wait_prior();
   constexpr int D = 128 * V;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + warp;
@@ -108,10 +110,10 @@ cudaError_t launch_rows(const RowArgs& a, cudaStream_t s) {
   const int grid = (a.c.M + 7) / 8;
   if (grid <= 0) return cudaSuccess;
   switch (a.D / 128) {
-    case 1: rows_kernel<1><<<grid, 256, 0, s>>>(a); break;
-    case 2: rows_kernel<2><<<grid, 256, 0, s>>>(a); break;
-    case 4: rows_kernel<4><<<grid, 256, 0, s>>>(a); break;
-    case 8: rows_kernel<8><<<grid, 256, 0, s>>>(a); break;
+    case 1: return launch_dependent(rows_kernel<1>, grid, 256, 0, s, a);
+    case 2: return launch_dependent(rows_kernel<2>, grid, 256, 0, s, a);
+    case 4: return launch_dependent(rows_kernel<4>, grid, 256, 0, s, a);
+    case 8: return launch_dependent(rows_kernel<8>, grid, 256, 0, s, a);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -124,6 +126,8 @@ cudaError_t launch_rows(const RowArgs& a, cudaStream_t s) {
 // CTA gets within one tile of the same share however the padding falls.
 __global__ void __launch_bounds__(1024) prepare_kernel(const int* lengths, int B, int S, int M, int* status,
                                                        int* tiles) {
+  grid_launch_dependents();
+  grid_wait_prior();  // the previous forward's kernels read the tile list
   __shared__ int warp_tot[32];
   bool bad = false;
   if (lengths != nullptr)
@@ -174,8 +178,7 @@ __global__ void __launch_bounds__(1024) prepare_kernel(const int* lengths, int B
 }
 
 cudaError_t launch_prepare(const int* lengths, int B, int S, int M, int* status, int* tiles, cudaStream_t s) {
-  prepare_kernel<<<1, 1024, 0, s>>>(lengths, B, S, M, status, tiles);
-  return cudaGetLastError();
+  return launch_dependent(prepare_kernel, 1, 1024, 0, s, lengths, B, S, M, status, tiles);
 }
 
 __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
@@ -191,6 +194,33 @@ __global__ void absmax_kernel(const float* __restrict__ src, size_t n, unsigned*
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+}
+
+// Folds a LayerNorm's affine part into the linear layer that reads it, in place:
+// LN(t) W^T + bias = rstd (t W'^T) - rstd mean u + bias', with
+// W'[j][k] = W[j][k] gamma[k], u[j] = sum_k W'[j][k], bias'[j] = bias[j] + sum_k W[j][k] beta[k]
+// (sums in fp64).  One thread per output row; create-time only.
+__global__ void fold_ln_kernel(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias,
+                               float* u) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= rows) return;
+  float* wr = w + (size_t)j * cols;
+  double su = 0.0, sb = 0.0;
+  for (int k = 0; k < cols; ++k) {
+    const float wk = wr[k];
+    const float wf = wk * gamma[k];
+    wr[k] = wf;
+    su += (double)wf;
+    sb += (double)wk * (double)beta[k];
+  }
+  u[j] = (float)su;
+  bias[j] = (float)((double)bias[j] + sb);
+}
+
+cudaError_t launch_fold_ln(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias,
+                           float* u, cudaStream_t s) {
+  fold_ln_kernel<<<(rows + 127) / 128, 128, 0, s>>>(w, rows, cols, gamma, beta, bias, u);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s) {
