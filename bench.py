@@ -164,8 +164,8 @@ def forward_bytes(shape: synth.Shape, valid: float):
 # traffic is reported null.
 NCU_TRAFFIC = {
     # (kernel, workload): (csrc fingerprint, bytes per launch)
-    ("postchain", "B64_S1024_D128_causal_ragged"): ("271d9629eda6", 42.613760e6 + 27.968000e6),
-    ("attention", "B64_S1024_D128_causal_ragged"): ("271d9629eda6", 41.432064e6 + 0.535552e6),
+    ("postchain", "B64_S1024_D128_causal_ragged"): ("f3129ed7ca06", 42.611200e6 + 25.210112e6),
+    ("attention", "B64_S1024_D128_causal_ragged"): ("f3129ed7ca06", 41.431552e6 + 0.564992e6),
     ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("c5b86c172990", 27.821056e6 + 0.539392e6),
 }
 
