@@ -77,3 +77,19 @@ def test_repeat_calls_are_deterministic():
     a, _ = run_gpu(shape, prm, x, [192, 100], True, repeat=1)
     b, _ = run_gpu(shape, prm, x, [192, 100], True, repeat=3)
     np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("offset", [10.0, 100.0])
+def test_d128_residual_far_from_zero_mean(offset):
+    # The fused chain applies the pre-LN LayerNorms' statistics after the GEMMs (their
+    # affines folded into the weights), so the GEMM operands carry the residual's mean.
+    # Rows whose mean is many standard deviations away from zero must still meet the rule.
+    B, S, D, H, F, L = 2, 200, 128, 4, 512, 2
+    shape = synth.Shape(B, S, D, H, F, L, True)
+    prm = synth.params(4, shape, ln_affine="random")
+    x = (synth.input_x(4, shape) + np.float32(offset)).astype(np.float32)
+    lens = np.asarray([200, 90], dtype=np.int32)
+    u, rc = run_gpu(shape, prm, x, lens, True, 0)
+    assert rc == 0
+    r = oracle.forward(prm, H, x, lens, True, 0)
+    assert_gate(u, r, f"residual offset {offset}")
