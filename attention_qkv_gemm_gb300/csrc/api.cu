@@ -285,8 +285,22 @@ cudaError_t rec_mark(const Rec& r, cudaStream_t s, int kind) {
 }
 
 // Enqueue the whole forward on `st`.
+// Host memory the device can address directly (pinned and mapped; with unified
+// addressing its device pointer is the host pointer).
+bool host_resident(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost && a.devicePointer != nullptr;
+}
+
 int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out, cudaStream_t st,
             const Rec& rec) {
+  // x in host memory (read over the host link): the input row kernel also copies it
+  // into the residual buffer, so the first layer's residual read stays in HBM
+  const bool x_host = host_resident(x);
   const bool pre = h->shape.norm_placement == 0;
   const int prec = h->opt.precision;
   const int ws = prec >= 1 ? 1 : 0;  // weights carry lo parts
@@ -328,6 +342,10 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ra.row.bb = h->layers[0].ln1_b;
     } else {
       ra.row.flags = ROW_CAST16;
+    }
+    if (x_host) {
+      ra.row.flags |= ROW_WRITE_H;
+      ra.row.h32 = h->h32;
     }
     TFL_CUDA(launch_rows(ra, st), "input row kernel launch");
   }
@@ -391,7 +409,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       }
       ca.lnf_g = h->lnf_g;
       ca.lnf_b = h->lnf_b;
-      ca.res = (l == 0) ? x : h->h32;
+      ca.res = (l == 0 && !x_host) ? x : h->h32;
       ca.h32 = h->h32;
       ca.n16 = h->n16;
       ca.n16lo = h->n16lo;
@@ -434,7 +452,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       g.K = D;
       g.acc_scale = ly.wo.acc_scale;
       g.bias = ly.bo;
-      g.res = (l == 0) ? x : h->h32;
+      g.res = (l == 0 && !x_host) ? x : h->h32;
       RowOps ro;
       ro.eps = eps;
       ro.h32 = h->h32;
@@ -817,6 +835,28 @@ int tfl_forward_host(tfl_handle* h, const float* x_host, const int32_t* lengths_
   if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
   if (!x_host || !out_host) return fail(TFL_ERR_INVALID_ARG, "x and out must be non-NULL host pointers");
   const size_t bytes = (size_t)h->M * h->D * sizeof(float);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Pinned, mapped host buffers: the kernels read x and write out across the host
+  // link themselves (no staging copies); only the lengths are copied to the device.
+  if (host_resident(x_host) && host_resident(out_host) &&
+      !((reinterpret_cast<uintptr_t>(x_host) | reinterpret_cast<uintptr_t>(out_host)) & 15)) {
+    const uint8_t *xb = reinterpret_cast<const uint8_t*>(x_host), *ob = reinterpret_cast<const uint8_t*>(out_host);
+    if (xb < ob + bytes && ob < xb + bytes) return fail(TFL_ERR_INVALID_ARG, "out overlaps x");
+    if (lengths_host && !h->hlen_dev && cudaMalloc(&h->hlen_dev, (size_t)h->shape.B * sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TFL_ERR_OOM, "lengths buffer for tfl_forward_host");
+    }
+    if (lengths_host)
+      TFL_CUDA(cudaMemcpyAsync(h->hlen_dev, lengths_host, (size_t)h->shape.B * sizeof(int), cudaMemcpyHostToDevice, st),
+               "lengths upload");
+    cudaPointerAttributes ax{}, ao{};
+    TFL_CUDA(cudaPointerGetAttributes(&ax, x_host), "x attributes");
+    TFL_CUDA(cudaPointerGetAttributes(&ao, out_host), "out attributes");
+    const int rc = run_forward(h, static_cast<const float*>(ax.devicePointer), lengths_host ? h->hlen_dev : nullptr,
+                               causal, static_cast<float*>(ao.devicePointer), st);
+    if (rc) return rc;
+    return tfl_status(h, stream);
+  }
   if (!h->hx_dev) {
     if (cudaMalloc(&h->hx_dev, bytes) != cudaSuccess || cudaMalloc(&h->hout_dev, bytes) != cudaSuccess ||
         cudaMalloc(&h->hlen_dev, (size_t)h->shape.B * sizeof(int)) != cudaSuccess) {
@@ -824,7 +864,6 @@ int tfl_forward_host(tfl_handle* h, const float* x_host, const int32_t* lengths_
       return fail(TFL_ERR_OOM, "staging buffers for tfl_forward_host");
     }
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   TFL_CUDA(cudaMemcpyAsync(h->hx_dev, x_host, bytes, cudaMemcpyHostToDevice, st), "x upload");
   if (lengths_host)
     TFL_CUDA(cudaMemcpyAsync(h->hlen_dev, lengths_host, (size_t)h->shape.B * sizeof(int), cudaMemcpyHostToDevice, st),

@@ -137,10 +137,14 @@ int tfl_forward(tfl_handle* h, const float* x, const int32_t* lengths,
                 int causal, float* out, tfl_stream stream);
 
 /*
- * The same forward from host buffers: copies x (and lengths, if not NULL)
- * to handle-owned device buffers on `stream`, runs tfl_forward, copies out
- * back and synchronizes `stream`.  Buffers may be pageable or pinned (pinned
- * is faster).  Allocates its device buffers on the first call.
+ * The same forward from host buffers, synchronizing `stream` before it returns.
+ * If x and out are pinned host memory the device can address (cudaHostAlloc /
+ * cudaHostRegister, mapped), 16-byte aligned and not overlapping, the kernels
+ * read x and write out across the host link directly (the input row kernel
+ * keeps a device copy of x as the first residual) and only the lengths are
+ * copied.  Otherwise (pageable buffers) x and lengths are copied to
+ * handle-owned device buffers, tfl_forward runs and out is copied back.
+ * Allocates its device buffers on the first call.
  * Returns what tfl_status returns after the run.
  */
 int tfl_forward_host(tfl_handle* h, const float* x_host, const int32_t* lengths_host,

@@ -56,10 +56,13 @@ def test_precision_modes_order_errors():
     assert errs[2] < 0.6 * errs[0], errs
 
 
-def test_forward_host_matches_device_path():
+@pytest.mark.parametrize("D", [128, 256])
+def test_forward_host_matches_device_path(D):
+    # pinned buffers take the mapped path (kernels read x / write out across the host
+    # link), pageable ones the staging copies; both must equal the device path bit for bit
     import torch
     import attention_qkv_gemm_gb300 as pkg
-    shape = synth.Shape(2, 200, 128, 4, 512, 2, True)
+    shape = synth.Shape(2, 200, D, 4, 512, 2, True)
     prm = synth.params(4, shape)
     x = synth.input_x(4, shape)
     lens = np.array([200, 111], dtype=np.int32)
