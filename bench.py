@@ -162,19 +162,30 @@ def forward_bytes(shape: synth.Shape, valid: float):
 # only while every kernel source it was taken with is unchanged: the fingerprint is
 # the sha256 prefix over all files of the package's csrc/ directory; otherwise
 # traffic is reported null.
+# The translation unit of each measured kernel plus every kernel header: the
+# fingerprint a traffic figure was captured with (host code such as api.cu is
+# not part of any kernel's build).
+KERNEL_SOURCES = {
+    "postchain": ["postchain.cu"],
+    "attention": ["attention.cu"],
+    "gemm_qkv": ["gemm.cu"],
+}
+KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh"]
+
 NCU_TRAFFIC = {
-    # (kernel, workload): (csrc fingerprint, bytes per launch)
-    ("postchain", "B64_S1024_D128_causal_ragged"): ("f3129ed7ca06", 42.611200e6 + 25.210112e6),
-    ("attention", "B64_S1024_D128_causal_ragged"): ("f3129ed7ca06", 41.431552e6 + 0.564992e6),
-    ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("c5b86c172990", 27.821056e6 + 0.539392e6),
+    # (kernel, workload): (kernel source fingerprint, bytes per launch)
+    ("postchain", "B64_S1024_D128_causal_ragged"): ("6b5fd17c012f", 42.611200e6 + 25.210112e6),
+    ("attention", "B64_S1024_D128_causal_ragged"): ("cadac466a603", 41.431552e6 + 0.564992e6),
 }
 
 
-def csrc_fingerprint() -> str:
+def csrc_fingerprint(kernel: str = None) -> str:
+    """sha256 prefix over the package's csrc/ files (all of them, or one kernel's sources)."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "attention_qkv_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    files = sorted(os.listdir(d)) if kernel is None else sorted(KERNEL_SOURCES[kernel] + KERNEL_HEADERS)
+    for f in files:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:12]
@@ -182,10 +193,10 @@ def csrc_fingerprint() -> str:
 
 def ncu_traffic(kernel: str, workload: str):
     e = NCU_TRAFFIC.get((kernel, workload))
-    if e is None:
+    if e is None or kernel not in KERNEL_SOURCES:
         return None
     sha, nbytes = e
-    return nbytes if csrc_fingerprint() == sha else None
+    return nbytes if csrc_fingerprint(kernel) == sha else None
 
 
 def run_oracle_sample(shape, prm, seed, n_seq):
