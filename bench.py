@@ -176,6 +176,7 @@ NCU_TRAFFIC = {
     # (kernel, workload): (kernel source fingerprint, bytes per launch)
     ("postchain", "B64_S1024_D128_causal_ragged"): ("6b5fd17c012f", 42.611200e6 + 25.210112e6),
     ("attention", "B64_S1024_D128_causal_ragged"): ("cadac466a603", 41.431552e6 + 0.564992e6),
+    ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("f3319f953b69", 27.822080e6 + 0.816384e6),
 }
 
 
