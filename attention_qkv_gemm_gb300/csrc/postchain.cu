@@ -135,20 +135,6 @@ __device__ __forceinline__ void normalize32(float* t, float mean, float rstd, co
   }
 }
 
-// (t - mean) * rstd * g + b for 16 values in place.
-__device__ __forceinline__ void normalize16(float* t, float mean, float rstd, const float* g, const float* b) {
-  const uint64_t m2 = f2_splat(mean), r2 = f2_splat(rstd);
-  const float2* g2 = reinterpret_cast<const float2*>(g);
-  const float2* b2 = reinterpret_cast<const float2*>(b);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float2 gg = g2[i], bb = b2[i];
-    const uint64_t y = f2_fma(f2_mul(f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2), r2), f2_pack(gg.x, gg.y),
-                              f2_pack(bb.x, bb.y));
-    f2_unpack(y, t[2 * i], t[2 * i + 1]);
-  }
-}
-
 // LayerNorm of a row split over four warps; g, b: shared-memory gamma / beta of the whole row.
 __device__ __forceinline__ void layer_norm32(float* t, float eps, const float* g, const float* b, int c0,
                                              float* red, int& slot, int part, int r) {
