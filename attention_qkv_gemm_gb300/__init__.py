@@ -89,6 +89,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.tfl_create.restype = ctypes.c_int
     lib.tfl_forward.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
     lib.tfl_forward.restype = ctypes.c_int
+    lib.tfl_forward_bf16.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.tfl_forward_bf16.restype = ctypes.c_int
     lib.tfl_forward_noalloc.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
     lib.tfl_forward_noalloc.restype = ctypes.c_int
     lib.tfl_forward_host.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
@@ -148,6 +150,11 @@ def tfl_create(shape: TflShape, layer_ptrs: Sequence[dict], lnf_g: int, lnf_b: i
 
 def tfl_forward(handle: int, x: int, lengths: Optional[int], causal: int, out: int, stream: int = 0) -> None:
     _check(load().tfl_forward(handle, x, lengths, int(causal), out, stream))
+
+
+def tfl_forward_bf16(handle: int, x: int, lengths: Optional[int], causal: int, out: int, stream: int = 0) -> None:
+    """The forward with bf16 model inputs and outputs (device pointers to bf16 [B, S, D])."""
+    _check(load().tfl_forward_bf16(handle, x, lengths, int(causal), out, stream))
 
 
 def tfl_forward_noalloc(handle: int, x: int, lengths: Optional[int], causal: int, out: int, stream: int = 0) -> None:
@@ -229,14 +236,18 @@ class TransformerStack:
         del keep
 
     def forward(self, x, lengths=None, causal: bool = True, out=None, stream: Optional[int] = None):
-        """x: torch float32 CUDA [B, S, D]; lengths: int32 CUDA [B] or None. Returns out."""
+        """x: torch float32 or bfloat16 CUDA [B, S, D]; lengths: int32 CUDA [B] or None.
+        Returns out, in x's dtype."""
         import torch
         if out is None:
             out = torch.empty_like(x)
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
-        tfl_forward(self.handle, x.data_ptr(), None if lengths is None else lengths.data_ptr(), int(causal),
-                    out.data_ptr(), stream)
+        fn = tfl_forward_bf16 if x.dtype == torch.bfloat16 else tfl_forward
+        if out.dtype != x.dtype:
+            raise ValueError("out must have x's dtype")
+        fn(self.handle, x.data_ptr(), None if lengths is None else lengths.data_ptr(), int(causal), out.data_ptr(),
+           stream)
         return out
 
     def status(self, stream: Optional[int] = None) -> int:

@@ -117,6 +117,7 @@ struct LayerDev {
 
 struct GraphEntry {
   int causal;
+  int bf16;
   const void* x;
   const void* len;
   void* out;
@@ -296,11 +297,14 @@ bool host_resident(const void* p) {
   return a.type == cudaMemoryTypeHost && a.devicePointer != nullptr;
 }
 
+// bf16 = 1: x and out hold bf16 model-dtype rows (the pointers are reinterpreted).
 int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out, cudaStream_t st,
-            const Rec& rec) {
-  // x in host memory (read over the host link): the input row kernel also copies it
-  // into the residual buffer, so the first layer's residual read stays in HBM
-  const bool x_host = host_resident(x);
+            const Rec& rec, int bf16 = 0) {
+  // x in host memory (read over the host link) or in bf16: the input row kernel also
+  // writes it into the fp32 residual buffer, which is then the first layer's residual
+  const bool x_host = bf16 || host_resident(x);
+  const __nv_bfloat16* xbf = bf16 ? reinterpret_cast<const __nv_bfloat16*>(x) : nullptr;
+  __nv_bfloat16* outbf = bf16 ? reinterpret_cast<__nv_bfloat16*>(out) : nullptr;
   const bool pre = h->shape.norm_placement == 0;
   const int prec = h->opt.precision;
   const int ws = prec >= 1 ? 1 : 0;  // weights carry lo parts
@@ -332,7 +336,8 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
     RowArgs ra;
     ra.c = c;
     ra.D = D;
-    ra.in32 = x;
+    ra.in32 = bf16 ? nullptr : x;
+    ra.inbf = xbf;
     ra.row.eps = eps;
     ra.row.n16 = h->n16;
     ra.row.n16lo = h->n16lo;
@@ -413,7 +418,8 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ca.h32 = h->h32;
       ca.n16 = h->n16;
       ca.n16lo = h->n16lo;
-      ca.out32 = out;
+      ca.out32 = bf16 ? nullptr : out;
+      ca.outbf = outbf;
       ChainMaps cm;
       if (!last && chain_fuses_qkv(h)) {
         const LayerDev& nx = h->layers[l + 1];
@@ -515,7 +521,8 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ro.h32 = h->h32;
       ro.n16 = h->n16;
       ro.n16lo = h->n16lo;
-      ro.out32 = out;
+      ro.out32 = bf16 ? nullptr : out;
+      ro.outbf = outbf;
       if (!pre) {
         ro.flags |= ROW_POST_LN;
         ro.ga = ly.ln2_g;
@@ -774,17 +781,17 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
 }
 
 static int run_forward(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out,
-                       cudaStream_t st) {
-  if (!h->opt.use_graph) return enqueue(h, x, lengths, causal, out, st, Rec{});
+                       cudaStream_t st, int bf16 = 0) {
+  if (!h->opt.use_graph) return enqueue(h, x, lengths, causal, out, st, Rec{}, bf16);
   for (auto& g : h->graphs)
-    if (g.causal == causal && g.x == x && g.len == lengths && g.out == out) {
+    if (g.causal == causal && g.bf16 == bf16 && g.x == x && g.len == lengths && g.out == out) {
       TFL_CUDA(cudaGraphLaunch(g.exec, st), "cudaGraphLaunch");
       return TFL_OK;
     }
   cudaGraph_t graph = nullptr;
   cudaStream_t cs = h->cap_stream;
   TFL_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "cudaStreamBeginCapture");
-  int rc = enqueue(h, x, lengths, causal, out, cs, Rec{});
+  int rc = enqueue(h, x, lengths, causal, out, cs, Rec{}, bf16);
   cudaError_t e = cudaStreamEndCapture(cs, &graph);
   if (rc) {
     if (graph) cudaGraphDestroy(graph);
@@ -799,7 +806,7 @@ static int run_forward(tfl_handle* h, const float* x, const int32_t* lengths, in
     cudaGraphExecDestroy(h->graphs.front().exec);
     h->graphs.erase(h->graphs.begin());
   }
-  h->graphs.push_back(GraphEntry{causal, x, lengths, out, exec});
+  h->graphs.push_back(GraphEntry{causal, bf16, x, lengths, out, exec});
   TFL_CUDA(cudaGraphLaunch(exec, st), "cudaGraphLaunch");
   return TFL_OK;
 }
@@ -815,6 +822,21 @@ int tfl_forward(tfl_handle* h, const float* x, const int32_t* lengths, int causa
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
     return fail(TFL_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
   return run_forward(h, x, lengths, causal, out, static_cast<cudaStream_t>(stream));
+}
+
+int tfl_forward_bf16(tfl_handle* h, const void* x, const int32_t* lengths, int causal, void* out,
+                     tfl_stream stream) {
+  g_err.clear();
+  if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (!x || !out) return fail(TFL_ERR_INVALID_ARG, "x and out must be non-NULL device pointers");
+  if (causal != 0 && causal != 1) return fail(TFL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  const size_t bytes = (size_t)h->M * h->D * 2;
+  const uint8_t *xb = static_cast<const uint8_t*>(x), *ob = static_cast<const uint8_t*>(out);
+  if (xb < ob + bytes && ob < xb + bytes) return fail(TFL_ERR_INVALID_ARG, "out overlaps x");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(TFL_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  return run_forward(h, static_cast<const float*>(x), lengths, causal, static_cast<float*>(out),
+                     static_cast<cudaStream_t>(stream), 1);
 }
 
 int tfl_status(tfl_handle* h, tfl_stream stream) {

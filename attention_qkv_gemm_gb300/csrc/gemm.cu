@@ -248,8 +248,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < NH / 32; ++c)
-              xp_store_f32x32(st, lane, z, args.row.out32 + (size_t)m0w * BN + c0 + c * 32, BN, in_rows);
+            for (int c = 0; c < NH / 32; ++c) {
+              const size_t off = (size_t)m0w * BN + c0 + c * 32;
+              if (args.row.outbf)
+                xp_store_bf16<32>(st, lane, z, args.row.outbf + off, BN, in_rows);
+              else
+                xp_store_f32x32(st, lane, z, args.row.out32 + off, BN, in_rows);
+            }
           }
         }
         continue;
@@ -364,8 +369,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if (fin) {
 #pragma unroll
-            for (int c = 0; c < NH / 32; ++c)
-              xp_store_f32x32(st, lane, tv + c * 32, ro.out32 + (size_t)m0w * BN + c0 + c * 32, BN, in_rows);
+            for (int c = 0; c < NH / 32; ++c) {
+              const size_t off = (size_t)m0w * BN + c0 + c * 32;
+              if (ro.outbf)
+                xp_store_bf16<32>(st, lane, tv + c * 32, ro.outbf + off, BN, in_rows);
+              else
+                xp_store_f32x32(st, lane, tv + c * 32, ro.out32 + off, BN, in_rows);
+            }
           } else {
 #pragma unroll
             for (int c = 0; c < NH / 64; ++c) {

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -36,6 +37,7 @@ struct RowOps {
   __half* n16 = nullptr;                     // [M, D] fp16 (hi part when split)
   __half* n16lo = nullptr;                   // [M, D] fp16 residual plane, or null
   float* out32 = nullptr;                    // [M, D]
+  __nv_bfloat16* outbf = nullptr;            // [M, D] bf16 model output instead of out32 (FINAL)
 };
 
 struct Common {
@@ -83,6 +85,7 @@ struct RowArgs {
   Common c;
   int D = 0;
   const float* in32 = nullptr;   // [M, D] fp32 input rows (x or h32)
+  const __nv_bfloat16* inbf = nullptr;  // [M, D] bf16 input rows instead of in32
   RowOps row;
 };
 
@@ -114,6 +117,7 @@ struct ChainArgs {
   float* h32 = nullptr;                            // residual out (not last)
   __half *n16 = nullptr, *n16lo = nullptr;         // next layer's QKV input, hi/lo (not last, not fused)
   float* out32 = nullptr;                          // model output (last)
+  __nv_bfloat16* outbf = nullptr;                  // bf16 model output instead of out32 (last)
   // fuse_qkv (not last): the next layer's QKV projection runs in the tail on its
   // normed rows, writing qkv16 directly (n16 is not written)
   int fuse_qkv = 0;

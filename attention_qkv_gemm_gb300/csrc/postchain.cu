@@ -586,12 +586,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (ti >= n_live) {  // all-padding tile (last layer only): zero output rows
-        float z[16];
+        float z[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = 0.f;
+        for (int i = 0; i < 32; ++i) z[i] = 0.f;
+        if (args.outbf) {
+          xp_store_bf16<32>(st, lane, z, args.outbf + (size_t)m0w * kD + c0, kD, in_rows);
+        } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          xp_store_f32x16(st, lane, z, args.out32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
+          for (int h = 0; h < 2; ++h)
+            xp_store_f32x16(st, lane, z, args.out32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
+        }
         continue;
       }
       // ---- phase 1: t = o_proj + bias + residual (post-LN: LN1 of it).  t goes
@@ -785,9 +789,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = m < M && row_valid(m, S, lengths);
 #pragma unroll
         for (int i = 0; i < 32; ++i) tv[i] = valid ? tv[i] : 0.f;
+        if (args.outbf) {
+          xp_store_bf16<32>(st, lane, tv, args.outbf + (size_t)m0w * kD + c0, kD, in_rows);
+        } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          xp_store_f32x16(st, lane, tv + 16 * h, args.out32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
+          for (int h = 0; h < 2; ++h)
+            xp_store_f32x16(st, lane, tv + 16 * h, args.out32 + (size_t)m0w * kD + c0 + 16 * h, kD, in_rows);
+        }
       }
     }
   }

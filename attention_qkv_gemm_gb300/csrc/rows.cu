@@ -74,9 +74,20 @@ __global__ void __launch_bounds__(256) rows_kernel(const RowArgs a) {
   const RowOps& ro = a.row;
   const bool valid = row_valid(m, a.c.S, a.c.lengths);
   float4 t[V];
-  const float4* in = reinterpret_cast<const float4*>(a.in32 + (size_t)m * D);
+  if (a.inbf != nullptr) {  // bf16 model input: four values (8 bytes) per lane and chunk
+    const uint2* in = reinterpret_cast<const uint2*>(a.inbf + (size_t)m * D);
 #pragma unroll
-  for (int k = 0; k < V; ++k) t[k] = valid ? in[k * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < V; ++k) {
+      const uint2 w = valid ? in[k * 32 + lane] : make_uint2(0u, 0u);
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+      t[k] = make_float4(f0.x, f0.y, f1.x, f1.y);
+    }
+  } else {
+    const float4* in = reinterpret_cast<const float4*>(a.in32 + (size_t)m * D);
+#pragma unroll
+    for (int k = 0; k < V; ++k) t[k] = valid ? in[k * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (ro.flags & ROW_POST_LN) warp_ln<V>(t, ro.eps, ro.ga, ro.ba, lane, t);
   if (ro.flags & ROW_WRITE_H) {
     float4* hp = reinterpret_cast<float4*>(ro.h32 + (size_t)m * D);
@@ -86,9 +97,19 @@ __global__ void __launch_bounds__(256) rows_kernel(const RowArgs a) {
   if (ro.flags & ROW_FINAL) {
     float4 y[V];
     warp_ln<V>(t, ro.eps, ro.gf, ro.bf, lane, y);
-    float4* op = reinterpret_cast<float4*>(ro.out32 + (size_t)m * D);
+    if (ro.outbf != nullptr) {
+      uint2* op = reinterpret_cast<uint2*>(ro.outbf + (size_t)m * D);
 #pragma unroll
-    for (int k = 0; k < V; ++k) op[k * 32 + lane] = valid ? y[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < V; ++k) {
+        const float4 z = valid ? y[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(z.x, z.y), h1 = __floats2bfloat162_rn(z.z, z.w);
+        op[k * 32 + lane] = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+      }
+    } else {
+      float4* op = reinterpret_cast<float4*>(ro.out32 + (size_t)m * D);
+#pragma unroll
+      for (int k = 0; k < V; ++k) op[k * 32 + lane] = valid ? y[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   } else if (ro.flags & ROW_NORM16) {
     float4 y[V];
     warp_ln<V>(t, ro.eps, ro.gb, ro.bb, lane, y);

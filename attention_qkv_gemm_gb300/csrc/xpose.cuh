@@ -9,6 +9,7 @@
 // instead of 32 row fragments on 32 different lines.
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 namespace tfl {
@@ -89,6 +90,34 @@ __device__ __forceinline__ void pack_f16(const float* v, uint4* o, bool lo_part,
     }
     o[q] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+// N values (N multiple of 8) -> N/8 x 16 bytes of bf16, rounded to nearest even.
+template <int N>
+__device__ __forceinline__ void pack_bf16(const float* v, uint4* o) {
+#pragma unroll
+  for (int q = 0; q < N / 8; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * k], v[8 * q + 2 * k + 1]);
+      w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    o[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Store N bf16 columns (N = 32 or 64) of the warp's 32 rows through the stage.
+template <int N>
+__device__ __forceinline__ void xp_store_bf16(uint8_t* st, int lane, const float* v, __nv_bfloat16* row0,
+                                              size_t pitch_elems, uint32_t rows) {
+  using X = XStage<N * 2>;
+  uint4 h[N / 8];
+  pack_bf16<N>(v, h);
+  X::put_row(st, lane, h);
+  __syncwarp();
+  X::store_rows(st, lane, reinterpret_cast<uint8_t*>(row0), pitch_elems * 2, rows);
+  __syncwarp();
 }
 
 // Store N fp16 columns (N = 32 or 64; hi, and lo when given) of the warp's 32 rows through the stage.

@@ -137,6 +137,21 @@ int tfl_forward(tfl_handle* h, const float* x, const int32_t* lengths,
                 int causal, float* out, tfl_stream stream);
 
 /*
+ * The same forward with the model's inputs and outputs in bf16 (the model
+ * dtype of a bf16 checkpoint): x and out are device bf16 [B, S, d_model]
+ * (2 bytes per value, 16-byte aligned, not overlapping).  x is widened to fp32
+ * as it is read; the residual stream, LayerNorms, softmax and accumulation stay
+ * fp32 exactly as in tfl_forward; the final LayerNorm's output is rounded to
+ * bf16 (nearest even) as it is written, padded rows as +0.
+ * ("TikTok TechJam 2026 -- Problem 3", section 2.3, falls back to its baseline
+ * at bf16.)
+ * Graphs are cached per (causal, x, lengths, out) as for tfl_forward.
+ * Errors: INVALID_ARG, CUDA.  Device-side errors surface via tfl_status.
+ */
+int tfl_forward_bf16(tfl_handle* h, const void* x, const int32_t* lengths,
+                     int causal, void* out, tfl_stream stream);
+
+/*
  * The same forward from host buffers, synchronizing `stream` before it returns.
  * If x and out are pinned host memory the device can address (cudaHostAlloc /
  * cudaHostRegister, mapped), 16-byte aligned and not overlapping, the kernels

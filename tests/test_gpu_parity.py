@@ -93,3 +93,35 @@ def test_d128_residual_far_from_zero_mean(offset):
     assert rc == 0
     r = oracle.forward(prm, H, x, lens, True, 0)
     assert_gate(u, r, f"residual offset {offset}")
+
+
+@pytest.mark.parametrize("D,prec", [(128, 2), (256, 2), (128, 1)])
+def test_bf16_model_io(D, prec):
+    # bf16 in and out (fused chain; separate row kernel; GEMM row epilogue): the output
+    # must be the fp32 path's output on the same (widened) input, rounded once to bf16,
+    # and must meet the rule against the oracle run on that input.
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    B, S, H, F, L = 2, 200, 4, 512, 2
+    shape = synth.Shape(B, S, D, H, F, L, True)
+    prm = synth.params(6, shape, ln_affine="random")
+    xb = torch.from_numpy(synth.input_x(6, shape)).to(torch.bfloat16)
+    x_w = xb.float().numpy()
+    lens = np.array([200, 77], dtype=np.int32)
+    opts = pkg.tfl_default_options()
+    opts.precision = prec
+    m = pkg.TransformerStack(B, S, D, H, F, L, prm, options=opts)
+    try:
+        ld = torch.from_numpy(lens).cuda()
+        ob = m.forward(xb.cuda(), ld, causal=True, out=torch.full((B, S, D), float("nan"), dtype=torch.bfloat16,
+                                                                       device="cuda"))
+        of = m.forward(torch.from_numpy(x_w).cuda(), ld, causal=True)
+        assert m.status() == 0
+        u = ob.float().cpu().numpy()
+        np.testing.assert_array_equal(ob.cpu().view(torch.int16).numpy(), of.to(torch.bfloat16).cpu().view(torch.int16).numpy())
+    finally:
+        m.close()
+    for b in range(B):
+        assert np.all(u[b, lens[b]:] == 0.0)
+    r = oracle.forward(prm, H, x_w, lens, True, 0)
+    assert_gate(u, r, f"bf16 I/O D{D} precision {prec}")
