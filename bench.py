@@ -174,9 +174,9 @@ KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh"]
 
 NCU_TRAFFIC = {
     # (kernel, workload): (kernel source fingerprint, bytes per launch)
-    ("postchain", "B64_S1024_D128_causal_ragged"): ("6b5fd17c012f", 42.611200e6 + 25.210112e6),
-    ("attention", "B64_S1024_D128_causal_ragged"): ("cadac466a603", 41.431552e6 + 0.564992e6),
-    ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("f3319f953b69", 27.822080e6 + 0.816384e6),
+    ("postchain", "B64_S1024_D128_causal_ragged"): ("3de028492870", 42.636032e6 + 29.847296e6),
+    ("attention", "B64_S1024_D128_causal_ragged"): ("83300337c0a9", 41.431808e6 + 0.591872e6),
+    ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("33b68bcaadbf", 27.825920e6 + 0.646144e6),
 }
 
 
