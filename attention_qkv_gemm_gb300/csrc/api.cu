@@ -385,6 +385,10 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->hd));
       a.o16 = h->o16;
       a.counter = h->sched + l;
+      // work-order groups of (b, h) pairs whose keys and values (fp16) fit in 48 MB of L2
+      const double kv_pair = 4.0 * (double)h->shape.S * h->hd;
+      const double fit = 48.0 * 1024 * 1024 / kv_pair;
+      a.group = fit >= (double)h->shape.B * h->H ? 0 : (fit < 1.0 ? 1 : (int)fit);
       TFL_CUDA(launch_attention(h->hd, h->tm_q, h->tm_kv, a, h->num_sms, st), "attention");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_ATTENTION), "event");
     }

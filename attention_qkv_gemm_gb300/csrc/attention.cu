@@ -92,10 +92,22 @@ struct Item {
 
 constexpr int kItemRing = 4;
 
-// Work item i (heaviest first) -> (b, h, query block); false if the block is all padding.
+// Work item i -> (b, h, query block); false if the block is all padding.  The
+// (b, h) pairs are taken in groups of args.group; within a group the last (the
+// heaviest, under causal) query blocks of every pair come first, so each group,
+// and the launch, ends on light items.  One group (the default) is plain
+// heaviest-first.  Groups matter once the keys and values of all sequences no
+// longer fit in L2: the CTAs running at any moment then work on the few
+// sequences of one group and share their keys and values through L2, instead
+// of each streaming its own sequence's prefix from HBM once per query block.
 __device__ __forceinline__ bool decode_item(int i, const AttnArgs& a, int nqb, int bn, Item& it) {
   const int bh_count = a.B * a.H;
-  const int qr = i / bh_count, bh = i - qr * bh_count;
+  const int G = (a.group > 0 && a.group < bh_count) ? a.group : bh_count;
+  const int grp = i / (G * nqb);                 // every group before this one is full
+  const int gsize = min(G, bh_count - grp * G);  // pairs in this group
+  const int j = i - grp * G * nqb;
+  const int qr = j / gsize;
+  const int bh = grp * G + (j - qr * gsize);
   it.qb = nqb - 1 - qr;
   it.b = bh / a.H;
   it.h = bh - it.b * a.H;

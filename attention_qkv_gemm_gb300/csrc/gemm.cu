@@ -43,12 +43,14 @@ namespace tfl {
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
-template <int BN, int AS, int WS>
+template <int BN, int AS, int WS, int EPI>
 struct GemmCfg {
   static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;
   static constexpr int B_BYTES = BN * kGemmBK * 2;
   static constexpr int STAGE = A_BYTES * (1 + AS) + B_BYTES * (1 + WS);
-  static constexpr int RED_BYTES = 4 * 2 * kGemmBM * 4;     // row-statistics exchange (EPI_BIAS_RES_ROW)
+  // row-statistics exchange, only the row-LayerNorm epilogue has one (the space it
+  // frees elsewhere buys the split-operand rings a third stage)
+  static constexpr int RED_BYTES = EPI == EPI_BIAS_RES_ROW ? 4 * 2 * kGemmBM * 4 : 0;
   static constexpr int XPOSE_BYTES = kEpiWarps * 32 * 128;  // one 32 x 128 B transpose stage per epilogue warp
   static constexpr int RING_MAX = 232448 - 1024 - RED_BYTES - XPOSE_BYTES - 256;
   static constexpr int STAGES = RING_MAX / STAGE > 8 ? 8 : RING_MAX / STAGE;
@@ -90,7 +92,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAlo,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBlo,
                 const GemmArgs args) {
-  using C = GemmCfg<BN, AS, WS>;
+  using C = GemmCfg<BN, AS, WS, EPI>;
   extern __shared__ uint8_t smem_raw[];
   grid_launch_dependents();  // the next kernel may set itself up meanwhile
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -427,7 +429,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <int BN, int EPI, int AS, int WS>
 static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int num_sms, cudaStream_t s) {
-  using C = GemmCfg<BN, AS, WS>;
+  using C = GemmCfg<BN, AS, WS, EPI>;
   const int tiles = ((a.c.M + kGemmBM - 1) / kGemmBM) * (a.N / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
@@ -438,7 +440,7 @@ static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int num_sms
 template <int BN, int EPI, int AS, int WS>
 static cudaError_t prepare_one() {
   return cudaFuncSetAttribute(gemm_kernel<BN, EPI, AS, WS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)GemmCfg<BN, AS, WS>::SMEM);
+                              (int)GemmCfg<BN, AS, WS, EPI>::SMEM);
 }
 
 // Every (BN, EPI) pair the planner uses, at the three operand modes (AS, WS) = (0,0), (0,1), (1,1).

@@ -79,6 +79,7 @@ struct AttnArgs {
   float scale_log2 = 0.f;        // log2(e) / sqrt(head_dim)
   __half* o16 = nullptr;         // [M, D]
   int* counter = nullptr;        // work-item counter, zero before the launch
+  int group = 0;                 // (b, h) pairs per work-order group (see decode_item); 0: one group
 };
 
 struct RowArgs {

@@ -66,10 +66,11 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path: str = ""):
+        import tempfile
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"tfl_clocks_gpu{gpu_index}.csv")
 
     def start(self):
         try:
@@ -113,6 +114,16 @@ def workload(idx: int) -> synth.Shape:
     return synth.WORKLOADS[idx]
 
 
+def custom_shape(spec: str) -> synth.Shape:
+    """'B,S,D,H,F,L,causal[,len_lo,len_hi]' -> a Shape (for small profiling cases)."""
+    f = [int(v) for v in spec.split(",")]
+    if len(f) not in (7, 9):
+        raise SystemExit("--shape wants B,S,D,H,F,L,causal[,len_lo,len_hi]")
+    lo, hi = (f[7], f[8]) if len(f) == 9 else (None, None)
+    name = f"B{f[0]}_S{f[1]}_D{f[2]}_H{f[3]}_F{f[4]}_L{f[5]}_" + ("causal" if f[6] else "keymask")
+    return synth.Shape(f[0], f[1], f[2], f[3], f[4], f[5], bool(f[6]), lo, hi, name=name)
+
+
 def algorithmic(shape: synth.Shape, lens: np.ndarray, causal: bool):
     """Per-forward algorithmic FLOPs and per-kernel units (valid rows, allowed pairs only)."""
     D, F, H, L = shape.d_model, shape.d_ff, shape.n_heads, shape.n_layers
@@ -124,6 +135,13 @@ def algorithmic(shape: synth.Shape, lens: np.ndarray, causal: bool):
     att = 4.0 * pairs * hd * H * L
     return {"valid_tokens": valid, "pairs": pairs, "linear_flops": lin, "attn_flops": att,
             "attn_exps_per_launch": pairs * H, "attn_flops_per_launch": 4.0 * pairs * hd * H}
+
+
+def gemm_flops(kind: str, shape: synth.Shape, valid: float):
+    """Algorithmic FLOPs of one launch of a projection GEMM (valid rows only)."""
+    D, F = shape.d_model, shape.d_ff
+    nk = {"gemm_qkv": (3 * D, D), "gemm_oproj": (D, D), "gemm_ffn1": (F, D), "gemm_ffn2": (D, F)}.get(kind)
+    return None if nk is None else 2.0 * valid * nk[0] * nk[1]
 
 
 def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
@@ -169,6 +187,9 @@ KERNEL_SOURCES = {
     "postchain": ["postchain.cu"],
     "attention": ["attention.cu"],
     "gemm_qkv": ["gemm.cu"],
+    "gemm_oproj": ["gemm.cu"],
+    "gemm_ffn1": ["gemm.cu"],
+    "gemm_ffn2": ["gemm.cu"],
 }
 KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh"]
 
@@ -200,15 +221,39 @@ def ncu_traffic(kernel: str, workload: str):
     return nbytes if csrc_fingerprint(kernel) == sha else None
 
 
+# Sequences longer than this are sampled by query rows for the oracle timing (one
+# causal layer: a row depends only on the keys before it, so a row sample is exact)
+ORACLE_FULL_S = 8192
+ORACLE_ROWS = 64
+
+
+def oracle_rows(shape):
+    if shape.S <= ORACLE_FULL_S or not (shape.causal and shape.n_layers == 1):
+        return None
+    rng = np.random.default_rng(12345)
+    return np.unique(np.concatenate([[0, shape.S - 1], rng.choice(shape.S, ORACLE_ROWS - 2, replace=False)]))
+
+
 def run_oracle_sample(shape, prm, seed, n_seq):
+    """Time the fp64 oracle on n_seq sequences (or on a row sample of them); returns
+    (seconds, output rows computed)."""
     import oracle
     lens = synth.lengths(seed, shape)
     batches = np.arange(n_seq)
     x = synth.input_x(seed, shape, batches=batches)
+    rows = oracle_rows(shape)
     t0 = time.perf_counter()
-    oracle.forward(prm, shape.n_heads, x, lens[batches], shape.causal)
+    oracle.forward(prm, shape.n_heads, x, lens[batches], shape.causal, rows=rows)
     dt = time.perf_counter() - t0
-    return dt, n_seq * shape.S
+    return dt, n_seq * (shape.S if rows is None else len(rows))
+
+
+def oracle_sample_text(shape, n_seq, tok):
+    rows = oracle_rows(shape)
+    if rows is None:
+        return f"{n_seq} of {shape.B} sequences ({tok} tokens), fp64 numpy"
+    return (f"{n_seq} of {shape.B} sequences x {len(rows)} sampled query rows ({tok} output rows; keys and values "
+            f"projected for every position up to the last sampled row), fp64 numpy")
 
 
 def reference_arm(args, shape, world, rank):
@@ -216,15 +261,16 @@ def reference_arm(args, shape, world, rank):
     if rank != 0:
         return 0
     prm = synth.params(0, shape)
-    n_seq = max(1, min(shape.B, args.ref_seqs))
+    n_seq = max(1, min(shape.B, args.ref_seqs if oracle_rows(shape) is None else 1))
     for _ in range(max(0, min(args.warmup, 1))):
         run_oracle_sample(shape, prm, 0, 1)
     times = []
+    tok = 0
     for _ in range(args.steps):
         dt, tok = run_oracle_sample(shape, prm, 0, n_seq)
         times.append(dt)
     ms = 1e3 * statistics.mean(times)
-    value = (n_seq * shape.S) / (ms / 1e3)
+    value = tok / (ms / 1e3)
     cores = os.cpu_count()
     line = {
         "impl": "reference", "metric": "forward_tokens_per_s", "value": value, "unit": "tokens/s",
@@ -232,7 +278,7 @@ def reference_arm(args, shape, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(shape),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n_seq} of {shape.B} sequences ({n_seq * shape.S} tokens) per step"},
+                         "sample": oracle_sample_text(shape, n_seq, tok) + " per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -253,13 +299,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=1, help="index into the workload table (default: B64 S1024)")
+    ap.add_argument("--shape", default="", help="B,S,D,H,F,L,causal[,len_lo,len_hi]: a custom (profiling) shape")
+    ap.add_argument("--clocks-csv", default="", help="where to keep the nvidia-smi clock samples")
     ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference/oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
     world, rank, local = dist_env()
-    shape = workload(args.workload)
+    shape = custom_shape(args.shape) if args.shape else workload(args.workload)
     if args.impl == "reference":
         return reference_arm(args, shape, world, rank)
 
@@ -302,7 +350,7 @@ def main():
         raise RuntimeError(f"device status {rc}: {pkg.tfl_last_error()}")
 
     # ---------------- timed region: graph replays, L2 flushed between steps
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, args.clocks_csv)
     sampler.start()
     time.sleep(0.3)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -341,22 +389,42 @@ def main():
     dom_ms_launch = per_kind[dom][0] / per_kind[dom][1]
     alg = algorithmic(shape, lens_np, shape.causal)
     peaks = load_peaks()
+    # a launch longer than this runs under the power cap: the sustained tensor peak applies
+    tc_peak = peaks["tc_tflops_sustained"] if dom_ms_launch > 50.0 else peaks["tc_tflops"]
     if dom == "attention":
         exps = alg["attn_exps_per_launch"]
-        achieved = exps / (dom_ms_launch / 1e3) / 1e9
-        peak = MUFU_PER_CLK_PER_SM * 152 * peaks["sm_max_mhz"] * 1e6 / 1e9
-        roof = {"kernel": "attention", "bound": "alu", "achieved": achieved, "peak": peak, "unit": "Gexp2/s",
-                "frac": achieved / peak, "traffic": ncu_traffic("attention", shape.name),
-                "note": "MUFU ex2 rate: 32/clk/SM (measured) x 152 SMs x max SM clock; per launch = allowed "
-                        "(query, key) pairs x heads",
-                "tensor_tflops": alg["attn_flops_per_launch"] / (dom_ms_launch / 1e3) / 1e12}
+        fl = alg["attn_flops_per_launch"]
+        mufu_peak = MUFU_PER_CLK_PER_SM * 152 * peaks["sm_max_mhz"] * 1e6 / 1e9
+        mufu = exps / (dom_ms_launch / 1e3) / 1e9
+        tflops = fl / (dom_ms_launch / 1e3) / 1e12
+        # the unit that bounds the launch at peak: one exp2 per allowed (query, key) pair and
+        # head against 4 * head_dim tensor FLOPs for the same pair (QK^T and P V)
+        if exps / (mufu_peak * 1e9) >= fl / (tc_peak * 1e12):
+            roof = {"kernel": "attention", "bound": "alu", "achieved": mufu, "peak": mufu_peak, "unit": "Gexp2/s",
+                    "frac": mufu / mufu_peak, "tensor_tflops": tflops}
+        else:
+            roof = {"kernel": "attention", "bound": "tensor", "achieved": tflops, "peak": tc_peak,
+                    "unit": "TFLOP/s", "frac": tflops / tc_peak, "mufu_gexp2_s": mufu, "mufu_frac": mufu / mufu_peak}
+        roof["traffic"] = ncu_traffic("attention", shape.name)
+        roof["note"] = ("MUFU ex2 rate: 32/clk/SM (measured) x 152 SMs x max SM clock; per launch = allowed "
+                        "(query, key) pairs x heads; tensor = 4 x head_dim FLOPs per allowed pair and head")
+    elif shape.d_model > 128 and gemm_flops(dom, shape, alg["valid_tokens"]) is not None:
+        # d_model > 128: the projection GEMMs are dense contractions (fp16 operands, fp32
+        # accumulate), measured against the dense tensor peak (fp16 = bf16 nominal rate)
+        fl = gemm_flops(dom, shape, alg["valid_tokens"])
+        achieved = fl / (dom_ms_launch / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": ncu_traffic(dom, shape.name),
+                "algorithmic_flops_per_launch": fl,
+                "note": "split-fp16 operands execute 3 MMAs per 16-wide k-step (2 for o_proj); achieved counts "
+                        "the algorithmic 2*M*N*K only"}
     else:
         by = kernel_bytes(dom, shape, alg["valid_tokens"])
         achieved = by / (dom_ms_launch / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom, shape.name),
                 "algorithmic_bytes_per_launch": by}
-    roof["peak_source"] = peaks["source"]
+    roof["peak_source"] = peaks["source"] + (" (sustained)" if roof["unit"] == "TFLOP/s" and tc_peak != peaks["tc_tflops"] else "")
     roof["launch_ms"] = dom_ms_launch
     roof["kernels_ms_per_forward"] = {k: round(v[0], 4) for k, v in per_kind.items()}
 
@@ -400,9 +468,10 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        dt, tok = run_oracle_sample(shape, prm, seed, min(shape.B, args.ref_seqs))
+        n_seq = min(shape.B, args.ref_seqs if oracle_rows(shape) is None else 1)
+        dt, tok = run_oracle_sample(shape, prm, seed, n_seq)
         cpu = {"value": tok / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{min(shape.B, args.ref_seqs)} of {shape.B} sequences ({tok} tokens), fp64 numpy"}
+               "sample": oracle_sample_text(shape, n_seq, tok)}
 
     line = {
         "metric": "forward_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

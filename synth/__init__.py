@@ -129,8 +129,8 @@ class Shape:
         return self.B * self.S
 
 
-# The five benchmark shapes (TechJam 2026 problem 3 matrix as restated for
-# this build).  Index 0 is the small latency-bound case.
+# The five benchmark shapes (the TechJam 2026 problem 3 shape matrix).
+# Index 0 is the small latency-bound case.
 WORKLOADS: List[Shape] = [
     Shape(1, 128, 128, 4, 512, 4, True, name="B1_S128_D128_causal"),
     Shape(64, 1024, 128, 4, 512, 4, True, 512, 1024, name="B64_S1024_D128_causal_ragged"),
