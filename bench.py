@@ -195,9 +195,16 @@ KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh"]
 
 NCU_TRAFFIC = {
     # (kernel, workload): (kernel source fingerprint, bytes per launch)
-    ("postchain", "B64_S1024_D128_causal_ragged"): ("3de028492870", 42.636032e6 + 29.847296e6),
-    ("attention", "B64_S1024_D128_causal_ragged"): ("83300337c0a9", 41.431808e6 + 0.591872e6),
-    ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("33b68bcaadbf", 27.825920e6 + 0.646144e6),
+    ("postchain", "B64_S1024_D128_causal_ragged"): ("f6e63fb10f67", 42.612736e6 + 29.804032e6),
+    ("attention", "B64_S1024_D128_causal_ragged"): ("222a4a4c89a8", 41.433088e6 + 0.554752e6),
+    ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("f2139ce26c7e", 27.822592e6 + 0.657664e6),
+    ("gemm_qkv", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 46.189568e6 + 12.694784e6),
+    ("gemm_oproj", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 54.557184e6 + 2.611456e6),
+    ("gemm_ffn1", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 50.419968e6 + 83.465728e6),
+    ("gemm_ffn2", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 186.352896e6 + 19.356416e6),
+    ("attention", "B16_S512_D1024_H4_causal"): ("222a4a4c89a8", 50.391808e6 + 0.699392e6),
+    # full-size launch, DRAM counters only (one ncu pass)
+    ("attention", "B32_S100000_D1024_H16_causal"): ("222a4a4c89a8", 24.62e9 + 6.56e9),
 }
 
 

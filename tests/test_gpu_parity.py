@@ -125,3 +125,29 @@ def test_bf16_model_io(D, prec):
         assert np.all(u[b, lens[b]:] == 0.0)
     r = oracle.forward(prm, H, x_w, lens, True, 0)
     assert_gate(u, r, f"bf16 I/O D{D} precision {prec}")
+
+
+def test_d1024_hd64_long_sequences_grouped_work_order():
+    # Long sequences: the keys and values of all (b, h) pairs (32 pairs x 1.6 MB) exceed the
+    # attention kernel's L2 budget, so its work items are taken in groups of (b, h) pairs
+    # (here 30, then a ragged group of 2).  One causal layer: a sampled output row depends only
+    # on the keys before it, so the oracle computes the sampled rows exactly.
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    B, S, D, H, F, L = 2, 6144, 1024, 16, 1024, 1
+    shape = synth.Shape(B, S, D, H, F, L, True)
+    prm = synth.params(11, shape, ln_affine="random")
+    x = synth.input_x(11, shape)
+    lens = np.array([S, 4000], dtype=np.int32)
+    m = pkg.TransformerStack(B, S, D, H, F, L, prm)
+    try:
+        out = m.forward(torch.from_numpy(x).cuda(), torch.from_numpy(lens).cuda(), causal=True)
+        assert m.status() == 0, pkg.tfl_last_error()
+        u_all = out.cpu().numpy()
+    finally:
+        m.close()
+    assert np.all(u_all[1, lens[1]:] == 0.0)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 127, 128, 3999, 4000, S - 1], rng.choice(S, 122, replace=False)]))
+    r = oracle.forward(prm, H, x, lens, True, rows=rows)
+    assert_gate(u_all[:, rows], r, "B2 S6144 D1024 H16 grouped attention order")
