@@ -47,6 +47,29 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, pg, device) -> float:
+    """The largest of every rank's x (the job is as slow as its slowest rank); x itself
+    without a process group.  device: where the reduction tensor lives (cuda for NCCL,
+    cpu for gloo)."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(rank: int) -> int:
+    """Seed of the batch a rank runs: every rank an independent replica with its own
+    batch (sequences are independent, so ranks exchange nothing on the data path)."""
+    return rank
+
+
+def job_value(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -334,7 +357,7 @@ def main():
         libbuild.build()
     pkg.load()
 
-    seed = rank  # each replica its own batch
+    seed = replica_seed(rank)
     prm = synth.params(seed, shape)
     lens_np = synth.lengths(seed, shape)
     x_np = synth.input_x(seed, shape)
@@ -377,13 +400,9 @@ def main():
     rc = m.status(sp)
     if rc != 0:
         raise RuntimeError(f"device status {rc}: {pkg.tfl_last_error()}")
-    ms = float(statistics.mean(step_ms))
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), pg, dev)
     tokens = shape.B * shape.S
-    value = world * tokens / (ms / 1e3)
+    value = job_value(world, tokens, ms / 1e3)
 
     # ---------------- per-kernel times (eager, events around every launch)
     prof = {}
@@ -448,12 +467,8 @@ def main():
         e2e_t.append(time.perf_counter() - t0)
         if rc2 != 0:
             raise RuntimeError(f"e2e status {rc2}")
-    e2e_s = statistics.mean(e2e_t)
-    if pg:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(hx.numel() * 4 + hl.numel() * 4),
+    e2e_s = max_over_ranks(statistics.mean(e2e_t), pg, dev)
+    e2e = {"value": job_value(world, tokens, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": int(hx.numel() * 4 + hl.numel() * 4),
            "d2h_bytes_per_step": int(ho.numel() * 4)}
 
     launches = pkg.tfl_launch_count(m.handle, int(shape.causal)) * args.steps
@@ -487,7 +502,7 @@ def main():
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "algorithmic": {"valid_tokens": alg["valid_tokens"], "gflop": (alg["linear_flops"] + alg["attn_flops"]) / 1e9,
                         "tflops_achieved": (alg["linear_flops"] + alg["attn_flops"]) / (ms / 1e3) / 1e12,
-                        "valid_tokens_per_s": alg["valid_tokens"] * world / (ms / 1e3)},
+                        "valid_tokens_per_s": job_value(world, alg["valid_tokens"], ms / 1e3)},
         "forward_roofline": fwd_roof,
     }
     print(json.dumps(line), flush=True)
