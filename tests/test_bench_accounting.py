@@ -1,0 +1,81 @@
+"""bench.py's accounting, checked against closed forms (CPU).
+
+Algorithmic FLOPs per forward count only the work the method must do: the four
+projections on valid rows (2 * rows * (3D*D + D*D + 2*D*F) per layer) and, for
+attention, 4 * head_dim FLOPs (QK^T and P V) per allowed (query, key) pair and
+head.  With full lengths and a causal mask a sequence of S tokens has
+S (S + 1) / 2 allowed pairs.
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+
+def _full(shape):
+    return np.full(shape.B, shape.S, dtype=np.int32)
+
+
+@pytest.mark.parametrize("idx", [0, 3, 4])
+def test_algorithmic_flops_full_lengths_closed_form(idx):
+    shape = synth.WORKLOADS[idx]
+    B, S, D, H, F, L = shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers
+    a = bench.algorithmic(shape, _full(shape), True)
+    lin = 2.0 * B * S * (4 * D * D + 2 * D * F) * L
+    att = 4.0 * (D // H) * H * B * S * (S + 1) / 2 * L
+    assert a["valid_tokens"] == B * S
+    assert a["linear_flops"] == pytest.approx(lin, rel=1e-12)
+    assert a["attn_flops"] == pytest.approx(att, rel=1e-12)
+    assert a["attn_exps_per_launch"] == pytest.approx(H * B * S * (S + 1) / 2, rel=1e-12)
+
+
+def test_algorithmic_flops_match_the_workload_table():
+    # totals per forward, GFLOP: B16 S512 D1024 ~ 859, B32 S100000 D1024 ~ 735 900, B1 S128 ~ 0.218
+    got = {i: (lambda s: sum(bench.algorithmic(s, _full(s), True)[k] for k in ("linear_flops", "attn_flops")))(
+        synth.WORKLOADS[i]) / 1e9 for i in (0, 3, 4)}
+    assert got[0] == pytest.approx(0.218, rel=0.01)
+    assert got[3] == pytest.approx(859.1, rel=0.001)
+    assert got[4] == pytest.approx(735_900, rel=0.001)
+
+
+def test_key_padding_counts_only_valid_pairs():
+    shape = synth.Shape(2, 128, 128, 4, 512, 1, False, 32, 128)
+    lens = np.array([100, 7], dtype=np.int32)
+    a = bench.algorithmic(shape, lens, False)
+    assert a["valid_tokens"] == 107
+    assert a["pairs"] == 100 * 100 + 7 * 7
+
+
+def test_gemm_flops_per_launch():
+    shape = synth.WORKLOADS[3]
+    assert bench.gemm_flops("gemm_ffn2", shape, 8192) == 2.0 * 8192 * 1024 * 4096
+    assert bench.gemm_flops("gemm_qkv", shape, 8192) == 2.0 * 8192 * 3072 * 1024
+    assert bench.gemm_flops("attention", shape, 8192) is None
+
+
+def test_chain_bytes_per_valid_token():
+    # fused chain at d_model 128, averaged over a forward's four launches:
+    # (3 x (256 + 512 + 512 + 768) + (256 + 512 + 512)) / 4 = 1856 bytes per valid token
+    shape = synth.WORKLOADS[1]
+    assert bench.kernel_bytes("postchain", shape, 1.0) == pytest.approx(1856.0)
+
+
+def test_custom_shape_and_row_sample():
+    s = bench.custom_shape("2,16384,1024,16,4096,1,1")
+    assert (s.B, s.S, s.d_model, s.n_heads, s.d_ff, s.n_layers, s.causal) == (2, 16384, 1024, 16, 4096, 1, True)
+    s2 = bench.custom_shape("4,200,128,4,512,2,0,32,200")
+    assert (s2.causal, s2.len_lo, s2.len_hi) == (False, 32, 200)
+    with pytest.raises(SystemExit):
+        bench.custom_shape("1,2,3")
+    rows = bench.oracle_rows(synth.WORKLOADS[4])
+    assert rows is not None and len(rows) == bench.ORACLE_ROWS
+    assert rows[0] == 0 and rows[-1] == synth.WORKLOADS[4].S - 1 and np.all(np.diff(rows) > 0)
+    assert bench.oracle_rows(synth.WORKLOADS[1]) is None  # short sequences: whole sequences
