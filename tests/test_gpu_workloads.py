@@ -10,7 +10,8 @@ checks, element by element with the graded rule:
     padded row of the whole batch is exactly zero;
   * B=32 S=100000 (one layer): 2 sequences x 64 query rows per seed, always
     including rows 0 and S-1 (exact: with one causal layer a row depends
-    only on the keys before it).
+    only on the keys before it); seeds 0..2 by default (about 20 s each),
+    more with --s100k-seeds N.
 Seeds drive both weights and inputs.  The worst ratio |u-r| / max(2e-3,
 0.02|r|) over all seeds is printed for the record.
 """
@@ -101,12 +102,13 @@ def test_workload_b16_s512_d1024():
     _check_sequences(3, 1)
 
 
-def test_workload_b32_s100000_sampled_rows():
+def test_workload_b32_s100000_sampled_rows(request):
     import torch
     import attention_qkv_gemm_gb300 as pkg
     shape = synth.WORKLOADS[4]
+    n_seeds = request.config.getoption("--s100k-seeds")
     worst = 0.0
-    for seed in range(3):
+    for seed in range(n_seeds):
         prm = synth.params(seed, shape)
         lens = synth.lengths(seed, shape)
         x = synth.input_x(seed, shape)
@@ -126,4 +128,4 @@ def test_workload_b32_s100000_sampled_rows():
         r = oracle.forward(prm, shape.n_heads, x[bsel], lens[bsel], True, rows=rows)
         assert oracle.gate(u, r).all(), f"seed {seed}: {gate_report(u, r)}"
         worst = max(worst, _ratio(u, r))
-    print(f"\n{shape.name}: worst |u-r|/budget over 3 seeds (sampled rows) = {worst:.3f}")
+    print(f"\n{shape.name}: worst |u-r|/budget over {n_seeds} seeds (sampled rows) = {worst:.3f}")
