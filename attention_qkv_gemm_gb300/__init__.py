@@ -29,7 +29,8 @@ TFL_ERR_BAD_LENGTHS = -6
 KIND_NAMES = {1: "rownorm", 2: "gemm_qkv", 3: "attention", 4: "gemm_oproj", 5: "gemm_ffn1", 6: "gemm_ffn2",
               7: "postchain"}
 
-EXPORTS = ("tfl_default_options", "tfl_workspace_bytes", "tfl_create", "tfl_forward", "tfl_forward_host",
+EXPORTS = ("tfl_default_options", "tfl_workspace_bytes", "tfl_create", "tfl_forward", "tfl_forward_bf16",
+           "tfl_forward_host",
            "tfl_status", "tfl_destroy", "tfl_last_error", "tfl_profile_forward", "tfl_launch_count",
            "tfl_probe_wait_timeout", "tfl_forward_noalloc", "tfl_selftest_gelu")
 

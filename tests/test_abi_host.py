@@ -24,12 +24,13 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "tfl.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tfl_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(tfl_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("tfl_create", "tfl_forward", "tfl_destroy", "tfl_status", "tfl_last_error"):
+    for n in ("tfl_create", "tfl_forward", "tfl_destroy", "tfl_status", "tfl_last_error", "tfl_forward_bf16",
+              "tfl_forward_host", "tfl_forward_noalloc"):
         assert n in names
     assert set(pkg.EXPORTS) == set(names)
 
