@@ -1,7 +1,7 @@
 """The ctypes binding's structs have the C header's layout (CPU; gcc).
 
-A small C program compiled against include/tfl.h prints sizeof and offsetof
-of every struct and field; the binding's ctypes structures must agree, or
+A small C program compiled against include/tfl.h prints sizeof of every struct
+and the offset and size of every field; the binding's ctypes structures must agree, or
 every call through them would hand the library misplaced arguments.
 """
 import os
@@ -32,6 +32,7 @@ def _c_layout():
         lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
         for f, _ in cls._fields_:
             lines.append(f'  printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+            lines.append(f'  printf("{cname} {f}.size %zu\\n", sizeof((({cname}*)0)->{f}));')
     lines += ["  return 0;", "}"]
     with tempfile.TemporaryDirectory() as d:
         src, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
@@ -52,7 +53,8 @@ def test_struct_sizes_and_offsets_match_the_header():
     for cname, cls in STRUCTS.items():
         assert c[(cname, "size")] == ctypes_sizeof(cls), cname
         for f, _ in cls._fields_:
-            assert c[(cname, f)] == getattr(cls, f).offset, f"{cname}.{f}"
+            assert c[(cname, f)] == getattr(cls, f).offset, f"{cname}.{f} offset"
+            assert c[(cname, f + ".size")] == getattr(cls, f).size, f"{cname}.{f} size"
 
 
 def ctypes_sizeof(cls):
