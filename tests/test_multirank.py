@@ -64,3 +64,21 @@ def test_job_value_counts_every_rank_over_the_slowest_time():
     assert bench.job_value(2, 65536, 0.5) == pytest.approx(262144.0)
     assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
     assert bench.replica_seed(0) != bench.replica_seed(1)
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    import json
+    import subprocess
+    import sys
+    base = dict(os.environ, MASTER_ADDR="127.0.0.1", WORLD_SIZE="2")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "0", "--workload", "0"]
+    r1 = subprocess.run(cmd, env=dict(base, RANK="1", LOCAL_RANK="1"), capture_output=True, text=True, timeout=300)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    r0 = subprocess.run(cmd, env=dict(base, RANK="0", LOCAL_RANK="0"), capture_output=True, text=True, timeout=300)
+    assert r0.returncode == 0
+    lines = [l for l in r0.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
