@@ -175,6 +175,130 @@ def forward(params, n_heads: int, x: np.ndarray, lengths: Optional[np.ndarray], 
     return np.stack(outs)
 
 
+def attention_batched(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int,
+                      lengths: np.ndarray, causal: bool) -> np.ndarray:
+    """``attention`` for a batch of sequences at once: q, k, v [nb, S, D], lengths [nb].
+
+    The same five steps of "TikTok TechJam 2026 -- Problem 3", section 2.1
+    (scores, 1/sqrt(d_k) scale, mask, row softmax over keys, weighted values),
+    applied to every sequence and head together; sequence b allows key j for
+    query i iff j < lengths[b] (and j <= i when causal).  A query with no
+    allowed key gets a zero output.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    nb, S, D = q.shape
+    hd = D // n_heads
+    j = np.arange(S)
+    allowed = np.broadcast_to((j[None, :] < np.asarray(lengths)[:, None])[:, None, :], (nb, S, S))
+    if causal:
+        allowed = allowed & (j[None, :] <= j[:, None])[None]
+    allowed = allowed[:, None]                                          # [nb, 1, S, S]
+    any_allowed = allowed.any(axis=-1, keepdims=True)
+    heads = lambda t: t.reshape(nb, S, n_heads, hd).transpose(0, 2, 1, 3)  # [nb, H, S, hd]
+    qh, kh, vh = heads(q), heads(k), heads(v)
+    s = qh @ kh.transpose(0, 1, 3, 2)                                   # (1) scores
+    s = s / np.sqrt(hd)                                                 # (2) scale
+    s = np.where(allowed, s, -np.inf)                                   # (3) mask
+    m = np.max(s, axis=-1, keepdims=True)                               # (4) softmax over keys
+    m = np.where(np.isfinite(m), m, 0.0)
+    e = np.where(allowed, np.exp(s - m), 0.0)
+    den = e.sum(axis=-1, keepdims=True)
+    p = np.where(any_allowed, e / np.where(den > 0, den, 1.0), 0.0)
+    o = p @ vh                                                          # (5) weighted values
+    return o.transpose(0, 2, 1, 3).reshape(nb, S, D)
+
+
+def _chunk_forward(params, n_heads: int, xs: np.ndarray, lens: np.ndarray, causal: bool,
+                   norm_placement: int, eps: float) -> np.ndarray:
+    """``sequence_forward`` for a chunk of sequences [nb, S, D] with lengths [nb]."""
+    nb, S, D = xs.shape
+    # tokens of all sequences as the rows of one matrix for the linear layers
+    h = np.asarray(xs, dtype=np.float64).reshape(nb * S, D)
+    seq = lambda t: t.reshape(nb, S, -1)
+    for P in params.layers:
+        a = layer_norm(h, P.ln1_g, P.ln1_b, eps) if norm_placement == 0 else h
+        q = a @ P.wq.astype(np.float64).T + P.bq
+        k = a @ P.wk.astype(np.float64).T + P.bk
+        v = a @ P.wv.astype(np.float64).T + P.bv
+        o = attention_batched(seq(q), seq(k), seq(v), n_heads, lens, causal).reshape(nb * S, D)
+        t = h + o @ P.wo.astype(np.float64).T + P.bo
+        if norm_placement == 1:
+            t = layer_norm(t, P.ln1_g, P.ln1_b, eps)
+            a2 = t
+        else:
+            a2 = layer_norm(t, P.ln2_g, P.ln2_b, eps)
+        f = gelu(a2 @ P.w1.astype(np.float64).T + P.b1) @ P.w2.astype(np.float64).T + P.b2
+        h = t + f
+        if norm_placement == 1:
+            h = layer_norm(h, P.ln2_g, P.ln2_b, eps)
+    y = seq(layer_norm(h, params.lnf_g, params.lnf_b, eps))
+    y[np.arange(S)[None, :] >= np.asarray(lens)[:, None]] = 0.0
+    return y
+
+
+def _chunk_task(args):
+    return _chunk_forward(*args)
+
+
+_POOL = None
+
+
+def _process_pool():
+    """A pool of one worker process per core, started with ``spawn`` and kept for
+    the life of the process.  Each worker runs single-threaded BLAS: many small
+    array operations in parallel processes beat threads that contend for one
+    multi-threaded BLAS."""
+    global _POOL
+    if _POOL is None:
+        import atexit
+        import multiprocessing as mp
+        keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in keys}
+        for k in keys:
+            os.environ[k] = "1"
+        try:
+            _POOL = mp.get_context("spawn").Pool(max(1, os.cpu_count() or 1))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        atexit.register(_POOL.terminate)
+    return _POOL
+
+
+def forward_batched(params, n_heads: int, x: np.ndarray, lengths: Optional[np.ndarray], causal: bool,
+                    norm_placement: int = 0, eps: float = 1e-5, chunk: int = 0,
+                    processes: bool = False) -> np.ndarray:
+    """The whole forward of ``forward`` (same layer order, masks and tail), with the
+    sequences taken ``chunk`` at a time through batched array operations instead of
+    one at a time.  Sequences are independent, so this is the same definition
+    evaluated for many sequences per array operation.
+
+    With ``processes`` the chunks are spread over a pool of worker processes
+    (see ``_process_pool``); otherwise they run one after another in this process.
+
+    x: float32 [nb, S, D]; lengths: int [nb] or None.  Returns float64 [nb, S, D].
+    """
+    x = np.asarray(x)
+    nb, S, D = x.shape
+    lens = np.full(nb, S, dtype=np.int64) if lengths is None else np.asarray(lengths, dtype=np.int64)
+    if chunk <= 0:
+        # about 64 MB of fp64 scores per chunk
+        chunk = max(1, min(nb, (64 << 20) // (8 * n_heads * S * S)))
+    starts = list(range(0, nb, chunk))
+    tasks = [(params, n_heads, x[s0:s0 + chunk], lens[s0:s0 + chunk], causal, norm_placement, eps)
+             for s0 in starts]
+    if processes and len(tasks) > 1:
+        parts = _process_pool().map(_chunk_task, tasks)
+    else:
+        parts = [_chunk_task(t) for t in tasks]
+    return np.concatenate(parts, axis=0)
+
+
 def gate(u: np.ndarray, r: np.ndarray) -> np.ndarray:
     """Elementwise acceptance: |u - r| <= 2e-3 or |u - r| <= 0.02 |r|.
 

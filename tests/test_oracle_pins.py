@@ -178,14 +178,24 @@ def _torch_forward(prm, shape, x, lens, causal, norm_first):
         return fn(h).numpy()
 
 
+def _batched_pool(prm, H, x, lens, causal, norm_placement=0):
+    return oracle.forward_batched(prm, H, x, lens, causal, norm_placement, chunk=1, processes=True)
+
+
+def _batched_inproc(prm, H, x, lens, causal, norm_placement=0):
+    return oracle.forward_batched(prm, H, x, lens, causal, norm_placement, chunk=2)
+
+
+@pytest.mark.parametrize("fwd", [oracle.forward, _batched_inproc, _batched_pool],
+                         ids=["per_sequence", "batched", "batched_processes"])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("norm_placement", [0, 1])
-def test_forward_matches_torch_transformer_encoder(causal, norm_placement):
+def test_forward_matches_torch_transformer_encoder(causal, norm_placement, fwd):
     shape = tiny_shape(B=3, S=8, D=16, H=2, F_=32, L=2, causal=causal)
     prm = synth.params(11, shape, ln_affine="random", bias_std=0.3)
     x = synth.input_x(11, shape)
     lens = np.array([8, 5, 1], dtype=np.int32)
-    ours = oracle.forward(prm, shape.n_heads, x, lens, causal, norm_placement)
+    ours = fwd(prm, shape.n_heads, x, lens, causal, norm_placement)
     ref = _torch_forward(prm, shape, x, lens, causal, norm_first=(norm_placement == 0))
     for b in range(shape.B):
         np.testing.assert_allclose(ours[b, :lens[b]], ref[b, :lens[b]], atol=1e-11)
@@ -365,3 +375,64 @@ def test_dropped_bias_is_caught():
         getattr(P.layers[0], f)[:] = 0
         ours = oracle.forward(P, 2, x, None, True)
         assert np.max(np.abs(ours - ref)) > 1e-6, f
+
+
+# --------------------------------------------------------------------------
+# The batched attention against the library routine and planted mistakes
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_batched_matches_torch_sdpa(causal):
+    r = rng(21)
+    nb, S, D, H = 3, 9, 24, 3
+    q, k, v = (r.normal(size=(nb, S, D)) for _ in range(3))
+    lens = np.array([9, 4, 1])
+    ours = oracle.attention_batched(q, k, v, H, lens, causal)
+    for b in range(nb):
+        np.testing.assert_allclose(ours[b], _sdpa_ref(q[b], k[b], v[b], H, lens[b], causal), atol=1e-12)
+
+
+def test_attention_batched_zero_length_is_zero():
+    r = rng(22)
+    q, k, v = (r.normal(size=(2, 5, 8)) for _ in range(3))
+    out = oracle.attention_batched(q, k, v, 2, np.array([0, 5]), False)
+    assert np.all(out[0] == 0.0) and np.all(np.isfinite(out))
+
+
+def _bmut_scale(q, k, v, n_heads, lengths, causal):
+    hd = q.shape[-1] // n_heads
+    return ORIG_ATTENTION_B(q / np.sqrt(hd), k, v, n_heads, lengths, causal)
+
+
+def _bmut_lengths_off_by_one(q, k, v, n_heads, lengths, causal):
+    return ORIG_ATTENTION_B(q, k, v, n_heads, np.asarray(lengths) - 1, causal)
+
+
+def _bmut_heads_transposed(q, k, v, n_heads, lengths, causal):
+    D = q.shape[-1]
+    hd = D // n_heads
+    perm = np.arange(D).reshape(hd, n_heads).T.reshape(-1)
+    o = ORIG_ATTENTION_B(q[..., perm], k[..., perm], v[..., perm], n_heads, lengths, causal)
+    return o[..., np.argsort(perm)]
+
+
+ORIG_ATTENTION_B = ofw.attention_batched
+
+
+@pytest.mark.parametrize("target,mut", [
+    ("attention_batched", _bmut_scale),
+    ("attention_batched", _bmut_lengths_off_by_one),
+    ("attention_batched", _bmut_heads_transposed),
+    ("layer_norm", _mut_unbiased_var),
+    ("gelu", _mut_tanh_gelu),
+])
+def test_planted_mistakes_are_caught_batched(monkeypatch, target, mut):
+    monkeypatch.setattr(ofw, target, mut)
+    shape = tiny_shape(B=2, S=8, D=16, H=2, F_=32, L=2, causal=False)
+    prm = synth.params(12, shape, ln_affine="random", bias_std=0.3)
+    x = synth.input_x(12, shape) * np.float32(2.0)
+    lens = np.array([8, 6], dtype=np.int32)
+    ours = ofw.forward_batched(prm, 2, x, lens, False)
+    ref = _torch_forward(prm, shape, x, lens, False, norm_first=True)
+    diff = max(np.max(np.abs(ours[b, :lens[b]] - ref[b, :lens[b]])) for b in range(2))
+    assert diff > 1e-6, f"mutation {mut.__name__} not caught (diff {diff})"
