@@ -39,8 +39,8 @@ library routines (torch float64 ``layer_norm``, ``gelu``,
 ``scaled_dot_product_attention`` and ``TransformerEncoder``), closed forms
 and invariants.
 """
-from .stack import (attention, attention_batched, forward, forward_batched, gate, gelu,
-                    layer_norm, sequence_forward)
+from .stack import (attention, attention_backward, attention_batched, attention_lse, forward,
+                    forward_batched, gate, gelu, layer_norm, sequence_forward)
 
-__all__ = ["attention", "attention_batched", "forward", "forward_batched", "gate", "gelu", "layer_norm",
-           "sequence_forward"]
+__all__ = ["attention", "attention_backward", "attention_batched", "attention_lse", "forward", "forward_batched",
+           "gate", "gelu", "layer_norm", "sequence_forward"]

@@ -175,6 +175,75 @@ def forward(params, n_heads: int, x: np.ndarray, lengths: Optional[np.ndarray], 
     return np.stack(outs)
 
 
+def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, n_heads: int,
+                       length: int, causal: bool):
+    """Gradients (dq, dk, dv) of the attention of ``attention`` for one sequence.
+
+    The gradient of O = softmax(Q K^T / sqrt(d_k) + mask) V ("TikTok TechJam 2026 --
+    Problem 3", section 2.1) by the chain rule, per head:
+      dV = P^T dO;  dP = dO V^T;  dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik);
+      dQ = dS K / sqrt(d_k);  dK = dS^T Q / sqrt(d_k).
+    sum_k P_ik dP_ik equals dO_i . O_i, the row sum the fused backward of
+    "Training throughput baseline" (Fused attention) takes from the output gradient
+    and the output.  Query rows at or past ``length`` are padding: their output
+    gradient is ignored (taken as zero), so their dq is zero and they add nothing
+    to dk and dv; keys at or past ``length`` are masked and get zero gradient.
+    q, k, v, dout: [S, D].  Returns float64 dq, dk, dv [S, D].
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.array(dout, dtype=np.float64)
+    S, D = q.shape
+    hd = D // n_heads
+    do[length:] = 0.0
+    j = np.arange(S)
+    allowed = (j[None, :] < length)
+    if causal:
+        allowed = allowed & (j[None, :] <= j[:, None])
+    any_allowed = allowed.any(axis=1, keepdims=True)
+    dq = np.zeros((S, D))
+    dk = np.zeros((S, D))
+    dv = np.zeros((S, D))
+    for h in range(n_heads):
+        c = slice(h * hd, (h + 1) * hd)
+        s = np.where(allowed, q[:, c] @ k[:, c].T / np.sqrt(hd), -np.inf)
+        m = np.max(s, axis=1, keepdims=True)
+        m = np.where(np.isfinite(m), m, 0.0)
+        e = np.where(allowed, np.exp(s - m), 0.0)
+        den = e.sum(axis=1, keepdims=True)
+        p = np.where(any_allowed, e / np.where(den > 0, den, 1.0), 0.0)
+        dv[:, c] = p.T @ do[:, c]
+        dp = do[:, c] @ v[:, c].T
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        dq[:, c] = ds @ k[:, c] / np.sqrt(hd)
+        dk[:, c] = ds.T @ q[:, c] / np.sqrt(hd)
+    return dq, dk, dv
+
+
+def attention_lse(q: np.ndarray, k: np.ndarray, n_heads: int, length: int, causal: bool) -> np.ndarray:
+    """Natural log of the softmax normaliser of every (head, query row) of ``attention``:
+    LSE_hi = log sum_{allowed j} exp(q_i . k_j / sqrt(d_k)); -inf where no key is allowed.
+    Returns float64 [n_heads, S]."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    S, D = q.shape
+    hd = D // n_heads
+    j = np.arange(S)
+    allowed = (j[None, :] < length)
+    if causal:
+        allowed = allowed & (j[None, :] <= j[:, None])
+    out = np.full((n_heads, S), -np.inf)
+    for h in range(n_heads):
+        c = slice(h * hd, (h + 1) * hd)
+        s = np.where(allowed, q[:, c] @ k[:, c].T / np.sqrt(hd), -np.inf)
+        m = np.max(s, axis=1)
+        ok = np.isfinite(m)
+        mm = np.where(ok, m, 0.0)
+        out[h] = np.where(ok, mm + np.log(np.where(allowed, np.exp(s - mm[:, None]), 0.0).sum(axis=1)), -np.inf)
+    return out
+
+
 def attention_batched(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int,
                       lengths: np.ndarray, causal: bool) -> np.ndarray:
     """``attention`` for a batch of sequences at once: q, k, v [nb, S, D], lengths [nb].
