@@ -9,7 +9,7 @@ if ROOT not in sys.path:
 
 
 def pytest_addoption(parser):
-    parser.addoption("--s100k-seeds", type=int, default=3,
+    parser.addoption("--s100k-seeds", type=int, default=5,
                      help="seeds for the B=32 S=100000 workload gate (about 20 s each)")
 
 

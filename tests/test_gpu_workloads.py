@@ -1,17 +1,20 @@
-"""GPU parity at the five benchmark shapes, over 25 seeds each (S=100000: 3).
+"""GPU parity at the five benchmark shapes, element by element, over 25 seeds.
 
-The GPU runs the whole batch at full size through the C ABI, in the same
-launch configuration the benchmark times (graph replay).  The oracle then
-checks, element by element with the graded rule:
-  * B=1 S=128: every output element;
-  * B=64 S=1024, B=10000 S=128, B=16 S=512: whole sequences sampled per seed
-    (sequences are independent, so a sampled sequence is checked exactly),
-    always including the longest and the shortest, plus a check that every
-    padded row of the whole batch is exactly zero;
-  * B=32 S=100000 (one layer): 2 sequences x 64 query rows per seed, always
-    including rows 0 and S-1 (exact: with one causal layer a row depends
-    only on the keys before it); seeds 0..2 by default (about 20 s each),
-    more with --s100k-seeds N.
+"Transformerkernel" (Challenges) ran its checks over 25 trials and warns that the
+worst element of a run grows like sigma * sqrt(2 ln N) with the number N of
+elements checked, so a gate that samples a few sequences understates the error
+the rule has to absorb.  The GPU runs the whole batch at full size through the
+C ABI, in the launch configuration the benchmark times (graph replay), and the
+fp64 oracle then checks it with the graded rule |u-r| <= 2e-3 or <= 0.02|r|:
+  * B=1 S=128, B=64 S=1024 and B=16 S=512: every element of every sequence,
+    seeds 0..24;
+  * B=10000 S=128: every element of every sequence for seeds 0..4, and for
+    seeds 5..24 whole sampled sequences (always the longest and the shortest),
+    with every padded row of the whole batch checked to be exactly zero;
+  * B=32 S=100000 (one causal layer): 2 sequences x 64 query rows per seed,
+    always including rows 0 and S-1 (exact: with one causal layer a row depends
+    only on the keys before it); seeds 0..4 by default (about 20 s each), more
+    with --s100k-seeds N.
 Seeds drive both weights and inputs.  The worst ratio |u-r| / max(2e-3,
 0.02|r|) over all seeds is printed for the record.
 """
@@ -25,6 +28,7 @@ from tests.helpers import gate_report
 pytestmark = pytest.mark.gpu
 
 SEEDS = list(range(25))
+FULL_SEEDS_B10000 = 5
 
 
 def _run_full(shape, prm, x, lens):
@@ -46,7 +50,25 @@ def _ratio(u, r):
     return float(np.max(np.abs(u - r) / np.maximum(2e-3, 0.02 * np.abs(r))))
 
 
-def _check_sequences(wl_index, n_seq, seeds=SEEDS):
+def _oracle_all(shape, prm, x, lens):
+    """fp64 oracle output of every sequence of the batch."""
+    if shape.d_model <= 128:
+        # many small array operations: worker processes, one sequence group per task
+        chunk = 1 if shape.S >= 512 else 128
+        return oracle.forward_batched(prm, shape.n_heads, x, lens, shape.causal, chunk=chunk, processes=True)
+    # large projections: one batch, multi-threaded BLAS in this process
+    return oracle.forward_batched(prm, shape.n_heads, x, lens, shape.causal, chunk=shape.B)
+
+
+def _padded_rows_zero(out, lens, S, seed):
+    import torch
+    pad = np.arange(S)[None, :] >= lens[:, None]
+    if pad.any():
+        padmask = torch.from_numpy(pad).cuda()
+        assert bool((out[padmask] == 0).all()), f"seed {seed}: padded rows not zero"
+
+
+def _check_every_element(wl_index, seeds):
     shape = synth.WORKLOADS[wl_index]
     worst = 0.0
     for seed in seeds:
@@ -54,52 +76,59 @@ def _check_sequences(wl_index, n_seq, seeds=SEEDS):
         lens = synth.lengths(seed, shape)
         x = synth.input_x(seed, shape)
         out = _run_full(shape, prm, x, lens)
-        # padded rows of the whole batch are exactly zero
-        pos = np.arange(shape.S)[None, :]
-        pad = (pos >= lens[:, None])
-        if pad.any():
-            import torch
-            padmask = torch.from_numpy(pad).cuda()
-            assert bool((out[padmask] == 0).all()), f"seed {seed}: padded rows not zero"
+        _padded_rows_zero(out, lens, shape.S, seed)
+        u = out.cpu().numpy()
+        del out
+        r = _oracle_all(shape, prm, x, lens)
+        assert np.isfinite(u).all(), f"{shape.name} seed {seed}: non-finite output"
+        ok = oracle.gate(u, r)
+        assert ok.all(), f"{shape.name} seed {seed}: {gate_report(u, r)}"
+        worst = max(worst, _ratio(u, r))
+    print(f"\n{shape.name}: worst |u-r|/budget over {len(seeds)} seeds, every element = {worst:.3f}")
+    return worst
+
+
+def _check_sequences(wl_index, n_seq, seeds):
+    shape = synth.WORKLOADS[wl_index]
+    worst = 0.0
+    for seed in seeds:
+        prm = synth.params(seed, shape)
+        lens = synth.lengths(seed, shape)
+        x = synth.input_x(seed, shape)
+        out = _run_full(shape, prm, x, lens)
+        _padded_rows_zero(out, lens, shape.S, seed)
         rng = np.random.default_rng(1000 + seed)
         pick = {int(np.argmax(lens)), int(np.argmin(lens))}
         while len(pick) < min(n_seq, shape.B):
             pick.add(int(rng.integers(shape.B)))
         bsel = np.array(sorted(pick))
         u = out[bsel].cpu().numpy()
-        r = oracle.forward(prm, shape.n_heads, x[bsel], lens[bsel], shape.causal)
-        ok = oracle.gate(u, r)
-        assert np.isfinite(u).all()
-        assert ok.all(), f"{shape.name} seed {seed} sequences {bsel.tolist()}: {gate_report(u, r)}"
-        worst = max(worst, _ratio(u, r))
         del out
-    print(f"\n{shape.name}: worst |u-r|/budget over {len(seeds)} seeds = {worst:.3f}")
+        r = oracle.forward_batched(prm, shape.n_heads, x[bsel], lens[bsel], shape.causal)
+        assert np.isfinite(u).all()
+        assert oracle.gate(u, r).all(), f"{shape.name} seed {seed} sequences {bsel.tolist()}: {gate_report(u, r)}"
+        worst = max(worst, _ratio(u, r))
+    print(f"\n{shape.name}: worst |u-r|/budget over {len(seeds)} seeds ({n_seq} sampled sequences) = {worst:.3f}")
 
 
 def test_workload_b1_s128_all_elements():
-    shape = synth.WORKLOADS[0]
-    worst = 0.0
-    for seed in SEEDS:
-        prm = synth.params(seed, shape)
-        lens = synth.lengths(seed, shape)
-        x = synth.input_x(seed, shape)
-        u = _run_full(shape, prm, x, lens).cpu().numpy()
-        r = oracle.forward(prm, shape.n_heads, x, lens, shape.causal)
-        assert oracle.gate(u, r).all(), f"seed {seed}: {gate_report(u, r)}"
-        worst = max(worst, _ratio(u, r))
-    print(f"\n{shape.name}: worst |u-r|/budget over {len(SEEDS)} seeds = {worst:.3f}")
+    _check_every_element(0, SEEDS)
 
 
-def test_workload_b64_s1024_ragged():
-    _check_sequences(1, 3)
+def test_workload_b64_s1024_ragged_all_elements():
+    _check_every_element(1, SEEDS)
 
 
-def test_workload_b10000_s128_keymask():
-    _check_sequences(2, 16)
+def test_workload_b10000_s128_keymask_all_elements():
+    _check_every_element(2, list(range(FULL_SEEDS_B10000)))
 
 
-def test_workload_b16_s512_d1024():
-    _check_sequences(3, 1)
+def test_workload_b10000_s128_keymask_sampled_sequences():
+    _check_sequences(2, 16, list(range(FULL_SEEDS_B10000, 25)))
+
+
+def test_workload_b16_s512_d1024_all_elements():
+    _check_every_element(3, SEEDS)
 
 
 def test_workload_b32_s100000_sampled_rows(request):
