@@ -74,9 +74,7 @@ constexpr int kMaxF = 2048;
 constexpr int kPBo = 0, kPB2 = 128, kPLn1g = 256, kPLn1b = 384, kPLn2g = 512, kPLn2b = 640, kPLnng = 768,
               kPLnnb = 896, kPLnfg = 1024, kPLnfb = 1152, kPB1 = 1280;
 constexpr int kPBqkv = kPB1 + kMaxF;  // next layer's [bq | bk | bv] (fuse_qkv)
-constexpr int kPU1 = kPBqkv + 3 * kD;   // row sums of the LN-folded W1 (pre-LN; else zeros)
-constexpr int kPUqkv = kPU1 + kMaxF;   // row sums of the next layer's LN-folded W_qkv
-constexpr int kParamBytes = (kPUqkv + 3 * kD) * 4;
+constexpr int kParamBytes = (kPBqkv + 3 * kD) * 4;
 constexpr size_t kSmem = 1024 + kOBytes + (size_t)kRing * kUnit + kXpBytes + kRedBytes + kParamBytes + 512;
 
 constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;  // GP: hi [384,448), lo [448,512)
@@ -155,27 +153,15 @@ __device__ __forceinline__ void scale_bias32(float* v, float scale, const float*
   }
 }
 
-// v[i] = v[i] * a + (u[i] * b + p[i]) for 32 values, u and p in shared memory: the
-// output of a linear layer whose input LayerNorm (per-row statistics folded into
-// a = rstd * 2^-s, b = -rstd * mean) is applied after the product.
-__device__ __forceinline__ void fold_bias32(float* v, float a, float b, const float* u, const float* p) {
-  const float2* u2 = reinterpret_cast<const float2*>(u);
-  const float2* p2 = reinterpret_cast<const float2*>(p);
-  const uint64_t a2 = f2_splat(a), b2 = f2_splat(b);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 uu = u2[i], q = p2[i];
-    const uint64_t c = f2_fma(f2_pack(uu.x, uu.y), b2, f2_pack(q.x, q.y));
-    f2_unpack(f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), a2, c), v[2 * i], v[2 * i + 1]);
-  }
-}
-
-// fp16 hi/lo pairs of 16 values (first value of a pair in the low half): v = hi + lo + O(2^-22 |v|).
-__device__ __forceinline__ void split_pairs16(const float* v, uint32_t* hi, uint32_t* lo) {
+// fp16 hi/lo pairs of v[i] - c for 16 values (the row's mean taken out before the split).
+__device__ __forceinline__ void split_centered_pairs16(const float* v, float c, uint32_t* hi, uint32_t* lo) {
+  const uint64_t c2 = f2_splat(c);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint64_t x = f2_pack(v[2 * i], v[2 * i + 1]);
-    const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+    const uint64_t x = f2_sub(f2_pack(v[2 * i], v[2 * i + 1]), c2);
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    const __half2 h = __floats2half2_rn(x0, x1);
     const float2 hf = __half22float2(h);
     float l0, l1;
     f2_unpack(f2_sub(x, f2_pack(hf.x, hf.y)), l0, l1);
@@ -292,9 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto source = [&](int i) -> const float* {
       if (i < kPB1) return src[i / kD] ? src[i / kD] + (i % kD) : nullptr;
       if (i < kPBqkv) return i - kPB1 < args.F ? args.b1 + (i - kPB1) : nullptr;
-      if (i < kPU1) return args.fuse_qkv ? args.bqkv + (i - kPBqkv) : nullptr;
-      if (i < kPUqkv) return (args.u1 && i - kPU1 < args.F) ? args.u1 + (i - kPU1) : nullptr;
-      return (args.fuse_qkv && args.uqkv) ? args.uqkv + (i - kPUqkv) : nullptr;
+      return args.fuse_qkv ? args.bqkv + (i - kPBqkv) : nullptr;
     };
     float pv[kPer];
 #pragma unroll
@@ -611,8 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bounded(acc_full, afph, ewc)) break;
       afph ^= 1u;
       tc_fence_after();
-      // FFN-in input row statistics: GELU input = acc a1 + (u1 b1v + b1)
-      float a1 = args.scale_1, b1v = 0.f;
+      // FFN-in: GELU input = acc * a1 + b1 (pre-LN: a1 = rstd 2^-s, the row's mean taken
+      // out of the operand before the product; post-LN: a1 = 2^-s)
+      float a1 = args.scale_1;
       {
         float tv[32];
         tmem_ld32(tq + kColA1 + c0, tv);
@@ -628,13 +613,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
 #pragma unroll
         for (int i = 0; i < 32; ++i) tv[i] *= args.scale_2;
-        // the FFN's input as fp16 hi/lo pairs in TMEM: t itself.  Pre-LN, LN2's
-        // affine is folded into W1 and its row statistics, computed while FFN-in
-        // runs, enter the GELU input (post-LN the FFN reads t unnormalised).
+        // the FFN's input as fp16 hi/lo pairs in TMEM.  Pre-LN, LN2's affine is folded
+        // into W1 and the operand is t - mean (centred before the split, so its size is
+        // the row's spread, not its offset); rstd enters the GELU input.  Post-LN the FFN
+        // reads t itself.
+        float mean = 0.f;
+        if (!args.post_ln) {
+          float rstd;
+          stats32(tv, eps, red, slot, part, r, mean, rstd);
+          slot = (slot + 2) & 3;
+          a1 = rstd * args.scale_1;
+        }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint32_t hi[8], lo[8];
-          split_pairs16(tv + 16 * j, hi, lo);
+          split_centered_pairs16(tv + 16 * j, mean, hi, lo);
           tmem_st8_u(tq + kColN2 + part * 16 + 8 * j, hi);
           tmem_st8_u(tq + kColN2 + 64 + part * 16 + 8 * j, lo);
         }
@@ -642,15 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_read);
-        if (!args.post_ln) {
-          float mean, rstd;
-          stats32(tv, eps, red, slot, part, r, mean, rstd);
-          slot = (slot + 2) & 3;
-          a1 = rstd * args.scale_1;
-          b1v = -rstd * mean;
-        }
       }
-      const uint64_t a1x2 = f2_splat(a1), b1x2 = f2_splat(b1v);
+      const uint64_t a1x2 = f2_splat(a1);
       // pull the next tile's residual rows into L2 while this tile's FFN runs
       if (ti + (int)gridDim.x < n_live) {
         const int mn = t_next * kGemmBM + q * 32 + lane;
@@ -673,15 +659,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(g_read);
         const int f0 = ((c + t) % nch) * kFC + c0;
         const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + f0);
-        const float2* u1 = reinterpret_cast<const float2*>(prm + kPU1 + f0);
         // GELU and fp16 hi/lo split of the 32 values in registers, then into GP once
         // FFN-out of the previous chunk has read it (the GELU overlaps that MMA)
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 bq = b1[e], uq = u1[e];
-          const uint64_t x0 = f2_fma(f2_pack(uq.x, uq.y), b1x2, f2_pack(bq.x, bq.y));
-          const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), a1x2, x0));
+          const float2 bq = b1[e];
+          const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), a1x2, f2_pack(bq.x, bq.y)));
           float g0, g1;
           f2_unpack(gl, g0, g1);
           const __half2 h = __floats2half2_rn(g0, g1);  // first value in the low half
@@ -722,15 +706,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       scale_bias32(tv, args.scale_2, prm + kPB2 + c0);
       if (args.post_ln) layer_norm32(tv, eps, prm + kPLn2g, prm + kPLn2b, c0, red, slot, part, r);
       if (!args.last && args.fuse_qkv) {
-        // the next layer's QKV input, t2 itself, as fp16 hi/lo pairs into this warp's own
-        // 32 OUT columns of [0, 128) (values c0 + 16 j .. +15: hi at 32 part + 8 j, lo 16
+        // the next layer's QKV input as fp16 hi/lo pairs into this warp's own 32 OUT
+        // columns of [0, 128) (values c0 + 16 j .. +15: hi at 32 part + 8 j, lo 16
         // further), so no other warp's OUT read is overtaken.  Pre-LN, the next LN1's
-        // affine is folded into W_qkv and its row statistics, computed while the QKV MMAs
-        // run, enter the drains below; post-LN, t2 is the normalised residual already.
+        // affine is folded into W_qkv and the operand is t2 - mean (rstd enters the
+        // drains below); post-LN, t2 is the normalised residual already.
+        float aq = args.scale_qkv, mean = 0.f;
+        if (!args.post_ln) {
+          float rstd;
+          stats32(tv, eps, red, slot, part, r, mean, rstd);
+          slot = (slot + 2) & 3;
+          aq = rstd * args.scale_qkv;
+        }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint32_t hi[8], lo[8];
-          split_pairs16(tv + 16 * j, hi, lo);
+          split_centered_pairs16(tv + 16 * j, mean, hi, lo);
           tmem_st8_u(tq + 32 * part + 8 * j, hi);
           tmem_st8_u(tq + 32 * part + 16 + 8 * j, lo);
         }
@@ -738,14 +729,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(n_ready);
-        float aq = args.scale_qkv, bqv = 0.f;
-        if (!args.post_ln) {
-          float mean, rstd;
-          stats32(tv, eps, red, slot, part, r, mean, rstd);
-          slot = (slot + 2) & 3;
-          aq = rstd * args.scale_qkv;
-          bqv = -rstd * mean;
-        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint4 pk[4];
@@ -766,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float qv[32];
           tmem_ld32(tq + 128 + 128 * j + c0, qv);
           tmem_wait_ld();
-          fold_bias32(qv, aq, bqv, prm + kPUqkv + 128 * j + c0, prm + kPBqkv + 128 * j + c0);
+          scale_bias32(qv, aq, prm + kPBqkv + 128 * j + c0);
           if (!valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) qv[i] = 0.f;

@@ -218,29 +218,25 @@ __global__ void absmax_kernel(const float* __restrict__ src, size_t n, unsigned*
 }
 
 // Folds a LayerNorm's affine part into the linear layer that reads it, in place:
-// LN(t) W^T + bias = rstd (t W'^T) - rstd mean u + bias', with
-// W'[j][k] = W[j][k] gamma[k], u[j] = sum_k W'[j][k], bias'[j] = bias[j] + sum_k W[j][k] beta[k]
-// (sums in fp64).  One thread per output row; create-time only.
-__global__ void fold_ln_kernel(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias,
-                               float* u) {
+// LN(t) W^T + bias = rstd ((t - mean) W'^T) + bias', with W'[j][k] = W[j][k] gamma[k]
+// and bias'[j] = bias[j] + sum_k W[j][k] beta[k] (sum in fp64).  One thread per
+// output row; create-time only.
+__global__ void fold_ln_kernel(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias) {
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= rows) return;
   float* wr = w + (size_t)j * cols;
-  double su = 0.0, sb = 0.0;
+  double sb = 0.0;
   for (int k = 0; k < cols; ++k) {
     const float wk = wr[k];
-    const float wf = wk * gamma[k];
-    wr[k] = wf;
-    su += (double)wf;
+    wr[k] = wk * gamma[k];
     sb += (double)wk * (double)beta[k];
   }
-  u[j] = (float)su;
   bias[j] = (float)((double)bias[j] + sb);
 }
 
 cudaError_t launch_fold_ln(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias,
-                           float* u, cudaStream_t s) {
-  fold_ln_kernel<<<(rows + 127) / 128, 128, 0, s>>>(w, rows, cols, gamma, beta, bias, u);
+                           cudaStream_t s) {
+  fold_ln_kernel<<<(rows + 127) / 128, 128, 0, s>>>(w, rows, cols, gamma, beta, bias);
   return cudaGetLastError();
 }
 

@@ -79,11 +79,11 @@ def test_repeat_calls_are_deterministic():
     np.testing.assert_array_equal(a, b)
 
 
-@pytest.mark.parametrize("offset", [10.0, 100.0])
+@pytest.mark.parametrize("offset", [10.0, 100.0, 1000.0])
 def test_d128_residual_far_from_zero_mean(offset):
-    # The fused chain applies the pre-LN LayerNorms' statistics after the GEMMs (their
-    # affines folded into the weights), so the GEMM operands carry the residual's mean.
-    # Rows whose mean is many standard deviations away from zero must still meet the rule.
+    # The fused chain folds the pre-LN LayerNorms' affines into the GEMM weights and
+    # takes each row's mean out of the operand before the fp16 hi/lo split.  Rows whose
+    # mean sits many standard deviations away from zero must still meet the rule.
     B, S, D, H, F, L = 2, 200, 128, 4, 512, 2
     shape = synth.Shape(B, S, D, H, F, L, True)
     prm = synth.params(4, shape, ln_affine="random")
