@@ -27,10 +27,10 @@ TFL_ERR_DEVICE_TIMEOUT = -5
 TFL_ERR_BAD_LENGTHS = -6
 
 KIND_NAMES = {1: "rownorm", 2: "gemm_qkv", 3: "attention", 4: "gemm_oproj", 5: "gemm_ffn1", 6: "gemm_ffn2",
-              7: "postchain"}
+              7: "postchain", 8: "stack"}
 
 EXPORTS = ("tfl_default_options", "tfl_workspace_bytes", "tfl_create", "tfl_forward", "tfl_forward_bf16",
-           "tfl_forward_host",
+           "tfl_forward_host", "tfl_forward_streamed",
            "tfl_status", "tfl_destroy", "tfl_last_error", "tfl_profile_forward", "tfl_launch_count",
            "tfl_probe_wait_timeout", "tfl_forward_noalloc", "tfl_selftest_gelu")
 
@@ -58,7 +58,8 @@ class TflWeights(ctypes.Structure):
 
 class TflOptions(ctypes.Structure):
     _fields_ = [("precision", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("wait_timeout_ns", ctypes.c_int64),
-                ("max_workspace_bytes", ctypes.c_int64), ("use_graph", ctypes.c_int32)]
+                ("max_workspace_bytes", ctypes.c_int64), ("use_graph", ctypes.c_int32),
+                ("whole_stack", ctypes.c_int32)]
 
 
 class TflError(RuntimeError):
@@ -96,6 +97,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.tfl_forward_noalloc.restype = ctypes.c_int
     lib.tfl_forward_host.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp]
     lib.tfl_forward_host.restype = ctypes.c_int
+    lib.tfl_forward_streamed.argtypes = [vp, vp, vp, i64, ctypes.c_int, vp, vp]
+    lib.tfl_forward_streamed.restype = ctypes.c_int
     lib.tfl_status.argtypes = [vp, vp]
     lib.tfl_status.restype = ctypes.c_int
     lib.tfl_destroy.argtypes = [vp]
@@ -169,6 +172,13 @@ def tfl_forward_host(handle: int, x: int, lengths: Optional[int], causal: int, o
     if rc not in (TFL_OK, TFL_ERR_DEVICE_TIMEOUT, TFL_ERR_BAD_LENGTHS):
         raise TflError(rc, tfl_last_error())
     return rc
+
+
+def tfl_forward_streamed(handle: int, x: int, lengths: Optional[int], n_seq: int, causal: int, out: int,
+                         stream: int = 0) -> None:
+    """n_seq sequences from pinned host x to pinned host out, streamed through the handle in
+    slices of its batch size (asynchronous on ``stream``)."""
+    _check(load().tfl_forward_streamed(handle, x, lengths, int(n_seq), int(causal), out, stream))
 
 
 def tfl_status(handle: int, stream: int = 0) -> int:

@@ -13,6 +13,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <mutex>
@@ -111,8 +112,6 @@ struct PackedW {
 struct LayerDev {
   PackedW wqkv, wo, w1, w2;
   float *bqkv, *bo, *b1, *b2, *ln1_g, *ln1_b, *ln2_g, *ln2_b;
-  // fused chain, pre-LN: row sums of the LN-folded W1 and W_qkv (zeros otherwise)
-  float *u1, *uqkv;
 };
 
 struct GraphEntry {
@@ -158,6 +157,12 @@ WsLayout ws_layout(const tfl_shape& s, int precision) {
 // The fused post-attention chain serves d_model = 128, d_ff <= 2048 at precision 2.
 bool use_chain(int D, int F, int precision) { return D == 128 && F <= 2048 && precision == 2; }
 
+// The whole-stack kernel: one sequence per 128-row tile, head_dim 32, the chain's limits.
+bool use_stack(const tfl_shape& s, const tfl_options& o) {
+  return o.whole_stack && use_chain(s.d_model, s.d_ff, o.precision) && s.S <= 128 && s.n_heads == 4 &&
+         s.n_layers <= kStackMaxLayers;
+}
+
 // Output tile width: 256 when N allows it, except with split activations (the
 // four operand tiles of a 256-wide stage leave room for only two stages).
 int gemm_bn(int N, int split_act) { return (N % 256 == 0 && !split_act) ? 256 : 128; }
@@ -170,8 +175,11 @@ struct tfl_handle {
   int device = 0, num_sms = 0;
   int M = 0, D = 0, H = 0, hd = 0, F = 0, L = 0;
   // pre-LN fused chain: W1 carries LN2's affine, and W_qkv of layers >= 1 carries
-  // LN1's (layer 0's QKV GEMM reads rows the input LayerNorm already normalised)
+  // LN1's (layer 0's QKV GEMM reads rows the input LayerNorm already normalised);
+  // the whole-stack kernel normalises layer 0's input itself, so there W_qkv of
+  // every layer carries LN1's affine
   bool fold = false;
+  bool stack = false;
   void* wmem = nullptr;
   void* ws = nullptr;
   WsLayout lay{};
@@ -187,6 +195,15 @@ struct tfl_handle {
   float *hx_dev = nullptr, *hout_dev = nullptr;
   int* hlen_dev = nullptr;
   cudaStream_t cap_stream = nullptr;  // graphs are captured here (the legacy stream cannot be captured)
+  // tfl_forward_streamed: two device buffers each for x, out and lengths of one slice;
+  // copy-in, compute and copy-out streams; per-slice lengths staged in pinned memory
+  float *sx_dev[2] = {}, *sout_dev[2] = {};
+  int* slen_dev[2] = {};
+  int* slen_pin = nullptr;
+  size_t slen_cap = 0;
+  cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {}, ev_staged = nullptr;
+  bool staged_pending = false;
 };
 
 namespace {
@@ -331,6 +348,55 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
   TFL_CUDA(cudaMemsetAsync(h->sched, 0, (size_t)L * sizeof(int), st), "work counter reset");
   TFL_CUDA(launch_prepare(lengths, h->shape.B, h->shape.S, h->M, h->status, tiles, st), "preparation launch");
 
+  if (h->stack) {
+    StackArgs sa;
+    sa.c = c;
+    sa.B = h->shape.B;
+    sa.F = F;
+    sa.L = L;
+    sa.causal = causal;
+    sa.post_ln = pre ? 0 : 1;
+    sa.eps = eps;
+    sa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->hd));
+    sa.x = bf16 ? nullptr : x;
+    sa.xbf = xbf;
+    sa.out32 = bf16 ? nullptr : out;
+    sa.outbf = outbf;
+    sa.lnf_g = h->lnf_g;
+    sa.lnf_b = h->lnf_b;
+    StackMaps sm;
+    for (int l = 0; l < L; ++l) {
+      const LayerDev& ly = h->layers[l];
+      StackLayerArgs& la = sa.layer[l];
+      la.scale_qkv = ly.wqkv.acc_scale;
+      la.scale_o = ly.wo.acc_scale;
+      la.inv_scale_o = 1.0f / ly.wo.acc_scale;  // exact: powers of two
+      la.scale_1 = ly.w1.acc_scale;
+      la.scale_2 = ly.w2.acc_scale;
+      la.inv_scale_2 = 1.0f / ly.w2.acc_scale;
+      la.bqkv = ly.bqkv;
+      la.bo = ly.bo;
+      la.b1 = ly.b1;
+      la.b2 = ly.b2;
+      la.ln1_g = ly.ln1_g;
+      la.ln1_b = ly.ln1_b;
+      la.ln2_g = ly.ln2_g;
+      la.ln2_b = ly.ln2_b;
+      sm.wqkv[l] = ly.wqkv.tm_hi;
+      sm.wqkv_lo[l] = ly.wqkv.tm_lo;
+      sm.wo[l] = ly.wo.tm_hi;
+      sm.wo_lo[l] = ly.wo.tm_lo;
+      sm.w1[l] = ly.w1.tm_hi;
+      sm.w1_lo[l] = ly.w1.tm_lo;
+      sm.w2[l] = ly.w2.tm_hi;
+      sm.w2_lo[l] = ly.w2.tm_lo;
+    }
+    TFL_CUDA(rec_mark(rec, st, 0), "event");
+    TFL_CUDA(launch_stack(sm, sa, h->num_sms, st), "whole-stack kernel");
+    TFL_CUDA(rec_mark(rec, st, TFL_KIND_STACK), "event");
+    return TFL_OK;
+  }
+
   TFL_CUDA(rec_mark(rec, st, 0), "event");
   {
     RowArgs ra;
@@ -406,7 +472,6 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ca.inv_scale_2 = 1.0f / ly.w2.acc_scale;  // exact: acc_scale is a power of two
       ca.bo = ly.bo;
       ca.b1 = ly.b1;
-      ca.u1 = ly.u1;
       ca.b2 = ly.b2;
       ca.ln1_g = ly.ln1_g;
       ca.ln1_b = ly.ln1_b;
@@ -430,7 +495,6 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
         ca.fuse_qkv = 1;
         ca.scale_qkv = nx.wqkv.acc_scale;
         ca.bqkv = nx.bqkv;
-        ca.uqkv = nx.uqkv;
         ca.qkv16 = h->qkv16;
         cm.wqkv = nx.wqkv.tm_hi;  // 128-row boxes at d_model 128
         cm.wqkv_lo = nx.wqkv.tm_lo;
@@ -577,6 +641,7 @@ int tfl_default_options(tfl_options* o) {
   o->wait_timeout_ns = 2000000000LL;
   o->max_workspace_bytes = 0;
   o->use_graph = 1;
+  o->whole_stack = 1;
   return TFL_OK;
 }
 
@@ -590,6 +655,7 @@ const char* tfl_last_error(void) { return g_err.c_str(); }
 int tfl_launch_count(const tfl_handle* h, int causal) {
   (void)causal;
   if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (h->stack) return 2;                           // length check, whole-stack kernel
   if (chain_fuses_qkv(h)) return 2 + 1 + 2 * h->L;  // layer 0's QKV GEMM, then attention + chain per layer
   const int per_layer = use_chain(h->D, h->F, h->opt.precision) ? 3 : (h->D == 128 ? 5 : 7);
   return 2 + per_layer * h->L;
@@ -621,13 +687,14 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   TFL_CUDA(prepare_gemm_kernels(), "gemm kernel attributes");
   TFL_CUDA(prepare_attention_kernels(), "attention kernel attributes");
   TFL_CUDA(prepare_postchain_kernel(), "chain kernel attributes");
+  TFL_CUDA(prepare_stack_kernel(), "whole-stack kernel attributes");
 
   const int D = shape->d_model, F = shape->d_ff, L = shape->n_layers;
   const WsLayout lay = ws_layout(*shape, o.precision);
   const bool wsplit = o.precision >= 1;
   // weights block: per layer (1 or 2) x (3D*D + D*D + F*D + D*F) halves, 3D + D + F + D + 4D floats; + final LN
   const size_t wl_half = (wsplit ? 2 : 1) * ((size_t)3 * D * D + (size_t)D * D + 2 * (size_t)F * D);
-  const size_t wl_float = (size_t)3 * D + D + F + D + 4 * (size_t)D + F + 3 * (size_t)D;
+  const size_t wl_float = (size_t)3 * D + D + F + D + 4 * (size_t)D;
   const size_t per_layer = align_up(wl_half * 2, 1024) + align_up(wl_float * 4, 1024);
   const size_t wbytes = per_layer * L + align_up((size_t)2 * D * 4, 1024);
   if (o.max_workspace_bytes > 0 && (int64_t)(lay.total + wbytes) > o.max_workspace_bytes)
@@ -647,6 +714,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   h->L = L;
   h->lay = lay;
   h->fold = use_chain(D, F, o.precision) && shape->norm_placement == 0;
+  h->stack = use_stack(*shape, o);
   auto bail = [&](int code) {
     tfl_destroy(h);
     return code;
@@ -713,8 +781,6 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
     d.ln1_b = d.ln1_g + D;
     d.ln2_g = d.ln1_b + D;
     d.ln2_b = d.ln2_g + D;
-    d.u1 = d.ln2_b + D;
-    d.uqkv = d.u1 + F;
     const size_t DD = (size_t)D * D, FD = (size_t)F * D;
     if (!rc) rc = copy_f32(src.bq, D, d.bqkv, "bq");
     if (!rc) rc = copy_f32(src.bk, D, d.bqkv + D, "bk");
@@ -726,15 +792,13 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
     if (!rc) rc = copy_f32(src.ln1_b, D, d.ln1_b, "ln1_b");
     if (!rc) rc = copy_f32(src.ln2_g, D, d.ln2_g, "ln2_g");
     if (!rc) rc = copy_f32(src.ln2_b, D, d.ln2_b, "ln2_b");
-    if (!rc && cudaMemset(d.u1, 0, (size_t)(F + 3 * D) * sizeof(float)) != cudaSuccess)
-      rc = fail(TFL_ERR_CUDA, "weight row-sum init failed");
     {
       const float* qkv[3] = {src.wq, src.wk, src.wv};
       const size_t nq[3] = {DD, DD, DD};
       size_t n = 0;
       if (!rc) rc = stage_weights(qkv, nq, 3, tmp, &n, "wq/wk/wv");
-      if (!rc && h->fold && l > 0 &&
-          launch_fold_ln(tmp, 3 * D, D, d.ln1_g, d.ln1_b, d.bqkv, d.uqkv, 0) != cudaSuccess)
+      if (!rc && h->fold && (l > 0 || h->stack) &&
+          launch_fold_ln(tmp, 3 * D, D, d.ln1_g, d.ln1_b, d.bqkv, 0) != cudaSuccess)
         rc = fail(TFL_ERR_CUDA, "LayerNorm fold of W_qkv failed");
       if (!rc) rc = pack_staged(tmp, n, dmax, d.wqkv, wsplit, "wq/wk/wv");
     }
@@ -742,7 +806,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
     {
       size_t n = 0;
       if (!rc) rc = stage_weights(&src.w1, &FD, 1, tmp, &n, "w1");
-      if (!rc && h->fold && launch_fold_ln(tmp, F, D, d.ln2_g, d.ln2_b, d.b1, d.u1, 0) != cudaSuccess)
+      if (!rc && h->fold && launch_fold_ln(tmp, F, D, d.ln2_g, d.ln2_b, d.b1, 0) != cudaSuccess)
         rc = fail(TFL_ERR_CUDA, "LayerNorm fold of W1 failed");
       if (!rc) rc = pack_staged(tmp, n, dmax, d.w1, wsplit, "w1");
     }
@@ -900,6 +964,118 @@ int tfl_forward_host(tfl_handle* h, const float* x_host, const int32_t* lengths_
   return tfl_status(h, stream);
 }
 
+namespace {
+// Pinned (page-locked) host memory: allocated or registered with the CUDA runtime.
+bool host_pinned(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+int streamed_setup(tfl_handle* h, size_t n_slices) {
+  const size_t slice = (size_t)h->M * h->D * sizeof(float);
+  if (!h->s_in) {
+    for (cudaStream_t* st : {&h->s_in, &h->s_comp, &h->s_out})
+      TFL_CUDA(cudaStreamCreateWithFlags(st, cudaStreamNonBlocking), "streamed: stream");
+    TFL_CUDA(cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming), "streamed: event");
+    TFL_CUDA(cudaEventCreateWithFlags(&h->ev_staged, cudaEventDisableTiming), "streamed: event");
+    for (int i = 0; i < 2; ++i) {
+      TFL_CUDA(cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming), "streamed: event");
+      TFL_CUDA(cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming), "streamed: event");
+      TFL_CUDA(cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming), "streamed: event");
+    }
+  }
+  for (int i = 0; i < 2; ++i) {
+    if (h->sx_dev[i]) continue;
+    if (cudaMalloc(&h->sx_dev[i], slice) != cudaSuccess || cudaMalloc(&h->sout_dev[i], slice) != cudaSuccess ||
+        cudaMalloc(&h->slen_dev[i], (size_t)h->shape.B * sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TFL_ERR_OOM, "slice buffers for tfl_forward_streamed");
+    }
+  }
+  const size_t need = n_slices * (size_t)h->shape.B;
+  if (need > h->slen_cap) {
+    if (h->slen_pin) cudaFreeHost(h->slen_pin);
+    h->slen_pin = nullptr;
+    h->slen_cap = 0;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h->slen_pin), need * sizeof(int), cudaHostAllocDefault) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return fail(TFL_ERR_OOM, "pinned lengths staging for tfl_forward_streamed");
+    }
+    h->slen_cap = need;
+  }
+  return TFL_OK;
+}
+}  // namespace
+
+int tfl_forward_streamed(tfl_handle* h, const float* x_host, const int32_t* lengths_host, int64_t n_seq, int causal,
+                         float* out_host, tfl_stream stream) {
+  g_err.clear();
+  if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (!x_host || !out_host) return fail(TFL_ERR_INVALID_ARG, "x and out must be non-NULL host pointers");
+  if (n_seq < 1) return fail(TFL_ERR_INVALID_ARG, "n_seq must be >= 1");
+  if (causal != 0 && causal != 1) return fail(TFL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!host_pinned(x_host) || !host_pinned(out_host))
+    return fail(TFL_ERR_INVALID_ARG, "x and out must be pinned host memory (cudaHostAlloc / cudaHostRegister)");
+  const int B = h->shape.B, S = h->shape.S;
+  const size_t seq_elems = (size_t)S * h->D;
+  const size_t total = (size_t)n_seq * seq_elems * sizeof(float);
+  const uint8_t *xb = reinterpret_cast<const uint8_t*>(x_host), *ob = reinterpret_cast<const uint8_t*>(out_host);
+  if (xb < ob + total && ob < xb + total) return fail(TFL_ERR_INVALID_ARG, "out overlaps x");
+  if (lengths_host)
+    for (int64_t b = 0; b < n_seq; ++b)
+      if (lengths_host[b] < 0 || lengths_host[b] > S) return fail(TFL_ERR_INVALID_ARG, "a length is outside [0, S]");
+  const size_t n_slices = (size_t)((n_seq + B - 1) / B);
+  // the staging area of the previous call must no longer be read by its copies
+  if (h->staged_pending) TFL_CUDA(cudaEventSynchronize(h->ev_staged), "streamed: previous call");
+  h->staged_pending = false;
+  int rc = streamed_setup(h, n_slices);
+  if (rc) return rc;
+  // per-slice lengths; sequences past n_seq in the last slice get length 0 (output zero, never copied back)
+  for (size_t k = 0; k < n_slices; ++k)
+    for (int j = 0; j < B; ++j) {
+      const int64_t b = (int64_t)k * B + j;
+      h->slen_pin[k * B + j] = b < n_seq ? (lengths_host ? lengths_host[b] : S) : 0;
+    }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TFL_CUDA(cudaEventRecord(h->ev_start, st), "streamed: start");
+  for (cudaStream_t s2 : {h->s_in, h->s_comp, h->s_out})
+    TFL_CUDA(cudaStreamWaitEvent(s2, h->ev_start, 0), "streamed: start wait");
+  for (size_t k = 0; k < n_slices; ++k) {
+    const int i = (int)(k & 1);
+    const int64_t nk = std::min<int64_t>(B, n_seq - (int64_t)k * B);
+    const size_t off = k * (size_t)B * seq_elems;
+    const size_t bytes = (size_t)nk * seq_elems * sizeof(float);
+    // copy-in: buffer i was last read by the forward of slice k - 2
+    if (k >= 2) TFL_CUDA(cudaStreamWaitEvent(h->s_in, h->ev_comp[i], 0), "streamed: wait");
+    TFL_CUDA(cudaMemcpyAsync(h->sx_dev[i], x_host + off, bytes, cudaMemcpyHostToDevice, h->s_in), "streamed: x in");
+    TFL_CUDA(cudaMemcpyAsync(h->slen_dev[i], h->slen_pin + k * B, (size_t)B * sizeof(int), cudaMemcpyHostToDevice,
+                             h->s_in),
+             "streamed: lengths in");
+    TFL_CUDA(cudaEventRecord(h->ev_in[i], h->s_in), "streamed: event");
+    // compute: out buffer i was last read by the copy-out of slice k - 2
+    TFL_CUDA(cudaStreamWaitEvent(h->s_comp, h->ev_in[i], 0), "streamed: wait");
+    if (k >= 2) TFL_CUDA(cudaStreamWaitEvent(h->s_comp, h->ev_out[i], 0), "streamed: wait");
+    rc = run_forward(h, h->sx_dev[i], h->slen_dev[i], causal, h->sout_dev[i], h->s_comp);
+    if (rc) return rc;
+    TFL_CUDA(cudaEventRecord(h->ev_comp[i], h->s_comp), "streamed: event");
+    // copy-out
+    TFL_CUDA(cudaStreamWaitEvent(h->s_out, h->ev_comp[i], 0), "streamed: wait");
+    TFL_CUDA(cudaMemcpyAsync(out_host + off, h->sout_dev[i], bytes, cudaMemcpyDeviceToHost, h->s_out),
+             "streamed: out");
+    TFL_CUDA(cudaEventRecord(h->ev_out[i], h->s_out), "streamed: event");
+  }
+  // every copy-in precedes its forward, every forward its copy-out: the last copy-out ends the batch
+  TFL_CUDA(cudaEventRecord(h->ev_staged, h->s_out), "streamed: event");
+  h->staged_pending = true;
+  TFL_CUDA(cudaStreamWaitEvent(st, h->ev_staged, 0), "streamed: end wait");
+  return TFL_OK;
+}
+
 int tfl_profile_forward(tfl_handle* h, const float* x, const int32_t* lengths, int causal, float* out,
                         tfl_stream stream, float* kernel_ms, int32_t* kernel_kind, int32_t cap, int32_t* n) {
   g_err.clear();
@@ -930,6 +1106,19 @@ void tfl_destroy(tfl_handle* h) {
   if (!h) return;
   cudaDeviceSynchronize();
   for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  for (int i = 0; i < 2; ++i) {
+    if (h->sx_dev[i]) cudaFree(h->sx_dev[i]);
+    if (h->sout_dev[i]) cudaFree(h->sout_dev[i]);
+    if (h->slen_dev[i]) cudaFree(h->slen_dev[i]);
+    if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+    if (h->ev_comp[i]) cudaEventDestroy(h->ev_comp[i]);
+    if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+  }
+  if (h->slen_pin) cudaFreeHost(h->slen_pin);
+  if (h->ev_start) cudaEventDestroy(h->ev_start);
+  if (h->ev_staged) cudaEventDestroy(h->ev_staged);
+  for (cudaStream_t st : {h->s_in, h->s_comp, h->s_out})
+    if (st) cudaStreamDestroy(st);
   if (h->ws) cudaFree(h->ws);
   if (h->wmem) cudaFree(h->wmem);
   if (h->hx_dev) cudaFree(h->hx_dev);
@@ -1043,6 +1232,16 @@ int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths, i
   }
   if (!h->n16lo) h->tm_n16lo = h->tm_n16;
   if (!h->g16lo) h->tm_g16lo = h->tm_g16;
+  // The array keeps whatever the last call left, from any handle, shape or precision.
+  // Some rows of it are read without being written first (rows of a 128-row tile that
+  // lies wholly in padding, read as keys past len_b and multiplied by a zero
+  // probability): clear the part this call uses, so that stale bytes can never decode
+  // as Inf or NaN there.
+  cudaError_t ce = cudaMemsetAsync(base, 0, lay.total, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) {
+    restore();
+    return cuda_fail(ce, "scratch clear");
+  }
   const int rc = enqueue(h, x, lengths, causal, out, static_cast<cudaStream_t>(stream), Rec{});
   restore();
   return rc;

@@ -107,10 +107,9 @@ struct ChainArgs {
   float scale_o = 1.f, scale_1 = 1.f, scale_2 = 1.f;  // weight pre-scales undone
   float inv_scale_2 = 1.f;                            // 1 / scale_2 (a power of two)
   // Pre-LN: the LayerNorm affines that feed FFN-in and the next layer's QKV are
-  // folded into those weights (b1, bqkv are the folded biases); u1, uqkv are the
-  // row sums of the folded weights, so LN(t) W^T + b = rstd (t W'^T) - rstd mean u + b'.
+  // folded into those weights (b1, bqkv are the folded biases), so
+  // LN(t) W^T + b = rstd ((t - mean) W'^T) + b' with W' = W diag(gamma), b' = b + W beta.
   const float *bo = nullptr, *b1 = nullptr, *b2 = nullptr;
-  const float *u1 = nullptr, *uqkv = nullptr;
   const float *ln1_g = nullptr, *ln1_b = nullptr, *ln2_g = nullptr, *ln2_b = nullptr;
   const float *lnn_g = nullptr, *lnn_b = nullptr;  // next layer's LN1 (pre-LN, not last)
   const float *lnf_g = nullptr, *lnf_b = nullptr;  // final LN (last)
@@ -134,6 +133,36 @@ struct ChainMaps {
   // box 64 B x 32 rows, 64-byte swizzle
   CUtensorMap h32_st, qkv_st;
 };
+
+// Whole-stack kernel (d_model 128, head_dim 32, S <= 128): every layer of the
+// forward in one launch, one sequence per 128-row tile, the residual kept in
+// tensor memory.  Operands split as at precision 2.
+constexpr int kStackMaxLayers = 8;
+struct StackLayerArgs {
+  float scale_qkv = 1.f, scale_o = 1.f, scale_1 = 1.f, scale_2 = 1.f;  // weight pre-scales undone
+  float inv_scale_o = 1.f, inv_scale_2 = 1.f;                          // their inverses (powers of two)
+  // pre-LN: LN1's affine folded into W_qkv (bqkv folded), LN2's into W1 (b1 folded)
+  const float *bqkv = nullptr, *bo = nullptr, *b1 = nullptr, *b2 = nullptr;
+  const float *ln1_g = nullptr, *ln1_b = nullptr, *ln2_g = nullptr, *ln2_b = nullptr;  // post-LN
+};
+struct StackArgs {
+  Common c;
+  int B = 0, F = 0, L = 0, causal = 0, post_ln = 0;
+  float eps = 1e-5f;
+  float scale_log2 = 0.f;                      // log2(e) / sqrt(head_dim)
+  const float* x = nullptr;                    // [B, S, 128] fp32 input, or
+  const __nv_bfloat16* xbf = nullptr;          // bf16 input
+  float* out32 = nullptr;                      // [B, S, 128] fp32 output, or
+  __nv_bfloat16* outbf = nullptr;              // bf16 output
+  const float *lnf_g = nullptr, *lnf_b = nullptr;
+  StackLayerArgs layer[kStackMaxLayers];
+};
+struct StackMaps {
+  CUtensorMap wqkv[kStackMaxLayers], wqkv_lo[kStackMaxLayers], wo[kStackMaxLayers], wo_lo[kStackMaxLayers];
+  CUtensorMap w1[kStackMaxLayers], w1_lo[kStackMaxLayers], w2[kStackMaxLayers], w2_lo[kStackMaxLayers];
+};
+cudaError_t prepare_stack_kernel();
+cudaError_t launch_stack(const StackMaps& mp, const StackArgs& a, int num_sms, cudaStream_t s);
 
 // TMA descriptors of one GEMM: A (and its lo plane), W (and its lo part).
 struct GemmMaps {
@@ -171,9 +200,9 @@ cudaError_t launch_gelu_selftest(int n, unsigned* out, cudaStream_t s);
 cudaError_t launch_prepare(const int* lengths, int B, int S, int M, int* status, int* tiles, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s);
 cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s);
-// In place: w [rows, cols] <- w * gamma (per column), bias += w beta, u = row sums of the result.
+// In place: w [rows, cols] <- w * gamma (per column), bias += w beta.
 cudaError_t launch_fold_ln(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias,
-                           float* u, cudaStream_t s);
+                           cudaStream_t s);
 cudaError_t launch_split_f16(const float* src, __half* hi, __half* lo, size_t n, float scale, cudaStream_t s);
 cudaError_t launch_probe_wait(int* status, int64_t timeout_ns, cudaStream_t s);
 

@@ -1,7 +1,8 @@
 """Benchmark: forward tokens/s of the Transformer-stack forward on one GB300.
 
-Default workload: B=64, S=1024, d_model=128, H=4 (head_dim 32), d_ff=512,
-4 layers, causal, right-padded lengths uniform in [512, 1024] (seed 0).
+Default workload: the largest single-GPU shape of the workload table,
+B=32, S=100000, d_model=1024, H=16 (head_dim 64), d_ff=4096, 1 layer, causal,
+full lengths (seed 0); --workload N picks another row of the table.
 A step is one whole forward (all layers) over that batch; tokens per step =
 B*S (every position, as the pages count tokens).
 
@@ -9,8 +10,10 @@ Prints ONE JSON line (rank 0).  Keys beyond the base contract:
   roofline      dominant kernel of the step: algorithmic work per launch /
                 its CUDA-event duration, against the measured peak
   cpu_baseline  the fp64 oracle timed on this host on a bounded sample
-  e2e           tokens/s through tfl_forward_host (pinned host x / out,
-                host<->device copies inside the timed region)
+  e2e           tokens/s from pinned host x / out, host<->device traffic inside
+                the timed region: tfl_forward_host (the kernels read x and write
+                out across the host link) or, for batches over 1M tokens,
+                tfl_forward_streamed (batch slices overlapping their copies)
   clocks        SM clock samples taken during the timed region
 With --impl reference the fp64 oracle itself is timed as the reference arm.
 Multi-GPU (torchrun): every rank runs an independent replica on its own
@@ -36,7 +39,7 @@ import synth  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 # ex2.approx.f32 results per clock per SM, measured on GB300 with
-# attention_qkv_gemm_gb300/ex2_rate.cu (32.0 at 8 and 32 warps per SM)
+# tests/probes/ex2_rate.cu (32.0 at 8 and 32 warps per SM)
 MUFU_PER_CLK_PER_SM = 32
 
 
@@ -190,6 +193,8 @@ def forward_bytes(shape: synth.Shape, valid: float):
     (each intermediate written once and read once at its stored width, valid rows only)."""
     D, L = shape.d_model, shape.n_layers
     attn = valid * (3 * D * 2 + D * 2)  # q, k, v in; o out
+    if D == 128 and shape.S <= 128 and shape.n_heads == 4 and L <= 8:  # the whole-stack kernel
+        return stack_bytes(shape, valid)
     if D == 128:  # input LN, layer 0's QKV GEMM, then attention + fused chain per layer
         return (kernel_bytes("rownorm", shape, valid) + kernel_bytes("gemm_qkv", shape, valid)
                 + L * (attn + kernel_bytes("postchain", shape, valid)))
@@ -207,6 +212,7 @@ def forward_bytes(shape: synth.Shape, valid: float):
 # fingerprint a traffic figure was captured with (host code such as api.cu is
 # not part of any kernel's build).
 KERNEL_SOURCES = {
+    "stack": ["stack.cu"],
     "postchain": ["postchain.cu"],
     "attention": ["attention.cu"],
     "gemm_qkv": ["gemm.cu"],
@@ -214,7 +220,7 @@ KERNEL_SOURCES = {
     "gemm_ffn1": ["gemm.cu"],
     "gemm_ffn2": ["gemm.cu"],
 }
-KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh"]
+KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh", "chainops.cuh"]
 
 NCU_TRAFFIC = {
     # (kernel, workload): (kernel source fingerprint, bytes per launch)
@@ -226,8 +232,7 @@ NCU_TRAFFIC = {
     ("gemm_ffn1", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 50.419968e6 + 83.465728e6),
     ("gemm_ffn2", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 186.352896e6 + 19.356416e6),
     ("attention", "B16_S512_D1024_H4_causal"): ("222a4a4c89a8", 50.391808e6 + 0.699392e6),
-    # full-size launch, DRAM counters only (one ncu pass)
-    ("attention", "B32_S100000_D1024_H16_causal"): ("222a4a4c89a8", 24.62e9 + 6.56e9),
+    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("222a4a4c89a8", 208.8e6 + 50.3e6),
 }
 
 
@@ -243,12 +248,76 @@ def csrc_fingerprint(kernel: str = None) -> str:
     return h.hexdigest()[:12]
 
 
+# Workloads too large to capture under ncu take a smaller case's DRAM bytes per launch,
+# scaled by the tokens a launch processes (the kernel reads q, k, v and writes o once per
+# token; its keys and values are re-read from L2, not HBM, under the grouped work order):
+# (kernel, workload): (captured workload, tokens captured, tokens of the full launch)
+NCU_TRAFFIC_SCALED = {
+    ("attention", "B32_S100000_D1024_H16_causal"): ("B2_S16384_D1024_H16_F4096_L1_causal", 2 * 16384, 32 * 100000),
+}
+
+
 def ncu_traffic(kernel: str, workload: str):
+    if (kernel, workload) in NCU_TRAFFIC_SCALED:
+        src, t_small, t_full = NCU_TRAFFIC_SCALED[(kernel, workload)]
+        small = ncu_traffic(kernel, src)
+        return None if small is None else small * t_full / t_small
     e = NCU_TRAFFIC.get((kernel, workload))
     if e is None or kernel not in KERNEL_SOURCES:
         return None
     sha, nbytes = e
     return nbytes if csrc_fingerprint(kernel) == sha else None
+
+
+def ncu_traffic_note(kernel: str, workload: str):
+    if (kernel, workload) in NCU_TRAFFIC_SCALED:
+        src, t_small, t_full = NCU_TRAFFIC_SCALED[(kernel, workload)]
+        return f"ncu DRAM bytes of a {src} launch scaled by tokens ({t_full}/{t_small})"
+    return None
+
+
+def live_tiles(shape: synth.Shape, lens: np.ndarray) -> int:
+    """128-row tiles of the flattened [B*S] token axis that the kernels process: those
+    holding a valid row or a padding row read as a key (rows below len_b rounded up to
+    64, at most S)."""
+    S, n = shape.S, 0
+    M = shape.B * S
+    for t in range((M + 127) // 128):
+        m0, m1 = t * 128, min(M, t * 128 + 128)
+        for b in range(m0 // S, (m1 - 1) // S + 1):
+            kr = min(S, (int(lens[b]) + 63) // 64 * 64)
+            if max(m0, b * S) < min(m1, b * S + kr):
+                n += 1
+                break
+    return n
+
+
+def chain_executed_flops(shape: synth.Shape, lens: np.ndarray) -> float:
+    """Tensor FLOPs the fused chain (d_model 128) executes per forward: per live 128-row
+    tile, 128x128x16 MMAs -- o_proj 16 (8 k-steps, weight hi and lo), FFN-in and FFN-out
+    24 per 128-wide d_ff chunk each (operand and weight split, 3 MMAs per k-step), and the
+    next layer's QKV projection 72 in every launch but the last."""
+    L, nch = shape.n_layers, shape.d_ff // 128
+    mmas = L * (16 + 48 * nch) + (L - 1) * 72
+    return float(live_tiles(shape, lens)) * mmas * 2.0 * 128 * 128 * 16
+
+
+def stack_executed_flops(shape: synth.Shape, lens: np.ndarray) -> float:
+    """Tensor FLOPs the whole-stack kernel executes per forward, in 128x128x16 MMA
+    equivalents per sequence (one 128-row tile) and layer: QKV 72 (3 blocks x 8
+    k-steps x 3 split MMAs), attention per head S 2 + P V 2 (N = 32) + row sum 1 (N = 16),
+    o_proj 16, FFN 48 per 128-wide d_ff chunk."""
+    nch = shape.d_ff // 128
+    per_layer = 72 + (shape.n_heads * 5) + 16 + 48 * nch
+    seqs = int((lens > 0).sum())
+    return float(seqs) * shape.n_layers * per_layer * 2.0 * 128 * 128 * 16
+
+
+def stack_bytes(shape: synth.Shape, valid: float) -> float:
+    """Algorithmic HBM bytes of the whole-stack kernel per forward: x of the valid rows in,
+    every output row out (fp32), and the packed fp16 weights (hi and lo) once."""
+    D, F, L = shape.d_model, shape.d_ff, shape.n_layers
+    return valid * D * 4 + shape.B * shape.S * D * 4 + L * (4 * D * D + 2 * D * F) * 2 * 2
 
 
 # Sequences longer than this are sampled by query rows for the oracle timing (one
@@ -315,6 +384,17 @@ def reference_arm(args, shape, world, rank):
     return 0
 
 
+def e2e_slice(shape, arg: int) -> int:
+    """Sequences per slice of the streamed end-to-end path: 0 (no slicing) for batches of
+    up to 1M tokens, else an eighth of the batch (at least one sequence); arg > 0 forces a
+    slice size, arg < 0 turns slicing off."""
+    if arg < 0:
+        return 0
+    if arg > 0:
+        return min(arg, shape.B)
+    return 0 if shape.B * shape.S <= (1 << 20) else max(1, shape.B // 8)
+
+
 def config_dict(shape):
     return {"workload": shape.name, "B": shape.B, "S": shape.S, "d_model": shape.d_model, "n_heads": shape.n_heads,
             "d_ff": shape.d_ff, "n_layers": shape.n_layers, "causal": shape.causal,
@@ -328,11 +408,14 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=1, help="index into the workload table (default: B64 S1024)")
+    ap.add_argument("--workload", type=int, default=4,
+                    help="index into the workload table (default: B32 S100000, the largest)")
     ap.add_argument("--shape", default="", help="B,S,D,H,F,L,causal[,len_lo,len_hi]: a custom (profiling) shape")
     ap.add_argument("--clocks-csv", default="", help="where to keep the nvidia-smi clock samples")
     ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference/oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-slice", type=int, default=0,
+                    help="sequences per slice of the streamed e2e path (0: automatic, <0: off)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -346,6 +429,7 @@ def main():
     from attention_qkv_gemm_gb300 import build as libbuild
 
     torch.cuda.set_device(local)
+    n_sms = torch.cuda.get_device_properties(local).multi_processor_count
     if rank == 0 or world == 1:
         libbuild.build()
     pg = None
@@ -420,7 +504,7 @@ def main():
     if dom == "attention":
         exps = alg["attn_exps_per_launch"]
         fl = alg["attn_flops_per_launch"]
-        mufu_peak = MUFU_PER_CLK_PER_SM * 152 * peaks["sm_max_mhz"] * 1e6 / 1e9
+        mufu_peak = MUFU_PER_CLK_PER_SM * n_sms * peaks["sm_max_mhz"] * 1e6 / 1e9
         mufu = exps / (dom_ms_launch / 1e3) / 1e9
         tflops = fl / (dom_ms_launch / 1e3) / 1e12
         # the unit that bounds the launch at peak: one exp2 per allowed (query, key) pair and
@@ -432,8 +516,25 @@ def main():
             roof = {"kernel": "attention", "bound": "tensor", "achieved": tflops, "peak": tc_peak,
                     "unit": "TFLOP/s", "frac": tflops / tc_peak, "mufu_gexp2_s": mufu, "mufu_frac": mufu / mufu_peak}
         roof["traffic"] = ncu_traffic("attention", shape.name)
-        roof["note"] = ("MUFU ex2 rate: 32/clk/SM (measured) x 152 SMs x max SM clock; per launch = allowed "
+        roof["note"] = (f"MUFU ex2 rate: 32/clk/SM (measured) x {n_sms} SMs x max SM clock; per launch = allowed "
                         "(query, key) pairs x heads; tensor = 4 x head_dim FLOPs per allowed pair and head")
+    elif dom == "stack":
+        # the whole forward in one launch: algorithmic FLOPs against the dense tensor peak, and
+        # the split-operand MMAs it executes; HBM moves only x, the output and the weights
+        fl = alg["linear_flops"] + alg["attn_flops"]
+        achieved = fl / (dom_ms_launch / 1e3) / 1e12
+        ex = stack_executed_flops(shape, lens_np)
+        hb = stack_bytes(shape, alg["valid_tokens"])
+        roof = {"kernel": "stack", "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak, "traffic": ncu_traffic("stack", shape.name),
+                "algorithmic_flops_per_launch": fl,
+                "tensor_executed": {"achieved": ex / (dom_ms_launch / 1e3) / 1e12, "peak": tc_peak,
+                                    "unit": "TFLOP/s", "frac": ex / (dom_ms_launch / 1e3) / 1e12 / tc_peak,
+                                    "executed_flops_per_launch": ex},
+                "hbm": {"algorithmic_bytes_per_launch": hb, "achieved": hb / (dom_ms_launch / 1e3) / 1e9,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": hb / (dom_ms_launch / 1e3) / 1e9 / peaks["hbm_gbs"]},
+                "note": "split-fp16 operands: the executed MMAs are 2-3x the algorithmic FLOPs"}
     elif shape.d_model > 128 and gemm_flops(dom, shape, alg["valid_tokens"]) is not None:
         # d_model > 128: the projection GEMMs are dense contractions (fp16 operands, fp32
         # accumulate), measured against the dense tensor peak (fp16 = bf16 nominal rate)
@@ -450,26 +551,56 @@ def main():
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom, shape.name),
                 "algorithmic_bytes_per_launch": by}
+        if dom == "postchain":
+            # the split-operand MMAs the chain executes, against the tensor peak: the unit
+            # that binds this kernel (see profiles/postchain_B64_S1024_D128.md)
+            ex = chain_executed_flops(shape, lens_np) / shape.n_layers
+            roof["tensor_executed"] = {"achieved": ex / (dom_ms_launch / 1e3) / 1e12, "peak": tc_peak,
+                                       "unit": "TFLOP/s",
+                                       "frac": ex / (dom_ms_launch / 1e3) / 1e12 / tc_peak,
+                                       "executed_flops_per_launch": ex}
+    note = ncu_traffic_note(dom, shape.name)
+    if note and roof.get("traffic") is not None:
+        roof["traffic_note"] = note
     roof["peak_source"] = peaks["source"] + (" (sustained)" if roof["unit"] == "TFLOP/s" and tc_peak != peaks["tc_tflops"] else "")
     roof["launch_ms"] = dom_ms_launch
     roof["kernels_ms_per_forward"] = {k: round(v[0], 4) for k, v in per_kind.items()}
 
-    # ---------------- e2e through tfl_forward_host (pinned host buffers)
+    # ---------------- e2e from pinned host buffers, host<->device traffic inside the timed region
     hx = torch.from_numpy(x_np).pin_memory()
     hl = torch.from_numpy(lens_np).pin_memory()
     ho = torch.empty_like(hx).pin_memory()
+    slice_b = e2e_slice(shape, args.e2e_slice)
+    if slice_b:
+        # batch slices streamed through a handle of the slice's batch size, copies of the
+        # next and previous slices overlapping the forward of the current one
+        ms_ = pkg.TransformerStack(slice_b, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm)
+
+        def e2e_step():
+            pkg.tfl_forward_streamed(ms_.handle, hx.data_ptr(), hl.data_ptr(), shape.B, int(shape.causal),
+                                     ho.data_ptr(), sp)
+            return pkg.tfl_status(ms_.handle, sp)
+        e2e_path = f"tfl_forward_streamed, slices of {slice_b} sequences"
+    else:
+        ms_ = None
+
+        def e2e_step():
+            return pkg.tfl_forward_host(m.handle, hx.data_ptr(), hl.data_ptr(), int(shape.causal), ho.data_ptr(), sp)
+        e2e_path = "tfl_forward_host (kernels read x and write out across the host link)"
     for _ in range(2):
-        pkg.tfl_forward_host(m.handle, hx.data_ptr(), hl.data_ptr(), int(shape.causal), ho.data_ptr(), sp)
+        e2e_step()
     e2e_t = []
     for _ in range(max(3, min(args.steps, 10))):
         t0 = time.perf_counter()
-        rc2 = pkg.tfl_forward_host(m.handle, hx.data_ptr(), hl.data_ptr(), int(shape.causal), ho.data_ptr(), sp)
+        rc2 = e2e_step()
         e2e_t.append(time.perf_counter() - t0)
         if rc2 != 0:
             raise RuntimeError(f"e2e status {rc2}")
+    if ms_ is not None:
+        ms_.close()
     e2e_s = max_over_ranks(statistics.mean(e2e_t), pg, dev)
     e2e = {"value": job_value(world, tokens, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": int(hx.numel() * 4 + hl.numel() * 4),
-           "d2h_bytes_per_step": int(ho.numel() * 4)}
+           "d2h_bytes_per_step": int(ho.numel() * 4), "path": e2e_path, "ms_per_step": e2e_s * 1e3}
 
     launches = pkg.tfl_launch_count(m.handle, int(shape.causal)) * args.steps
     m.close()
@@ -490,7 +621,7 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        n_seq = min(shape.B, args.ref_seqs if oracle_rows(shape) is None else 1)
+        n_seq = min(shape.B, args.ref_seqs)
         dt, tok = run_oracle_sample(shape, prm, seed, n_seq)
         cpu = {"value": tok / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": oracle_sample_text(shape, n_seq, tok)}

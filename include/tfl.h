@@ -99,6 +99,9 @@ typedef struct {
     int64_t wait_timeout_ns;      /* bound on every device-side wait, default 2e9 */
     int64_t max_workspace_bytes;  /* 0 = unlimited */
     int32_t use_graph;            /* 1 (default): replay the forward as one CUDA graph */
+    int32_t whole_stack;          /* 1 (default): run every layer in one kernel where the
+                                     shape allows it (d_model 128, head_dim 32, S <= 128,
+                                     precision 2, d_ff <= 2048, n_layers <= 8); 0: per-layer kernels */
 } tfl_options;
 
 /* Fill *opt with the defaults above.  Returns TFL_OK or TFL_ERR_INVALID_ARG. */
@@ -166,6 +169,34 @@ int tfl_forward_host(tfl_handle* h, const float* x_host, const int32_t* lengths_
                      int causal, float* out_host, tfl_stream stream);
 
 /*
+ * The forward of a batch held in host memory, streamed through the device in
+ * slices of the handle's batch size B ("Shape-specialized Transformer
+ * Inference on Commodity GPUs", How we built it: the S = 100000 case runs with
+ * its input in host RAM, batch slices streaming through the device and the
+ * outputs streaming back; its stream loop ran copies and compute one after
+ * the other, here they overlap).
+ *   x_host:       pinned host float32 [n_seq, S, d_model] (cudaHostAlloc /
+ *                 cudaHostRegister; pageable memory is rejected)
+ *   lengths_host: host int32 [n_seq] or NULL (every sequence has length S);
+ *                 read during the call; a value outside [0, S] is rejected
+ *   n_seq:        any number >= 1 of sequences; the last slice may be partial
+ *   out_host:     pinned host float32 [n_seq, S, d_model], written in full
+ *                 (padded rows = 0); must not overlap x_host
+ * Slice k (sequences k*B .. k*B+B-1) is copied in while slice k-1 computes and
+ * slice k-2's output is copied back, through two device buffers each for x
+ * and out, so the device holds B sequences' workspace and four slice buffers
+ * whatever n_seq is.  Asynchronous on `stream` (its earlier work runs first;
+ * its later work waits for the whole batch); synchronize or call tfl_status
+ * before reading out_host.  Allocates its device buffers (and a pinned
+ * lengths staging area) on the first call, and again when n_seq grows; a call
+ * first waits for the previous streamed call of the handle to finish with that
+ * staging area.  Errors: INVALID_ARG, OOM, CUDA; device-side errors surface
+ * via tfl_status.
+ */
+int tfl_forward_streamed(tfl_handle* h, const float* x_host, const int32_t* lengths_host, int64_t n_seq,
+                         int causal, float* out_host, tfl_stream stream);
+
+/*
  * Synchronize `stream` and read (then clear) the device status word.
  * Returns TFL_OK, TFL_ERR_DEVICE_TIMEOUT or TFL_ERR_BAD_LENGTHS (timeout
  * wins), or TFL_ERR_CUDA.
@@ -191,6 +222,7 @@ const char* tfl_last_error(void);
 #define TFL_KIND_GEMM_FFN1 5
 #define TFL_KIND_GEMM_FFN2 6
 #define TFL_KIND_POSTCHAIN 7   /* d_model 128: o_proj .. FFN-out .. next LayerNorm fused */
+#define TFL_KIND_STACK     8   /* whole_stack: every layer of the forward in one kernel */
 int tfl_profile_forward(tfl_handle* h, const float* x, const int32_t* lengths,
                         int causal, float* out, tfl_stream stream,
                         float* kernel_ms, int32_t* kernel_kind, int32_t cap, int32_t* n);
@@ -236,18 +268,23 @@ int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream);
  * output, FFN activations, attention work counters -- lives in one fixed
  * device array inside the library, TFL_NOALLOC_SCRATCH_BYTES (32 MiB) on each
  * GPU that loads the library, held until the process exits.  A shape whose
- * intermediates do not fit (tfl_workspace_bytes(shape) at the handle's
- * precision > 32 MiB, e.g. more than roughly 7000 tokens at d_model 128) is
- * rejected with TFL_ERR_UNSUPPORTED and a message naming both sizes.
+ * intermediates do not fit is rejected with TFL_ERR_UNSUPPORTED and a message
+ * naming both sizes.  The intermediates take the handle's workspace layout:
+ * per token 4 d_model (residual) + 2 d_model (normed rows) + 6 d_model (q, k, v)
+ * + 2 d_model (attention output) + 2 d_ff (FFN activations) bytes, plus 2
+ * d_model + 2 d_ff more at precision 2 (the lo planes), plus a few KiB; at
+ * d_model 128, d_ff 512, precision 2 that is 4 KiB per token, so at most about
+ * 8190 tokens (B * S) fit.  tfl_workspace_bytes(shape) gives that size at
+ * precision 2.
  *
  * The first call on a device looks up the array's device address (one
  * cudaGetSymbolAddress with that device current); make that first call before
  * any stream capture.  All calls, on every handle and stream of a device,
  * share the array and it keeps the last call's contents: calls that overlap
  * on the GPU race and corrupt each other, so serialize them (one stream, or
- * events).  The work counters that must start at zero are cleared by each
- * call on `stream`.  The handle is used only on the host during the call (not
- * thread-safe with other calls on the same handle).
+ * events).  Each call clears the part of the array it uses (a memset on
+ * `stream`) before its kernels run.  The handle is used only on the host
+ * during the call (not thread-safe with other calls on the same handle).
  */
 #define TFL_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths,

@@ -4,6 +4,7 @@
 // The attention kernel's roofline peak is this ex2 rate x SMs x SM clock.
 //
 //   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -o ex2_rate ex2_rate.cu && ./ex2_rate
+// (tests/test_gpu_ex2_rate.py builds and runs it)
 //
 // Each thread runs 8 independent dependency chains; one CTA per SM; the
 // clock64 interval around the loop gives the rate.

@@ -44,6 +44,7 @@ def test_default_options(lib):
     o = pkg.tfl_default_options()
     assert o.precision == 2 and abs(o.ln_eps - 1e-5) < 1e-12
     assert o.wait_timeout_ns == 2_000_000_000 and o.use_graph == 1 and o.max_workspace_bytes == 0
+    assert o.whole_stack == 1
 
 
 def test_workspace_bytes(lib):

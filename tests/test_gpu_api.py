@@ -88,10 +88,13 @@ def test_forward_host_matches_device_path(D):
 def test_profile_forward_reports_every_launch():
     import torch
     import attention_qkv_gemm_gb300 as pkg
-    for D, H in ((128, 4), (256, 4)):
+    for D, H, whole in ((128, 4, 0), (256, 4, 1), (128, 4, 1)):
         shape = synth.Shape(1, 128, D, H, 256, 2, True)
         prm = synth.params(5, shape)
-        m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm)
+        o = pkg.tfl_default_options()
+        o.whole_stack = whole
+        m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm,
+                                 options=o)
         try:
             x = torch.from_numpy(synth.input_x(5, shape)).cuda()
             out = torch.empty_like(x)
@@ -100,10 +103,13 @@ def test_profile_forward_reports_every_launch():
             kinds = [k for k, _ in prof]
             # every launch except the length check is timed
             assert len(kinds) == pkg.tfl_launch_count(m.handle, 1) - 1
+            assert all(ms > 0 for _, ms in prof)
+            if D == 128 and whole:  # S <= 128, head_dim 32: every layer in one kernel
+                assert kinds == ["stack"]
+                continue
             assert kinds.count("attention") == 2
             # at d_model 128 the fused chain computes layer 1's QKV projection itself
             assert kinds.count("gemm_qkv") == (1 if D == 128 else 2)
-            assert all(ms > 0 for _, ms in prof)
         finally:
             m.close()
 
@@ -114,3 +120,4 @@ def test_gelu_matches_erff_gelu():
     # plus the rounding of the MUFU reciprocal / exponential and of erff itself
     d = pkg.tfl_selftest_gelu(1 << 20)
     assert d < 2e-6, d
+
