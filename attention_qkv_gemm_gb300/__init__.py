@@ -31,6 +31,7 @@ KIND_NAMES = {1: "rownorm", 2: "gemm_qkv", 3: "attention", 4: "gemm_oproj", 5: "
 
 EXPORTS = ("tfl_default_options", "tfl_workspace_bytes", "tfl_create", "tfl_forward", "tfl_forward_bf16",
            "tfl_forward_host", "tfl_forward_streamed",
+           "tfl_attn_create", "tfl_attn_forward", "tfl_attn_backward", "tfl_attn_status", "tfl_attn_destroy",
            "tfl_status", "tfl_destroy", "tfl_last_error", "tfl_profile_forward", "tfl_launch_count",
            "tfl_probe_wait_timeout", "tfl_forward_noalloc", "tfl_selftest_gelu")
 
@@ -99,6 +100,16 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.tfl_forward_host.restype = ctypes.c_int
     lib.tfl_forward_streamed.argtypes = [vp, vp, vp, i64, ctypes.c_int, vp, vp]
     lib.tfl_forward_streamed.restype = ctypes.c_int
+    lib.tfl_attn_create.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp)]
+    lib.tfl_attn_create.restype = ctypes.c_int
+    lib.tfl_attn_forward.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp]
+    lib.tfl_attn_forward.restype = ctypes.c_int
+    lib.tfl_attn_backward.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.tfl_attn_backward.restype = ctypes.c_int
+    lib.tfl_attn_status.argtypes = [vp, vp]
+    lib.tfl_attn_status.restype = ctypes.c_int
+    lib.tfl_attn_destroy.argtypes = [vp]
+    lib.tfl_attn_destroy.restype = None
     lib.tfl_status.argtypes = [vp, vp]
     lib.tfl_status.restype = ctypes.c_int
     lib.tfl_destroy.argtypes = [vp]
@@ -179,6 +190,31 @@ def tfl_forward_streamed(handle: int, x: int, lengths: Optional[int], n_seq: int
     """n_seq sequences from pinned host x to pinned host out, streamed through the handle in
     slices of its batch size (asynchronous on ``stream``)."""
     _check(load().tfl_forward_streamed(handle, x, lengths, int(n_seq), int(causal), out, stream))
+
+
+def tfl_attn_create(B: int, S: int, n_heads: int, head_dim: int) -> int:
+    h = ctypes.c_void_p()
+    _check(load().tfl_attn_create(int(B), int(S), int(n_heads), int(head_dim), ctypes.byref(h)))
+    return h.value
+
+
+def tfl_attn_forward(handle: int, qkv: int, lengths: Optional[int], causal: int, o: int, lse: int,
+                     stream: int = 0) -> None:
+    _check(load().tfl_attn_forward(handle, qkv, lengths, int(causal), o, lse, stream))
+
+
+def tfl_attn_backward(handle: int, qkv: int, o: int, dout: int, lse: int, lengths: Optional[int], causal: int,
+                      dqkv: int, stream: int = 0) -> None:
+    _check(load().tfl_attn_backward(handle, qkv, o, dout, lse, lengths, int(causal), dqkv, stream))
+
+
+def tfl_attn_status(handle: int, stream: int = 0) -> int:
+    return load().tfl_attn_status(handle, stream)
+
+
+def tfl_attn_destroy(handle: int) -> None:
+    if handle:
+        load().tfl_attn_destroy(handle)
 
 
 def tfl_status(handle: int, stream: int = 0) -> int:

@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["gemm.cu", "attention.cu", "postchain.cu", "stack.cu", "rows.cu", "api.cu"]
+SOURCES = ["gemm.cu", "attention.cu", "attention_bwd.cu", "postchain.cu", "stack.cu", "rows.cu", "api.cu"]
 
 
 def _nvcc() -> str:

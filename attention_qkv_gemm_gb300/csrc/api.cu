@@ -1282,3 +1282,148 @@ int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Attention on its own (forward with the row log-sum-exp, backward).
+struct tfl_attn {
+  int B = 0, S = 0, H = 0, hd = 0;
+  int device = 0, num_sms = 0;
+  int* scratch = nullptr;  // [0] status word, [1] work counter (256 bytes), then delta
+  float* delta = nullptr;  // [B, H, S]
+  int64_t timeout_ns = 2000000000LL;
+};
+
+extern "C" {
+
+int tfl_attn_create(int32_t B, int32_t S, int32_t n_heads, int32_t head_dim, tfl_attn** out) {
+  g_err.clear();
+  if (!out) return fail(TFL_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (B < 1 || S < 1 || n_heads < 1) return fail(TFL_ERR_INVALID_ARG, "B, S and n_heads must be >= 1");
+  if (head_dim != 32 && head_dim != 64) return fail(TFL_ERR_UNSUPPORTED, "head_dim must be 32 or 64");
+  if ((int64_t)B * S * 3 * n_heads * head_dim >= ((int64_t)1 << 31))
+    return fail(TFL_ERR_UNSUPPORTED, "B * S * 3 * n_heads * head_dim must be < 2^31");
+  int dev = 0;
+  TFL_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  cudaDeviceProp prop;
+  TFL_CUDA(cudaGetDeviceProperties(&prop, dev), "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(TFL_ERR_UNSUPPORTED, "device is sm_" + std::to_string(prop.major) + std::to_string(prop.minor) +
+                                         "; this library is built for sm_103a (GB300)");
+  if (!get_encode()) return fail(TFL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  TFL_CUDA(prepare_attention_kernels(), "attention kernel attributes");
+  TFL_CUDA(prepare_attention_bwd_kernels(), "attention backward kernel attributes");
+  tfl_attn* a = new tfl_attn();
+  a->B = B;
+  a->S = S;
+  a->H = n_heads;
+  a->hd = head_dim;
+  a->device = dev;
+  a->num_sms = prop.multiProcessorCount;
+  const size_t bytes = 256 + (size_t)B * n_heads * S * sizeof(float);
+  if (cudaMalloc(&a->scratch, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete a;
+    return fail(TFL_ERR_OOM, "attention scratch allocation failed");
+  }
+  a->delta = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a->scratch) + 256);
+  if (cudaMemset(a->scratch, 0, 256) != cudaSuccess) {
+    cudaFree(a->scratch);
+    delete a;
+    return fail(TFL_ERR_CUDA, "attention scratch clear failed");
+  }
+  *out = a;
+  return TFL_OK;
+}
+
+int tfl_attn_forward(tfl_attn* a, const void* qkv, const int32_t* lengths, int causal, void* o, float* lse,
+                     tfl_stream stream) {
+  g_err.clear();
+  if (!a) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (!qkv || !o || !lse) return fail(TFL_ERR_INVALID_ARG, "qkv, o and lse must be non-NULL device pointers");
+  if (causal != 0 && causal != 1) return fail(TFL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(lse)) & 15)
+    return fail(TFL_ERR_INVALID_ARG, "qkv, o and lse must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int D = a->H * a->hd, atom = a->hd < 64 ? a->hd : 64;
+  CUtensorMap tq, tkv;
+  if (!make_map_qkv(&tq, qkv, a->B, a->S, 3 * D, atom, kAttnBM) ||
+      !make_map_qkv(&tkv, qkv, a->B, a->S, 3 * D, atom, attn_block_n(a->hd)))
+    return fail(TFL_ERR_CUDA, "attention tensor map encoding failed");
+  TFL_CUDA(cudaMemsetAsync(a->scratch + 1, 0, sizeof(int), st), "work counter reset");
+  AttnArgs args;
+  args.c.M = a->B * a->S;
+  args.c.S = a->S;
+  args.c.lengths = lengths;
+  args.c.status = a->scratch;
+  args.c.timeout_ns = a->timeout_ns;
+  args.B = a->B;
+  args.H = a->H;
+  args.D = D;
+  args.causal = causal;
+  args.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a->hd));
+  args.o16 = static_cast<__half*>(o);
+  args.counter = a->scratch + 1;
+  const double fit = 48.0 * 1024 * 1024 / (4.0 * (double)a->S * a->hd);
+  args.group = fit >= (double)a->B * a->H ? 0 : (fit < 1.0 ? 1 : (int)fit);
+  args.lse = lse;
+  TFL_CUDA(launch_prepare(lengths, a->B, a->S, a->B * a->S, a->scratch, nullptr, st), "length check");
+  TFL_CUDA(launch_attention(a->hd, tq, tkv, args, a->num_sms, st), "attention");
+  return TFL_OK;
+}
+
+int tfl_attn_backward(tfl_attn* a, const void* qkv, const void* o, const void* dout, const float* lse,
+                      const int32_t* lengths, int causal, float* dqkv, tfl_stream stream) {
+  g_err.clear();
+  if (!a) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  if (!qkv || !o || !dout || !lse || !dqkv) return fail(TFL_ERR_INVALID_ARG, "NULL device pointer");
+  if (causal != 0 && causal != 1) return fail(TFL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) |
+       reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(dqkv)) & 15)
+    return fail(TFL_ERR_INVALID_ARG, "all buffers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int D = a->H * a->hd;
+  CUtensorMap tqkv, tdo;
+  if (!make_map_qkv(&tqkv, qkv, a->B, a->S, 3 * D, a->hd, 64) || !make_map_qkv(&tdo, dout, a->B, a->S, D, a->hd, 64))
+    return fail(TFL_ERR_CUDA, "attention backward tensor map encoding failed");
+  TFL_CUDA(cudaMemsetAsync(dqkv, 0, (size_t)a->B * a->S * 3 * D * sizeof(float), st), "dqkv clear");
+  AttnBwdArgs args;
+  args.c.M = a->B * a->S;
+  args.c.S = a->S;
+  args.c.lengths = lengths;
+  args.c.status = a->scratch;
+  args.c.timeout_ns = a->timeout_ns;
+  args.B = a->B;
+  args.H = a->H;
+  args.causal = causal;
+  args.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a->hd));
+  args.inv_sqrt_hd = (float)(1.0 / std::sqrt((double)a->hd));
+  args.lse = lse;
+  args.delta = a->delta;
+  args.dqkv = dqkv;
+  TFL_CUDA(launch_prepare(lengths, a->B, a->S, a->B * a->S, a->scratch, nullptr, st), "length check");
+  TFL_CUDA(launch_attention_bwd(a->hd, tqkv, tdo, args, static_cast<const __half*>(dout),
+                                static_cast<const __half*>(o), a->num_sms, st),
+           "attention backward");
+  return TFL_OK;
+}
+
+int tfl_attn_status(tfl_attn* a, tfl_stream stream) {
+  if (!a) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
+  TFL_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
+  int v = 0;
+  TFL_CUDA(cudaMemcpy(&v, a->scratch, sizeof(int), cudaMemcpyDeviceToHost), "status read");
+  if (v) TFL_CUDA(cudaMemset(a->scratch, 0, sizeof(int)), "status clear");
+  if (v & TFL_DEV_TIMEOUT) return fail(TFL_ERR_DEVICE_TIMEOUT, "a device-side wait ran out of time");
+  if (v & TFL_DEV_BAD_LENGTHS) return fail(TFL_ERR_BAD_LENGTHS, "a length was outside [0, S] and was clamped");
+  return TFL_OK;
+}
+
+void tfl_attn_destroy(tfl_attn* a) {
+  if (!a) return;
+  cudaDeviceSynchronize();
+  if (a->scratch) cudaFree(a->scratch);
+  delete a;
+}
+
+}  // extern "C"

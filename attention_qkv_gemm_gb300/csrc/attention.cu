@@ -532,6 +532,9 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       oph ^= 1u;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      // the row's log-sum-exp for a backward pass: log2 sum_j 2^(s_j log2(e)/sqrt(hd)) = m + log2 l
+      if (args.lse != nullptr && qpos < it.len)
+        args.lse[((size_t)it.b * args.H + it.h) * S + qpos] = m_run + __log2f(l_run);
       const int q0 = it.qb * kAttnBM + q * 32;  // first query row of this warp
       const uint32_t rows = __ballot_sync(0xffffffffu, qpos < S);
       __half* orow0 = args.o16 + ((size_t)it.b * S + q0) * D + it.h * HD;

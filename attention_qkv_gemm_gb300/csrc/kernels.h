@@ -80,7 +80,23 @@ struct AttnArgs {
   __half* o16 = nullptr;         // [M, D]
   int* counter = nullptr;        // work-item counter, zero before the launch
   int group = 0;                 // (b, h) pairs per work-order group (see decode_item); 0: one group
+  float* lse = nullptr;          // [B, H, S] row log-sum-exp in log2 units (rows < len_b), or null
 };
+
+// Attention backward (head_dim 32 or 64): qkv [B, S, 3 H hd] fp16, dO [B, S, H hd] fp16.
+struct AttnBwdArgs {
+  Common c;
+  int B = 0, H = 0, causal = 0;
+  float scale_log2 = 0.f;        // log2(e) / sqrt(head_dim)
+  float inv_sqrt_hd = 0.f;
+  const float* lse = nullptr;    // [B, H, S] from the forward, log2 units
+  float* delta = nullptr;        // [B, H, S] dO_i . O_i, written by the first kernel
+  float* dqkv = nullptr;         // [B, S, 3 H hd] fp32; rows past len_b are left untouched
+};
+cudaError_t prepare_attention_bwd_kernels();
+// D = rowsum(dO O), then the dQ kernel and the dK / dV kernel.
+cudaError_t launch_attention_bwd(int hd, const CUtensorMap& tqkv, const CUtensorMap& tdo, const AttnBwdArgs& a,
+                                 const __half* dout, const __half* o, int num_sms, cudaStream_t s);
 
 struct RowArgs {
   Common c;
@@ -196,7 +212,7 @@ cudaError_t launch_attention(int hd, const CUtensorMap& tq, const CUtensorMap& t
 cudaError_t launch_rows(const RowArgs& a, cudaStream_t s);
 cudaError_t launch_postchain(const ChainMaps& mp, const ChainArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_gelu_selftest(int n, unsigned* out, cudaStream_t s);
-// Checks the lengths (TFL_DEV_BAD_LENGTHS) and writes the tile list of Common::tiles.
+// Checks the lengths (TFL_DEV_BAD_LENGTHS) and writes the tile list of Common::tiles (tiles may be null).
 cudaError_t launch_prepare(const int* lengths, int B, int S, int M, int* status, int* tiles, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, size_t n, cudaStream_t s);
 cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_t s);

@@ -50,24 +50,23 @@
 #include "ptx.cuh"
 #include "mathfn.cuh"
 #include "xpose.cuh"
+#include "chainops.cuh"
 
 namespace tfl {
 
 namespace {
 
-constexpr int kD = 128;
+using namespace chain;  // kD, kEpi, kParts, kRedBytes and the row operations
+
 constexpr int kFC = 128;            // d_ff chunk
 constexpr int kUnit = 64 * 1024;    // one ring unit: a 128 x 128 weight block, hi + lo planes
 constexpr int kHalf = 16 * 1024;    // one 64-column (K) half of a plane: 128 rows x 128 B
 constexpr int kRing = 2;
-constexpr int kEpi = 16;           // epilogue warps: four per TMEM lane quarter
-constexpr int kParts = 4;           // each owns 32 of a row's 128 columns
 constexpr int kFfn1Warp = 2 + kEpi;  // the FFN-in MMA issuer (scheduler 2; o_proj / FFN-out issue from warp 1)
 constexpr int kThreads = 32 * (kFfn1Warp + 1);
 constexpr int kOBytes = kGemmBM * kD * 2;
 constexpr int kXpWarp = 2048;       // per-warp transpose stage: 32 rows x 64 B
 constexpr int kXpBytes = kEpi * kXpWarp;
-constexpr int kRedBytes = 4 * kParts * kGemmBM * 4;
 // parameter vectors staged in shared memory once per CTA (floats):
 // bo, b2, ln1 g/b, ln2 g/b, next-layer ln1 g/b, final ln g/b (128 each), then b1 (d_ff <= kMaxF)
 constexpr int kMaxF = 2048;
@@ -78,105 +77,6 @@ constexpr int kParamBytes = (kPBqkv + 3 * kD) * 4;
 constexpr size_t kSmem = 1024 + kOBytes + (size_t)kRing * kUnit + kXpBytes + kRedBytes + kParamBytes + 512;
 
 constexpr uint32_t kColA1 = 0, kColN2 = 128, kColG = 256, kColGP = 384;  // GP: hi [384,448), lo [448,512)
-
-__device__ __forceinline__ void chain_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpi) : "memory"); }
-
-// Row mean / rstd of a 128-wide row split over four warps (32 values each).
-// Sums run as four packed pairs (eight partial sums) to keep the dependent
-// chains short; slots alternate so a fast warp never overwrites partial sums
-// a slow one still reads.
-__device__ __forceinline__ void stats32(const float* t, float eps, float* red, int slot, int part, int r,
-                                        float& mean, float& rstd) {
-  // This warp's 32 values: their sum and their sum of squares about their own mean;
-  // the four partial results of a row then combine in one exchange (Chan, Golub and
-  // LeVeque's pairwise update: M2 = sum M2_p + 32 sum (mean_p - mean)^2).
-  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i & 3] = f2_add(acc[i & 3], f2_pack(t[2 * i], t[2 * i + 1]));
-  float s0, s1;
-  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
-  const float sp = s0 + s1;
-  const uint64_t mp2 = f2_splat(sp * (1.0f / 32));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = 0ull;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint64_t d = f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), mp2);
-    acc[i & 3] = f2_fma(d, d, acc[i & 3]);
-  }
-  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
-  float* rs = red + slot * kParts * kGemmBM + r;
-  float* rq = rs + kParts * kGemmBM;
-  rs[part * kGemmBM] = sp;
-  rq[part * kGemmBM] = s0 + s1;
-  chain_bar();
-  const float a0 = rs[0], a1 = rs[kGemmBM], a2 = rs[2 * kGemmBM], a3 = rs[3 * kGemmBM];
-  mean = ((a0 + a1) + (a2 + a3)) * (1.0f / kD);
-  const float d0 = a0 * (1.0f / 32) - mean, d1 = a1 * (1.0f / 32) - mean, d2 = a2 * (1.0f / 32) - mean,
-              d3 = a3 * (1.0f / 32) - mean;
-  const float m2 = ((rq[0] + rq[kGemmBM]) + (rq[2 * kGemmBM] + rq[3 * kGemmBM])) +
-                   32.0f * ((d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3));
-  rstd = rsqrtf(m2 * (1.0f / kD) + eps);
-}
-
-// (t - mean) * rstd * g + b for 32 values in place; g, b: this warp's 32 columns in shared memory.
-__device__ __forceinline__ void normalize32(float* t, float mean, float rstd, const float* g, const float* b) {
-  const uint64_t m2 = f2_splat(mean), r2 = f2_splat(rstd);
-  const float2* g2 = reinterpret_cast<const float2*>(g);
-  const float2* b2 = reinterpret_cast<const float2*>(b);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 gg = g2[i], bb = b2[i];
-    const uint64_t y = f2_fma(f2_mul(f2_sub(f2_pack(t[2 * i], t[2 * i + 1]), m2), r2), f2_pack(gg.x, gg.y),
-                              f2_pack(bb.x, bb.y));
-    f2_unpack(y, t[2 * i], t[2 * i + 1]);
-  }
-}
-
-// LayerNorm of a row split over four warps; g, b: shared-memory gamma / beta of the whole row.
-__device__ __forceinline__ void layer_norm32(float* t, float eps, const float* g, const float* b, int c0,
-                                             float* red, int& slot, int part, int r) {
-  float mean, rstd;
-  stats32(t, eps, red, slot, part, r, mean, rstd);
-  slot = (slot + 2) & 3;
-  normalize32(t, mean, rstd, g + c0, b + c0);
-}
-
-// v[i] = v[i] * scale + p[i] for 32 values, p in shared memory.
-__device__ __forceinline__ void scale_bias32(float* v, float scale, const float* p) {
-  const float2* p2 = reinterpret_cast<const float2*>(p);
-  const uint64_t s2 = f2_splat(scale);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 q = p2[i];
-    f2_unpack(f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), s2, f2_pack(q.x, q.y)), v[2 * i], v[2 * i + 1]);
-  }
-}
-
-// fp16 hi/lo pairs of v[i] - c for 16 values (the row's mean taken out before the split).
-__device__ __forceinline__ void split_centered_pairs16(const float* v, float c, uint32_t* hi, uint32_t* lo) {
-  const uint64_t c2 = f2_splat(c);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint64_t x = f2_sub(f2_pack(v[2 * i], v[2 * i + 1]), c2);
-    float x0, x1;
-    f2_unpack(x, x0, x1);
-    const __half2 h = __floats2half2_rn(x0, x1);
-    const float2 hf = __half22float2(h);
-    float l0, l1;
-    f2_unpack(f2_sub(x, f2_pack(hf.x, hf.y)), l0, l1);
-    const __half2 l = __floats2half2_rn(l0, l1);
-    hi[i] = *reinterpret_cast<const uint32_t*>(&h);
-    lo[i] = *reinterpret_cast<const uint32_t*>(&l);
-  }
-}
-
-__device__ __forceinline__ void tmem_st8_u(uint32_t taddr, const uint32_t* r) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
-
 
 }  // namespace
 
@@ -624,19 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           slot = (slot + 2) & 3;
           a1 = rstd * args.scale_1;
         }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t hi[8], lo[8];
-          split_centered_pairs16(tv + 16 * j, mean, hi, lo);
-          tmem_st8_u(tq + kColN2 + part * 16 + 8 * j, hi);
-          tmem_st8_u(tq + kColN2 + 64 + part * 16 + 8 * j, lo);
-        }
+        store_split_operand(tq + kColN2, tv, mean, part);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_read);
       }
-      const uint64_t a1x2 = f2_splat(a1);
       // pull the next tile's residual rows into L2 while this tile's FFN runs
       if (ti + (int)gridDim.x < n_live) {
         const int mn = t_next * kGemmBM + q * 32 + lane;
@@ -658,24 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(g_read);
         const int f0 = ((c + t) % nch) * kFC + c0;
-        const float2* b1 = reinterpret_cast<const float2*>(prm + kPB1 + f0);
         // GELU and fp16 hi/lo split of the 32 values in registers, then into GP once
         // FFN-out of the previous chunk has read it (the GELU overlaps that MMA)
         uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 bq = b1[e];
-          const uint64_t gl = gelu2_as7126(f2_fma(f2_pack(gv[2 * e], gv[2 * e + 1]), a1x2, f2_pack(bq.x, bq.y)));
-          float g0, g1;
-          f2_unpack(gl, g0, g1);
-          const __half2 h = __floats2half2_rn(g0, g1);  // first value in the low half
-          const float2 hf = __half22float2(h);
-          float l0, l1;
-          f2_unpack(f2_sub(gl, f2_pack(hf.x, hf.y)), l0, l1);
-          const __half2 l = __floats2half2_rn(l0, l1);
-          hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-          lo[e] = *reinterpret_cast<const uint32_t*>(&l);
-        }
+        gelu_split32(gv, a1, prm + kPB1 + f0, hi, lo);
         if (gp_written) {  // GP is free once FFN-out of the previous chunk has read it
           if (!wait_bounded(gp_free, gffph, ewc)) {
             ok = false;

@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(1024) prepare_kernel(const int* lengths, int B
       bad |= (l < 0) || (l > S);
     }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, TFL_DEV_BAD_LENGTHS);
+  if (tiles == nullptr) return;  // the length check only (the same for every thread)
 
   const int num_m = (M + kGemmBM - 1) / kGemmBM;
   const int per = (num_m + blockDim.x - 1) / blockDim.x;

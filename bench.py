@@ -402,6 +402,68 @@ def config_dict(shape):
             "l2": "flushed (256 MiB write) between timed steps", "seed": 0}
 
 
+def attention_backward_bench(args):
+    """Standalone attention (tfl_attn_forward / tfl_attn_backward) on random fp16 q, k, v and
+    dO of the given shape: CUDA-event time of each, against the dense tensor peak.
+    Algorithmic FLOPs per allowed (query, key) pair and head: forward 4 hd (Q K^T, P V),
+    backward 10 hd (Q K^T rebuilt, dO V^T, P^T dO, dS K, dS^T Q)."""
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    from attention_qkv_gemm_gb300 import build as libbuild
+    B, S, H, hd, causal = [int(v) for v in args.attn_bwd.split(",")]
+    libbuild.build()
+    pkg.load()
+    D = H * hd
+    g = torch.Generator(device="cuda").manual_seed(0)
+    qkv = torch.randn(B, S, 3 * D, device="cuda", generator=g).half()
+    dout = torch.randn(B, S, D, device="cuda", generator=g).half()
+    o = torch.empty(B, S, D, device="cuda", dtype=torch.float16)
+    lse = torch.empty(B, H, S, device="cuda", dtype=torch.float32)
+    dqkv = torch.empty(B, S, 3 * D, device="cuda", dtype=torch.float32)
+    a = pkg.tfl_attn_create(B, S, H, hd)
+    st = torch.cuda.current_stream()
+    sp = st.cuda_stream
+    fwd = lambda: pkg.tfl_attn_forward(a, qkv.data_ptr(), None, causal, o.data_ptr(), lse.data_ptr(), sp)
+    bwd = lambda: pkg.tfl_attn_backward(a, qkv.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(), None,
+                                        causal, dqkv.data_ptr(), sp)
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    if pkg.tfl_attn_status(a, sp) != 0:
+        raise RuntimeError(pkg.tfl_last_error())
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for e in ev:
+        e[0].record(st)
+        fwd()
+        e[1].record(st)
+        bwd()
+        e[2].record(st)
+    torch.cuda.synchronize()
+    if pkg.tfl_attn_status(a, sp) != 0:
+        raise RuntimeError(pkg.tfl_last_error())
+    pkg.tfl_attn_destroy(a)
+    f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    pairs = B * (S * (S + 1) / 2 if causal else S * S)
+    peaks = load_peaks()
+    ff, bf = 4.0 * hd * pairs * H, 10.0 * hd * pairs * H
+    line = {"metric": "attention_backward_tflops", "value": bf / (b_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": f_ms + b_ms,
+            "higher_is_better": True, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"attention B{B} S{S} H{H} hd{hd} " + ("causal" if causal else "full"),
+                       "B": B, "S": S, "n_heads": H, "head_dim": hd, "causal": bool(causal)},
+            "forward_ms": f_ms, "backward_ms": b_ms,
+            "roofline": {"bound": "tensor", "peak": peaks["tc_tflops"], "unit": "TFLOP/s",
+                         "forward": {"achieved": ff / (f_ms / 1e3) / 1e12,
+                                     "frac": ff / (f_ms / 1e3) / 1e12 / peaks["tc_tflops"]},
+                         "backward": {"achieved": bf / (b_ms / 1e3) / 1e12,
+                                      "frac": bf / (b_ms / 1e3) / 1e12 / peaks["tc_tflops"]},
+                         "note": "FLOPs per allowed pair and head: forward 4 hd, backward 10 hd"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -416,10 +478,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-slice", type=int, default=0,
                     help="sequences per slice of the streamed e2e path (0: automatic, <0: off)")
+    ap.add_argument("--attn-bwd", default="",
+                    help="B,S,H,head_dim,causal: time the standalone attention forward + backward instead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
     world, rank, local = dist_env()
+    if args.attn_bwd and args.impl == "ours":
+        return attention_backward_bench(args)
     shape = custom_shape(args.shape) if args.shape else workload(args.workload)
     if args.impl == "reference":
         return reference_arm(args, shape, world, rank)

@@ -290,6 +290,52 @@ int tfl_probe_wait_timeout(int64_t timeout_ns, tfl_stream stream);
 int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths,
                         int causal, float* out, tfl_stream stream);
 
+/*
+ * Attention on its own, forward and backward, for training use ("Training
+ * throughput baseline", Fused attention: the forward keeps the row
+ * log-sum-exp; the backward rebuilds the probabilities from it and takes the
+ * softmax row sum from the output gradient and the output, in one kernel per
+ * query tile (dQ) and one per key tile (dK, dV), without atomics).
+ *
+ * Per sequence b and head h (columns h*hd .. h*hd+hd-1 of q, k and v):
+ *   O = softmax(Q K^T / sqrt(hd) + mask) V, key j visible to query i iff
+ *   j < len_b and (not causal or j <= i).
+ * Layouts (device memory, row-major):
+ *   qkv   fp16 [B, S, 3 H hd]: q | k | v, as the fused QKV projection writes it;
+ *         rows at or past len_b must hold finite values (masked keys are
+ *         multiplied by a zero probability)
+ *   o     fp16 [B, S, H hd]          lse  fp32 [B, H, S], log2 units:
+ *         lse = log2 sum_j 2^(q.k_j log2(e) / sqrt(hd)) (natural LSE * log2(e))
+ *   dout  fp16 [B, S, H hd]          dqkv fp32 [B, S, 3 H hd]: dq | dk | dv
+ * Query rows at or past len_b are padding: their o and lse are unspecified,
+ * their dout is ignored, their dq is 0 and they add nothing to dk and dv.
+ * All buffers 16-byte aligned.  Asynchronous on `stream`; device-side errors
+ * (a bounded wait that ran out, a length outside [0, S]) surface through
+ * tfl_attn_status.  A handle is not thread-safe.
+ */
+typedef struct tfl_attn tfl_attn;
+
+/* head_dim 32 or 64 (the backward's range; the forward also takes 256);
+ * B, S, n_heads >= 1.  Allocates the handle's status word, work counter and
+ * the backward's row-sum scratch (B * n_heads * S floats).
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA. */
+int tfl_attn_create(int32_t B, int32_t S, int32_t n_heads, int32_t head_dim, tfl_attn** out);
+
+/* o and lse from qkv (lengths: device int32 [B] or NULL = all S). */
+int tfl_attn_forward(tfl_attn* a, const void* qkv, const int32_t* lengths, int causal, void* o, float* lse,
+                     tfl_stream stream);
+
+/* dqkv from qkv, the forward's o and lse, and dout.  dqkv is cleared first, so
+ * padding rows read 0. */
+int tfl_attn_backward(tfl_attn* a, const void* qkv, const void* o, const void* dout, const float* lse,
+                      const int32_t* lengths, int causal, float* dqkv, tfl_stream stream);
+
+/* Synchronize `stream`, read and clear the status word: TFL_OK,
+ * TFL_ERR_DEVICE_TIMEOUT or TFL_ERR_BAD_LENGTHS. */
+int tfl_attn_status(tfl_attn* a, tfl_stream stream);
+
+void tfl_attn_destroy(tfl_attn* a);
+
 #ifdef __cplusplus
 }
 #endif

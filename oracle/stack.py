@@ -176,7 +176,7 @@ def forward(params, n_heads: int, x: np.ndarray, lengths: Optional[np.ndarray], 
 
 
 def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, n_heads: int,
-                       length: int, causal: bool):
+                       length: int, causal: bool, return_intermediates: bool = False):
     """Gradients (dq, dk, dv) of the attention of ``attention`` for one sequence.
 
     The gradient of O = softmax(Q K^T / sqrt(d_k) + mask) V ("TikTok TechJam 2026 --
@@ -188,7 +188,8 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
     and the output.  Query rows at or past ``length`` are padding: their output
     gradient is ignored (taken as zero), so their dq is zero and they add nothing
     to dk and dv; keys at or past ``length`` are masked and get zero gradient.
-    q, k, v, dout: [S, D].  Returns float64 dq, dk, dv [S, D].
+    q, k, v, dout: [S, D].  Returns float64 dq, dk, dv [S, D] (and, with
+    ``return_intermediates``, the per-head P and dS, [H, S, S] each).
     """
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
@@ -205,6 +206,7 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
     dq = np.zeros((S, D))
     dk = np.zeros((S, D))
     dv = np.zeros((S, D))
+    ps, dss = [], []
     for h in range(n_heads):
         c = slice(h * hd, (h + 1) * hd)
         s = np.where(allowed, q[:, c] @ k[:, c].T / np.sqrt(hd), -np.inf)
@@ -218,6 +220,11 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
         ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
         dq[:, c] = ds @ k[:, c] / np.sqrt(hd)
         dk[:, c] = ds.T @ q[:, c] / np.sqrt(hd)
+        if return_intermediates:
+            ps.append(p)
+            dss.append(ds)
+    if return_intermediates:
+        return dq, dk, dv, np.stack(ps), np.stack(dss)
     return dq, dk, dv
 
 
@@ -240,7 +247,8 @@ def attention_lse(q: np.ndarray, k: np.ndarray, n_heads: int, length: int, causa
         m = np.max(s, axis=1)
         ok = np.isfinite(m)
         mm = np.where(ok, m, 0.0)
-        out[h] = np.where(ok, mm + np.log(np.where(allowed, np.exp(s - mm[:, None]), 0.0).sum(axis=1)), -np.inf)
+        tot = np.where(allowed, np.exp(s - mm[:, None]), 0.0).sum(axis=1)
+        out[h] = np.where(ok, mm + np.log(np.where(ok, tot, 1.0)), -np.inf)
     return out
 
 
