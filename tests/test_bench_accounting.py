@@ -79,3 +79,34 @@ def test_custom_shape_and_row_sample():
     assert rows is not None and len(rows) == bench.ORACLE_ROWS
     assert rows[0] == 0 and rows[-1] == synth.WORKLOADS[4].S - 1 and np.all(np.diff(rows) > 0)
     assert bench.oracle_rows(synth.WORKLOADS[1]) is None  # short sequences: whole sequences
+
+
+def test_live_tiles_and_chain_executed_mmas():
+    # B2 S256, lengths 256 and 1: tiles 0-1 hold sequence 0; tile 2 holds sequence 1's only
+    # valid row (and its key rows up to 64); tile 3 is all padding
+    shape = synth.Shape(2, 256, 128, 4, 512, 3, True)
+    lens = np.array([256, 1], dtype=np.int32)
+    assert bench.live_tiles(shape, lens) == 3
+    # per live tile: o_proj 16 + FFN 48 per 128-wide chunk in every launch, QKV 72 in all but the last
+    per_tile = 3 * (16 + 48 * 4) + 2 * 72
+    assert bench.chain_executed_flops(shape, lens) == pytest.approx(3 * per_tile * 2.0 * 128 * 128 * 16)
+
+
+def test_whole_stack_accounting():
+    shape = synth.Shape(3, 128, 128, 4, 384, 2, False)
+    lens = np.array([128, 0, 5], dtype=np.int32)
+    # two non-empty sequences x two layers x (QKV 72 + 4 heads x 5 + o_proj 16 + 48 per chunk)
+    per_layer = 72 + 20 + 16 + 48 * 3
+    assert bench.stack_executed_flops(shape, lens) == pytest.approx(2 * 2 * per_layer * 2.0 * 128 * 128 * 16)
+    valid = float(lens.sum())
+    weights = 2 * (4 * 128 * 128 + 2 * 128 * 384) * 2 * 2
+    assert bench.stack_bytes(shape, valid) == pytest.approx(valid * 512 + 3 * 128 * 512 + weights)
+    assert bench.forward_bytes(shape, valid) == pytest.approx(bench.stack_bytes(shape, valid))
+
+
+def test_e2e_slice_rule():
+    big, small = synth.WORKLOADS[4], synth.WORKLOADS[1]
+    assert bench.e2e_slice(big, 0) == 4          # 3.2M tokens: an eighth of the batch
+    assert bench.e2e_slice(small, 0) == 0        # 65536 tokens: no slicing
+    assert bench.e2e_slice(big, -1) == 0 and bench.e2e_slice(big, 5) == 5
+    assert bench.e2e_slice(small, 100) == small.B
