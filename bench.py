@@ -224,7 +224,8 @@ KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh", "chainops.c
 
 NCU_TRAFFIC = {
     # (kernel, workload): (kernel source fingerprint, bytes per launch)
-    ("postchain", "B64_S1024_D128_causal_ragged"): ("f6e63fb10f67", 42.612736e6 + 29.804032e6),
+    ("postchain", "B64_S1024_D128_causal_ragged"): ("048a2bf32bcb", 42.617344e6 + 29.616384e6),
+    ("stack", "B2048_S128_D128_H4_F512_L4_keymask"): ("6babbc9c1ba1", 87.52e6 + 86.017024e6),
     ("attention", "B64_S1024_D128_causal_ragged"): ("222a4a4c89a8", 41.433088e6 + 0.554752e6),
     ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("f2139ce26c7e", 27.822592e6 + 0.657664e6),
     ("gemm_qkv", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 46.189568e6 + 12.694784e6),
@@ -254,6 +255,7 @@ def csrc_fingerprint(kernel: str = None) -> str:
 # (kernel, workload): (captured workload, tokens captured, tokens of the full launch)
 NCU_TRAFFIC_SCALED = {
     ("attention", "B32_S100000_D1024_H16_causal"): ("B2_S16384_D1024_H16_F4096_L1_causal", 2 * 16384, 32 * 100000),
+    ("stack", "B10000_S128_D128_keymask_ragged"): ("B2048_S128_D128_H4_F512_L4_keymask", 2048 * 128, 10000 * 128),
 }
 
 
