@@ -345,10 +345,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
     return m;
   };
 
-  TFL_CUDA(cudaMemsetAsync(h->sched, 0, (size_t)L * sizeof(int), st), "work counter reset");
-  TFL_CUDA(launch_prepare(lengths, h->shape.B, h->shape.S, h->M, h->status, tiles, st), "preparation launch");
-
-  if (h->stack) {
+  if (h->stack) {  // one launch: the kernel checks the lengths itself and needs no tile list
     StackArgs sa;
     sa.c = c;
     sa.B = h->shape.B;
@@ -396,6 +393,9 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
     TFL_CUDA(rec_mark(rec, st, TFL_KIND_STACK), "event");
     return TFL_OK;
   }
+
+  TFL_CUDA(cudaMemsetAsync(h->sched, 0, (size_t)L * sizeof(int), st), "work counter reset");
+  TFL_CUDA(launch_prepare(lengths, h->shape.B, h->shape.S, h->M, h->status, tiles, st), "preparation launch");
 
   TFL_CUDA(rec_mark(rec, st, 0), "event");
   {
@@ -655,7 +655,7 @@ const char* tfl_last_error(void) { return g_err.c_str(); }
 int tfl_launch_count(const tfl_handle* h, int causal) {
   (void)causal;
   if (!h) return fail(TFL_ERR_INVALID_ARG, "handle is NULL");
-  if (h->stack) return 2;                           // length check, whole-stack kernel
+  if (h->stack) return 1;                           // the whole-stack kernel (it checks the lengths)
   if (chain_fuses_qkv(h)) return 2 + 1 + 2 * h->L;  // layer 0's QKV GEMM, then attention + chain per layer
   const int per_layer = use_chain(h->D, h->F, h->opt.precision) ? 3 : (h->D == 128 ? 5 : 7);
   return 2 + per_layer * h->L;

@@ -321,30 +321,43 @@ __global__ void __launch_bounds__(192, 2)
           tmem_wait_ld();
           uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p2[2], ds2[2];
+          for (int e0 = 0; e0 < 32; e0 += 8) {
+            // the 8 columns' log-sum-exp and row sums: per-thread constants for dQ (row =
+            // query), per column from the step's shared staging for dK/dV (row = key)
+            float lse8[8], d8[8];
+            if (MODE == 0) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int col = c0 + 32 * half + e + k;  // streamed position
-              float lse_c, d_c;
-              bool allowed;
-              if (MODE == 0) {  // row = query, col = key
-                allowed = row < it.len && col < it.len && (!args.causal || col <= row);
-                lse_c = lse_r;
-                d_c = d_r;
-              } else {          // row = key, col = query
-                allowed = row < it.len && col < it.len && (!args.causal || row <= col);
-                lse_c = sf[32 * half + e + k];
-                d_c = sf[64 + 32 * half + e + k];
+              for (int k = 0; k < 8; ++k) {
+                lse8[k] = lse_r;
+                d8[k] = d_r;
               }
-              const float p = allowed ? ex2(fmaf(sv[e + k], sl2, -lse_c)) : 0.f;
-              p2[k] = p;
-              ds2[k] = p * (dv[e + k] - d_c);
+            } else {
+              const float4* l4 = reinterpret_cast<const float4*>(sf + 32 * half + e0);
+              const float4* d4 = reinterpret_cast<const float4*>(sf + 64 + 32 * half + e0);
+              const float4 la = l4[0], lb = l4[1], da = d4[0], db = d4[1];
+              lse8[0] = la.x; lse8[1] = la.y; lse8[2] = la.z; lse8[3] = la.w;
+              lse8[4] = lb.x; lse8[5] = lb.y; lse8[6] = lb.z; lse8[7] = lb.w;
+              d8[0] = da.x; d8[1] = da.y; d8[2] = da.z; d8[3] = da.w;
+              d8[4] = db.x; d8[5] = db.y; d8[6] = db.z; d8[7] = db.w;
             }
-            const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
-            const __half2 hd = __floats2half2_rn(ds2[0], ds2[1]);
-            pp[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
-            dd[e / 2] = *reinterpret_cast<const uint32_t*>(&hd);
+#pragma unroll
+            for (int e = e0; e < e0 + 8; e += 2) {
+              float p2[2], ds2[2];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int col = c0 + 32 * half + e + k;  // streamed position
+                const bool allowed = MODE == 0
+                                         ? (row < it.len && col < it.len && (!args.causal || col <= row))
+                                         : (row < it.len && col < it.len && (!args.causal || row <= col));
+                const float p = allowed ? ex2(fmaf(sv[e + k], sl2, -lse8[e - e0 + k])) : 0.f;
+                p2[k] = p;
+                ds2[k] = p * (dv[e + k] - d8[e - e0 + k]);
+              }
+              const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
+              const __half2 hd = __floats2half2_rn(ds2[0], ds2[1]);
+              pp[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+              dd[e / 2] = *reinterpret_cast<const uint32_t*>(&hd);
+            }
           }
           if (MODE == 0) {
             tmem_st16_u(t_row + C::S_COL + 16 * half, dd);   // dS over S

@@ -177,6 +177,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int S = args.c.S, B = args.B, L = args.L;
   const int nch = args.F / kFC;
+  // lengths outside [0, S] are clamped (seq_len) and reported through the status word
+  if (warp == 0 && args.c.lengths != nullptr) {
+    bool bad = false;
+    for (int b = blockIdx.x + lane * gridDim.x; b < B; b += 32 * gridDim.x) {
+      const int l = args.c.lengths[b];
+      bad |= (l < 0) || (l > S);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(args.c.status, TFL_DEV_BAD_LENGTHS);
+  }
   const int units = 4 + 2 * nch;  // ring units per tile and layer: Wk, Wv, Wq, Wo, W1 / W2 chunks
   const int* lengths = args.c.lengths;
   auto idx_w1 = [&](int k) { return 3 + (k == 0 ? 1 : (k == 1 ? 2 : 2 * k)); };

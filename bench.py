@@ -233,7 +233,7 @@ NCU_TRAFFIC = {
     ("gemm_ffn1", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 50.419968e6 + 83.465728e6),
     ("gemm_ffn2", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 186.352896e6 + 19.356416e6),
     ("attention", "B16_S512_D1024_H4_causal"): ("222a4a4c89a8", 50.391808e6 + 0.699392e6),
-    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("222a4a4c89a8", 208.8e6 + 50.3e6),
+    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("136681f07c31", 208.962048e6 + 50.533376e6),
 }
 
 
@@ -480,6 +480,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-slice", type=int, default=0,
                     help="sequences per slice of the streamed e2e path (0: automatic, <0: off)")
+    ap.add_argument("--whole-stack", type=int, default=1,
+                    help="tfl_options.whole_stack: 1 (default) or 0 (per-layer kernels)")
     ap.add_argument("--attn-bwd", default="",
                     help="B,S,H,head_dim,causal: time the standalone attention forward + backward instead")
     args = ap.parse_args()
@@ -517,7 +519,10 @@ def main():
     x = torch.from_numpy(x_np).to(dev)
     lens = torch.from_numpy(lens_np).to(dev)
     out = torch.empty_like(x)
-    m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm)
+    opts = pkg.tfl_default_options()
+    opts.whole_stack = args.whole_stack
+    m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm,
+                             options=opts)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)

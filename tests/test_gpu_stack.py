@@ -29,7 +29,7 @@ def _run(shape, prm, x, lens, causal, norm_placement=0, whole=1, bf16=False):
                              norm_placement=norm_placement, options=o)
     try:
         if whole:
-            assert pkg.tfl_launch_count(m.handle, int(causal)) == 2
+            assert pkg.tfl_launch_count(m.handle, int(causal)) == 1
         xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
         if bf16:
             xd = xd.to(torch.bfloat16)
@@ -48,6 +48,7 @@ def _run(shape, prm, x, lens, causal, norm_placement=0, whole=1, bf16=False):
     (5, 57, 128, 1, False, [57, 1, 30, 56, 2]),
     (1, 1, 256, 2, True, None),
     (2, 128, 1024, 5, False, [90, 128]),
+    (1, 128, 512, 4, True, None),
 ])
 def test_stack_matches_oracle(B, S, F, L, causal, lens):
     shape = synth.Shape(B, S, 128, 4, F, L, causal)
@@ -106,3 +107,16 @@ def test_stack_bf16_io_and_repeat_determinism():
     ub = _run(shape, prm, x_w, lens, True, bf16=True)
     # the bf16 output is the fp32 output rounded once
     np.testing.assert_array_equal(ub, torch.from_numpy(a).to(torch.bfloat16).float().numpy())
+
+
+def test_stack_flags_and_clamps_out_of_range_lengths():
+    import attention_qkv_gemm_gb300 as pkg
+    from tests.helpers import run_gpu
+    shape = synth.Shape(3, 128, 128, 4, 256, 1, False)
+    prm = synth.params(45, shape)
+    x = synth.input_x(45, shape)
+    u, rc = run_gpu(shape, prm, x, [500, -3, 70], False)
+    assert rc == pkg.TFL_ERR_BAD_LENGTHS
+    r = oracle.forward_batched(prm, 4, x, np.array([128, 0, 70], dtype=np.int32), False)
+    assert_gate(u, r, "stack, clamped lengths")
+    assert np.all(u[1] == 0.0)
