@@ -9,10 +9,14 @@
 //     Q K^T of u + 2, which runs while the softmax works on u + 1.  One barrier
 //     each way per sub-block: s_full (S ready; also certifies that the P V
 //     which last read the P buffer is done) and p_full (P written, S read).
+//   * A warp's sub-blocks that no mask touches (all but the last one or two
+//     of an item) run a body without any mask logic; the masked ones take a
+//     general body.
 //   * Online softmax in fp32, one query row per thread (the row's TMEM lane):
 //     running max m, running sum l, O rescaled by exp(m_old - m_new)
 //     (section 2.1, the running-max recurrence).  The row max of a sub-block
-//     is taken from registers before its exponentials, and the rescale is
+//     is taken from registers (four independent max chains) before its
+//     exponentials, and the rescale is
 //     lazy: the reference max only moves when the row max grew by more than 8
 //     in log2 units, so P <= 2^8 and O is touched rarely; O / l is exact
 //     either way.
@@ -84,6 +88,16 @@ size_t attn_smem_bytes(int hd) {
     case 256: return AttnCfg<256>::SMEM;
   }
   return 0;
+}
+
+// mbarrier arrive by the threads whose predicate is set, as a predicated instruction
+// (no branch)
+__device__ __forceinline__ void mbar_arrive_pred(uint64_t* bar, bool p) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"((uint32_t)p)
+      : "memory");
 }
 
 struct Item {
@@ -410,74 +424,94 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       const int wq0 = it.qb * kAttnBM + q * 32;          // first query row of this warp
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
-      for (int u = 0; u < nsub; ++u, ++g) {
-        const uint32_t b = g & 1u;
+      // How this warp's 32 rows meet the 64 keys of sub-block u.  Causal: with
+      // d = (first row of the warp) - k0, d >= 63 is unmasked, d <= -32 is
+      // entirely above the diagonal (P = 0, nothing computed), and d = 0 / 32
+      // (the only other values: query blocks are 128-row and sub-blocks
+      // 64-key aligned) mask one 32-key half triangularly.  Key padding
+      // masks the keys at or past len_b, the same for every row.
+      auto mode_of = [&](int u) -> int {
         const int k0 = u * C::SUB;
-        // How this warp's 32 rows meet the sub-block's 64 keys.  Causal: with
-        // d = (first row of the warp) - k0, d >= 63 is unmasked, d <= -32 is
-        // entirely above the diagonal (P = 0, nothing computed), and d = 0 / 32
-        // (the only other values: query blocks are 128-row and sub-blocks
-        // 64-key aligned) mask one 32-key half triangularly.  Key padding
-        // masks the keys at or past len_b, the same for every row.
-        int mode;
         if (args.causal) {
           const int d = wq0 - k0;
-          mode = d >= C::SUB - 1 ? kFull : d <= -32 ? kNone : d == 0 ? kTriLo : kTriHi;
-        } else {
-          mode = k0 + C::SUB > it.len ? kKeyPad : kFull;
+          return d >= C::SUB - 1 ? kFull : d <= -32 ? kNone : d == 0 ? kTriLo : kTriHi;
         }
-        if (!wait_bounded(&s_full[b], (g >> 1) & 1u, wc)) {
-          ok = false;
-          break;
-        }
+        return k0 + C::SUB > it.len ? kKeyPad : kFull;
+      };
+      // Sub-blocks [0, nfull) are unmasked for every row of this warp (all but
+      // the last one or two): they take a body with no mask logic.
+      int nfull;
+      if (args.causal) {
+        const int t = wq0 - (C::SUB - 1);
+        nfull = t < 0 ? 0 : t / C::SUB + 1;
+      } else {
+        nfull = it.len / C::SUB;
+      }
+      nfull = min(nfull, nsub);
+      float sv[C::SUB];
+      // S of sub-block gg from tensor memory (the columns that can be non-zero),
+      // once its QK^T has completed; the caller waits for the load
+      auto load_s = [&](uint32_t gg, int mode) -> bool {
+        if (!wait_bounded(&s_full[gg & 1u], (gg >> 1) & 1u, wc)) return false;
         tc_fence_after();
-        uint32_t pk[C::SUB / 2];
-        float sv[C::SUB];
-        const uint32_t t_s = t_row + C::S_COL + b * C::SUB;
+        const uint32_t t_s = t_row + C::S_COL + (gg & 1u) * C::SUB;
         if (mode != kNone) {
           tmem_ld32(t_s, sv);
           if (mode != kTriLo) tmem_ld32(t_s + 32, sv + 32);
-          tmem_wait_ld();
         }
-        if (mode == kNone) {
+        return true;
+      };
+      auto body = [&](auto full_tag, int u) -> bool {
+        constexpr bool FULL = decltype(full_tag)::value;
+        const uint32_t b = g & 1u;
+        const int k0 = u * C::SUB;
+        const int mode = FULL ? kFull : mode_of(u);
+        uint32_t pk[C::SUB / 2];
+        if (!load_s(g, mode)) return false;
+        if (!FULL && mode == kNone) {
 #pragma unroll
           for (int e = 0; e < C::SUB / 2; ++e) pk[e] = 0u;
         } else {
-          if (mode == kTriLo) {
+          tmem_wait_ld();
+          if constexpr (!FULL) {
+            if (mode == kTriLo) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sv[e] = e <= lane ? sv[e] : -INFINITY;
-          } else if (mode == kTriHi) {
+              for (int e = 0; e < 32; ++e) sv[e] = e <= lane ? sv[e] : -INFINITY;
+            } else if (mode == kTriHi) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sv[32 + e] = e <= lane ? sv[32 + e] : -INFINITY;
-          } else if (mode == kKeyPad) {
-            const int lim = it.len - 1 - k0;
+              for (int e = 0; e < 32; ++e) sv[32 + e] = e <= lane ? sv[32 + e] : -INFINITY;
+            } else if (mode == kKeyPad) {
+              const int lim = it.len - 1 - k0;
 #pragma unroll
-            for (int e = 0; e < C::SUB; ++e) sv[e] = e <= lim ? sv[e] : -INFINITY;
-          }
-          const int nv = mode == kTriLo ? 32 : C::SUB;  // values that can be non-zero
-          float bm0 = -INFINITY, bm1 = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            bm0 = fmax3(bm0, sv[e], sv[e + 1]);
-            bm1 = fmax3(bm1, sv[e + 2], sv[e + 3]);
-          }
-          if (nv == C::SUB) {
-#pragma unroll
-            for (int e = 32; e < C::SUB; e += 4) {
-              bm0 = fmax3(bm0, sv[e], sv[e + 1]);
-              bm1 = fmax3(bm1, sv[e + 2], sv[e + 3]);
+              for (int e = 0; e < C::SUB; ++e) sv[e] = e <= lim ? sv[e] : -INFINITY;
             }
           }
-          const float m_new = fmaxf(m_run, fmaxf(bm0, bm1) * sl2);
+          const bool half = !FULL && mode == kTriLo;  // only the first 32 keys can be non-zero
+          // block maximum in four independent chains (short dependent paths)
+          float bm0 = -INFINITY, bm1 = -INFINITY, bm2 = -INFINITY, bm3 = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            bm0 = fmax3(bm0, sv[e], sv[e + 1]);
+            bm1 = fmax3(bm1, sv[e + 2], sv[e + 3]);
+            bm2 = fmax3(bm2, sv[e + 4], sv[e + 5]);
+            bm3 = fmax3(bm3, sv[e + 6], sv[e + 7]);
+          }
+          if (!half) {
+#pragma unroll
+            for (int e = 32; e < C::SUB; e += 8) {
+              bm0 = fmax3(bm0, sv[e], sv[e + 1]);
+              bm1 = fmax3(bm1, sv[e + 2], sv[e + 3]);
+              bm2 = fmax3(bm2, sv[e + 4], sv[e + 5]);
+              bm3 = fmax3(bm3, sv[e + 6], sv[e + 7]);
+            }
+          }
+          const float m_new = fmaxf(m_run, fmaxf(fmax3(bm0, bm1, bm2), bm3) * sl2);
           const bool resc = m_new > m_run + 8.0f;
           if (__any_sync(0xffffffffu, resc)) {
             if (u > 0) {
               // O must hold P V of every earlier sub-block of this item before it is rescaled
               const uint32_t gp = g - 1;
-              if (!wait_bounded(&pv_done[gp & 1u], (gp >> 1) & 1u, wc)) {
-                ok = false;
-                break;
-              }
+              if (!wait_bounded(&pv_done[gp & 1u], (gp >> 1) & 1u, wc)) return false;
               tc_fence_after();
               const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
 #pragma unroll 1
@@ -509,7 +543,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           };
 #pragma unroll
           for (int e2 = 0; e2 < 16; ++e2) exp_pairs(e2);
-          if (nv == C::SUB) {
+          if (!half) {
 #pragma unroll
             for (int e2 = 16; e2 < C::SUB / 2; ++e2) exp_pairs(e2);
           } else {
@@ -525,8 +559,12 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[b]);
-      }
+        mbar_arrive_pred(&p_full[b], lane == 0);
+        return true;
+      };
+      int u = 0;
+      for (; ok && u < nfull; ++u, ++g) ok = body(std::true_type{}, u);
+      for (; ok && u < nsub; ++u, ++g) ok = body(std::false_type{}, u);
       if (!ok) break;
       if (!wait_bounded(o_full, oph, wc)) break;
       oph ^= 1u;
