@@ -223,17 +223,11 @@ KERNEL_SOURCES = {
 KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh", "chainops.cuh"]
 
 NCU_TRAFFIC = {
-    # (kernel, workload): (kernel source fingerprint, bytes per launch)
+    # (kernel, workload): (kernel source fingerprint, bytes per launch); entries whose
+    # fingerprint no longer matches the sources report null
     ("postchain", "B64_S1024_D128_causal_ragged"): ("048a2bf32bcb", 42.617344e6 + 29.616384e6),
-    ("stack", "B2048_S128_D128_H4_F512_L4_keymask"): ("6babbc9c1ba1", 87.52e6 + 86.017024e6),
-    ("attention", "B64_S1024_D128_causal_ragged"): ("222a4a4c89a8", 41.433088e6 + 0.554752e6),
-    ("gemm_qkv", "B64_S1024_D128_causal_ragged"): ("f2139ce26c7e", 27.822592e6 + 0.657664e6),
-    ("gemm_qkv", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 46.189568e6 + 12.694784e6),
-    ("gemm_oproj", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 54.557184e6 + 2.611456e6),
-    ("gemm_ffn1", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 50.419968e6 + 83.465728e6),
-    ("gemm_ffn2", "B16_S512_D1024_H4_causal"): ("f2139ce26c7e", 186.352896e6 + 19.356416e6),
-    ("attention", "B16_S512_D1024_H4_causal"): ("222a4a4c89a8", 50.391808e6 + 0.699392e6),
-    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("136681f07c31", 208.962048e6 + 50.533376e6),
+    ("stack", "B2048_S128_D128_H4_F512_L4_keymask"): ("6babbc9c1ba1", 87.52e6 + 86.017024e6),  # lengths U[32,128]
+    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("6bbea9362b5c", 208.719104e6 + 50.630144e6),
 }
 
 
