@@ -165,7 +165,15 @@ bool use_stack(const tfl_shape& s, const tfl_options& o) {
 
 // Output tile width: 256 when N allows it, except with split activations (the
 // four operand tiles of a 256-wide stage leave room for only two stages).
-int gemm_bn(int N, int split_act) { return (N % 256 == 0 && !split_act) ? 256 : 128; }
+// GEMM tile width.  A 256-wide tile issues half the MMA instructions per FLOP of a 128-wide
+// one, and MMA issue is what holds these GEMMs below the tensor peak; with split activations
+// (then two 96 KB ring stages) that pays for the QKV and FFN-in GEMMs above d_model 128
+// (N = 3 d_model, d_ff) but not for FFN-out (N = d_model: too few tile rounds on small
+// batches, no gain on large ones).  At d_model 128 the fused chain and the whole-stack kernel
+// share the 128-row weight maps.
+int gemm_bn(int N, int split_act, bool wide_split) {
+  return (N % 256 == 0 && (!split_act || wide_split)) ? 256 : 128;
+}
 
 }  // namespace
 
@@ -435,7 +443,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       g.acc_scale = ly.wqkv.acc_scale;
       g.bias = ly.bqkv;
       g.c16 = h->qkv16;
-      TFL_CUDA(launch_gemm(gemm_bn(3 * D, as), EPI_BIAS_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.wqkv), g,
+      TFL_CUDA(launch_gemm(gemm_bn(3 * D, as, D > 128), EPI_BIAS_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.wqkv), g,
                            h->num_sms, st),
                "qkv gemm");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_QKV), "event");
@@ -549,7 +557,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_OPROJ), "event");
       } else {
         g.h32 = h->h32;
-        TFL_CUDA(launch_gemm(gemm_bn(D, 0), EPI_BIAS_RES_F32, 0, ws, mp, g, h->num_sms, st), "o_proj gemm");
+        TFL_CUDA(launch_gemm(gemm_bn(D, 0, false), EPI_BIAS_RES_F32, 0, ws, mp, g, h->num_sms, st), "o_proj gemm");
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_OPROJ), "event");
         RowArgs ra;
         ra.c = c;
@@ -570,7 +578,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       g.bias = ly.b1;
       g.c16 = h->g16;
       g.c16lo = h->g16lo;
-      TFL_CUDA(launch_gemm(gemm_bn(F, as), EPI_BIAS_GELU_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.w1), g,
+      TFL_CUDA(launch_gemm(gemm_bn(F, as, D > 128), EPI_BIAS_GELU_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.w1), g,
                            h->num_sms, st),
                "ffn1 gemm");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN1), "event");
@@ -615,7 +623,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
       } else {
         g.h32 = h->h32;
-        TFL_CUDA(launch_gemm(gemm_bn(D, as), EPI_BIAS_RES_F32, as, ws, mp, g, h->num_sms, st), "ffn2 gemm");
+        TFL_CUDA(launch_gemm(gemm_bn(D, as, false), EPI_BIAS_RES_F32, as, ws, mp, g, h->num_sms, st), "ffn2 gemm");
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
         RowArgs ra;
         ra.c = c;
@@ -819,8 +827,8 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
         return ok;
       };
       const int aw = o.precision == 2;
-      bool ok = maps(d.wqkv, 3 * D, D, gemm_bn(3 * D, aw)) && maps(d.wo, D, D, D == 128 ? 128 : gemm_bn(D, 0)) &&
-                maps(d.w1, F, D, gemm_bn(F, aw)) && maps(d.w2, D, F, D == 128 ? 128 : gemm_bn(D, aw));
+      bool ok = maps(d.wqkv, 3 * D, D, gemm_bn(3 * D, aw, D > 128)) && maps(d.wo, D, D, D == 128 ? 128 : gemm_bn(D, 0, false)) &&
+                maps(d.w1, F, D, gemm_bn(F, aw, D > 128)) && maps(d.w2, D, F, D == 128 ? 128 : gemm_bn(D, aw, false));
       if (!ok) rc = fail(TFL_ERR_CUDA, "weight tensor map encoding failed");
     }
   }

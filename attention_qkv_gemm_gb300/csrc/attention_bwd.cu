@@ -12,7 +12,9 @@
 //   dQ    = dS K / sqrt(hd)      dK = dS^T Q / sqrt(hd)      dV = P^T dO
 // Masks: key j of sequence b exists iff j < len_b; with causal, query i sees
 // key j iff j <= i.  Query rows at or past len_b are padding: their dO is
-// ignored (dQ = 0 there) and they add nothing to dK and dV.
+// ignored (dQ = 0 there) and they add nothing to dK and dV.  A 64-row step no mask
+// touches for any row of an elementwise warp (all but the ones at len_b or across the
+// diagonal) takes a body without the per-pair test.
 //
 // One kernel template serves both directions.  A CTA owns 128 resident rows
 // (queries for dQ, keys for dK/dV) and streams 64-row tiles of the other side:
@@ -25,6 +27,8 @@
 // operands from tensor memory.  Warps: 0 MMA issuer and TMEM owner, 1 TMA
 // producer, 2-5 elementwise and output.  Work items (b, h, 128-row block) are
 // dealt round-robin, heaviest first under causal.
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -313,59 +317,72 @@ __global__ void __launch_bounds__(192, 2)
         }
         sph ^= 1u;
         tc_fence_after();
+        // A step no mask touches for any of this warp's rows (every row and column inside
+        // len_b and, under causal, every pair on the allowed side) skips the per-pair test.
+        const int wr0 = it.blk * 128 + q * 32;  // this warp's first resident row
+        const bool unmasked = wr0 + 31 < it.len && c0 + 63 < it.len &&
+                              (!args.causal || (MODE == 0 ? c0 + 63 <= wr0 : wr0 + 31 <= c0));
+        auto step = [&](auto full_tag) {
+          constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float sv[32], dv[32];
-          tmem_ld32(t_row + C::S_COL + 32 * half, sv);
-          tmem_ld32(t_row + C::DP_COL + 32 * half, dv);
-          tmem_wait_ld();
-          uint32_t pp[16], dd[16];
+          for (int half = 0; half < 2; ++half) {
+            float sv[32], dv[32];
+            tmem_ld32(t_row + C::S_COL + 32 * half, sv);
+            tmem_ld32(t_row + C::DP_COL + 32 * half, dv);
+            tmem_wait_ld();
+            uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int e0 = 0; e0 < 32; e0 += 8) {
-            // the 8 columns' log-sum-exp and row sums: per-thread constants for dQ (row =
-            // query), per column from the step's shared staging for dK/dV (row = key)
-            float lse8[8], d8[8];
+            for (int e0 = 0; e0 < 32; e0 += 8) {
+              // the 8 columns' log-sum-exp and row sums: per-thread constants for dQ (row =
+              // query), per column from the step's shared staging for dK/dV (row = key)
+              float lse8[8], d8[8];
+              if (MODE == 0) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  lse8[k] = lse_r;
+                  d8[k] = d_r;
+                }
+              } else {
+                const float4* l4 = reinterpret_cast<const float4*>(sf + 32 * half + e0);
+                const float4* d4 = reinterpret_cast<const float4*>(sf + 64 + 32 * half + e0);
+                const float4 la = l4[0], lb = l4[1], da = d4[0], db = d4[1];
+                lse8[0] = la.x; lse8[1] = la.y; lse8[2] = la.z; lse8[3] = la.w;
+                lse8[4] = lb.x; lse8[5] = lb.y; lse8[6] = lb.z; lse8[7] = lb.w;
+                d8[0] = da.x; d8[1] = da.y; d8[2] = da.z; d8[3] = da.w;
+                d8[4] = db.x; d8[5] = db.y; d8[6] = db.z; d8[7] = db.w;
+              }
+#pragma unroll
+              for (int e = e0; e < e0 + 8; e += 2) {
+                float p2[2], ds2[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int col = c0 + 32 * half + e + k;  // streamed position
+                  bool allowed = true;
+                  if constexpr (!FULL)
+                    allowed = MODE == 0 ? (row < it.len && col < it.len && (!args.causal || col <= row))
+                                        : (row < it.len && col < it.len && (!args.causal || row <= col));
+                  const float p = allowed ? ex2(fmaf(sv[e + k], sl2, -lse8[e - e0 + k])) : 0.f;
+                  p2[k] = p;
+                  ds2[k] = p * (dv[e + k] - d8[e - e0 + k]);
+                }
+                const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
+                const __half2 hd = __floats2half2_rn(ds2[0], ds2[1]);
+                pp[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+                dd[e / 2] = *reinterpret_cast<const uint32_t*>(&hd);
+              }
+            }
             if (MODE == 0) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                lse8[k] = lse_r;
-                d8[k] = d_r;
-              }
+              tmem_st16_u(t_row + C::S_COL + 16 * half, dd);   // dS over S
             } else {
-              const float4* l4 = reinterpret_cast<const float4*>(sf + 32 * half + e0);
-              const float4* d4 = reinterpret_cast<const float4*>(sf + 64 + 32 * half + e0);
-              const float4 la = l4[0], lb = l4[1], da = d4[0], db = d4[1];
-              lse8[0] = la.x; lse8[1] = la.y; lse8[2] = la.z; lse8[3] = la.w;
-              lse8[4] = lb.x; lse8[5] = lb.y; lse8[6] = lb.z; lse8[7] = lb.w;
-              d8[0] = da.x; d8[1] = da.y; d8[2] = da.z; d8[3] = da.w;
-              d8[4] = db.x; d8[5] = db.y; d8[6] = db.z; d8[7] = db.w;
-            }
-#pragma unroll
-            for (int e = e0; e < e0 + 8; e += 2) {
-              float p2[2], ds2[2];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int col = c0 + 32 * half + e + k;  // streamed position
-                const bool allowed = MODE == 0
-                                         ? (row < it.len && col < it.len && (!args.causal || col <= row))
-                                         : (row < it.len && col < it.len && (!args.causal || row <= col));
-                const float p = allowed ? ex2(fmaf(sv[e + k], sl2, -lse8[e - e0 + k])) : 0.f;
-                p2[k] = p;
-                ds2[k] = p * (dv[e + k] - d8[e - e0 + k]);
-              }
-              const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
-              const __half2 hd = __floats2half2_rn(ds2[0], ds2[1]);
-              pp[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
-              dd[e / 2] = *reinterpret_cast<const uint32_t*>(&hd);
+              tmem_st16_u(t_row + C::S_COL + 16 * half, pp);   // P^T over S^T
+              tmem_st16_u(t_row + C::DP_COL + 16 * half, dd);  // dS^T over dP^T
             }
           }
-          if (MODE == 0) {
-            tmem_st16_u(t_row + C::S_COL + 16 * half, dd);   // dS over S
-          } else {
-            tmem_st16_u(t_row + C::S_COL + 16 * half, pp);   // P^T over S^T
-            tmem_st16_u(t_row + C::DP_COL + 16 * half, dd);  // dS^T over dP^T
-          }
-        }
+        };
+        if (unmasked)
+          step(std::true_type{});
+        else
+          step(std::false_type{});
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

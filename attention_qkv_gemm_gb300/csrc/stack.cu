@@ -54,7 +54,13 @@ constexpr int kHD = 32;             // head_dim
 constexpr int kH = kD / kHD;        // heads
 constexpr int kKVTile = 128 * kHD * 2;  // one head's K (or V): 128 rows x 64 B, 64-byte swizzle
 constexpr int kOnesBytes = 16 * 128;
-constexpr size_t kSmem = 1024 + (size_t)kRing * kUnit + 2 * (size_t)kH * kKVTile + kOnesBytes + kRedBytes + 512;
+// Parameter vectors staged in shared memory once per CTA (floats): the final LayerNorm's
+// gamma / beta, then per layer [bq | bk | bv] (384), bo (128), b1 (d_ff), b2 (128) and, for
+// post-LN, LN1 / LN2 gamma and beta (4 x 128), for as many layers as fit; the epilogue reads
+// the others from global memory.
+constexpr int kPrmCap = 5632;
+constexpr size_t kSmem =
+    1024 + (size_t)kRing * kUnit + 2 * (size_t)kH * kKVTile + kOnesBytes + kRedBytes + (size_t)kPrmCap * 4 + 512;
 
 constexpr uint32_t kColR = 0, kColN = 128, kColQ = 128, kColOP = 192, kColA = 256, kColB = 384;
 
@@ -123,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = sK + (size_t)kH * kKVTile;
   uint8_t* sOnes = sV + (size_t)kH * kKVTile;
   float* red = reinterpret_cast<float*>(sOnes + kOnesBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
+  float* prm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(prm + kPrmCap);
   uint64_t* r_full = bars + 0;     // [kRing]
   uint64_t* r_empty = bars + 2;    // [kRing]
   uint64_t* n_ready = bars + 4;    // epilogue -> A: N and R written
@@ -166,6 +173,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     *never_flag = 0;
     fence_barrier_init();
+  }
+  // parameter staging (weights and vectors are written at create time, before any kernel
+  // of this stream, so this needs no dependent-launch wait); every thread issues all of its
+  // loads before any store: one global-memory round trip
+  const int prm_stride = 640 + args.F + (args.post_ln ? 4 * kD : 0);
+  const int prm_layers = min(args.L, (kPrmCap - 2 * kD) / prm_stride);
+  {
+    const int n = 2 * kD + prm_layers * prm_stride;
+    constexpr int kPer = (kPrmCap + kThreads - 1) / kThreads;
+    auto source = [&](int i) -> const float* {
+      if (i < kD) return args.lnf_g + i;
+      if (i < 2 * kD) return args.lnf_b + (i - kD);
+      const int j = i - 2 * kD, l = j / prm_stride;
+      int o = j - l * prm_stride;
+      const StackLayerArgs& P = args.layer[l];
+      if (o < 3 * kD) return P.bqkv + o;
+      if ((o -= 3 * kD) < kD) return P.bo + o;
+      if ((o -= kD) < args.F) return P.b1 + o;
+      if ((o -= args.F) < kD) return P.b2 + o;
+      o -= kD;
+      const int w = o / kD;
+      const float* ln = w == 0 ? P.ln1_g : w == 1 ? P.ln1_b : w == 2 ? P.ln2_g : P.ln2_b;
+      return ln + (o - w * kD);
+    };
+    float pv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      pv[k] = i < n ? __ldg(source(i)) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      if (i < n) prm[i] = pv[k];
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -411,6 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int l = 0; l < L; ++l) {
           const StackLayerArgs& P = args.layer[l];
+          // the layer's vectors: shared-memory copies when staged (offset within the layer's
+          // block), else global memory
+          const bool st_l = l < prm_layers;
+          auto vec = [&](int off, const float* g) -> const float* {
+            return st_l ? prm + 2 * kD + l * prm_stride + off : g;
+          };
           // ---- E1: the layer's QKV operand and the residual accumulator
           float mean = 0.f, rstd = 1.f;
           if (!args.post_ln) {
@@ -439,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(k_read);
-          scale_bias32(v, aq, P.bqkv + kD + c0);
+          scale_bias32(v, aq, vec(0, P.bqkv) + kD + c0);
           if (r >= len) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -450,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           tmem_ld32(tq + kColB + c0, v);
           tmem_wait_ld();
-          scale_bias32(v, aq, P.bqkv + 2 * kD + c0);
+          scale_bias32(v, aq, vec(0, P.bqkv) + 2 * kD + c0);
           if (r >= len) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -466,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           tmem_ld32(tq + kColA + c0, v);
           tmem_wait_ld();
-          scale_bias32(v, aq, P.bqkv + c0);
+          scale_bias32(v, aq, vec(0, P.bqkv) + c0);
           {
             uint32_t pq[16];
 #pragma unroll
@@ -547,8 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           tmem_ld32(tq + kColR + c0, tv);
           tmem_wait_ld();
-          scale_bias32(tv, P.scale_o, P.bo + c0);
-          if (args.post_ln) layer_norm32(tv, eps, P.ln1_g, P.ln1_b, c0, red, slot, part, r);
+          scale_bias32(tv, P.scale_o, vec(3 * kD, P.bo) + c0);
+          if (args.post_ln) layer_norm32(tv, eps, vec(5 * kD + args.F, P.ln1_g), vec(6 * kD + args.F, P.ln1_b), c0, red, slot, part, r);
           {
             float rv[32];
 #pragma unroll
@@ -579,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(g_read);
             uint32_t hi[16], lo[16];
-            gelu_split32(gv, a1, P.b1 + ((c + b) % nch) * kFC + c0, hi, lo);
+            gelu_split32(gv, a1, vec(4 * kD, P.b1) + ((c + b) % nch) * kFC + c0, hi, lo);
             if (gp_written) {  // GP is free once FFN-out of the previous chunk has read it
               if (!wait_bounded(gp_free, ph_gf, ewc)) { ok = false; break; }
               ph_gf ^= 1u;
@@ -600,12 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           tmem_ld32(tq + kColR + c0, tv);
           tmem_wait_ld();
-          scale_bias32(tv, P.scale_2, P.b2 + c0);
-          if (args.post_ln) layer_norm32(tv, eps, P.ln2_g, P.ln2_b, c0, red, slot, part, r);
+          scale_bias32(tv, P.scale_2, vec(4 * kD + args.F, P.b2) + c0);
+          if (args.post_ln) layer_norm32(tv, eps, vec(7 * kD + args.F, P.ln2_g), vec(8 * kD + args.F, P.ln2_b), c0, red, slot, part, r);
         }
         if (!ok) break;
         // ---- tail: final LayerNorm, padding rows zero
-        layer_norm32(tv, eps, args.lnf_g, args.lnf_b, c0, red, slot, part, r);
+        layer_norm32(tv, eps, prm, prm + kD, c0, red, slot, part, r);
         if (r >= len) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) tv[i] = 0.f;
