@@ -212,8 +212,9 @@ const char* tfl_last_error(void);
 /*
  * Eager forward (no graph) with a CUDA event around every launch, for
  * profiling.  Writes up to `cap` entries: kernel_ms[i] = device time of
- * launch i, kernel_kind[i] = TFL_KIND_* of that launch; *n = launches.
- * Synchronizes `stream`.
+ * launch i, kernel_kind[i] = TFL_KIND_* of that launch; *n = the timed launches: all of
+ * tfl_forward's launches but the length check of the per-layer path (the whole-stack
+ * kernel checks the lengths itself and is the one launch).  Synchronizes `stream`.
  */
 #define TFL_KIND_ROWNORM   1
 #define TFL_KIND_GEMM_QKV  2
