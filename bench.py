@@ -12,8 +12,9 @@ Prints ONE JSON line (rank 0).  Keys beyond the base contract:
   cpu_baseline  the fp64 oracle timed on this host on a bounded sample
   e2e           tokens/s from pinned host x / out, host<->device traffic inside
                 the timed region: tfl_forward_host (the kernels read x and write
-                out across the host link) or, for batches over 1M tokens,
-                tfl_forward_streamed (batch slices overlapping their copies)
+                out across the host link) or, for inputs over 4 GB,
+                tfl_forward_streamed (batch slices of a sixteenth of the batch,
+                their copies overlapping the forward of other slices)
   clocks        SM clock samples taken during the timed region
 With --impl reference the fp64 oracle itself is timed as the reference arm.
 Multi-GPU (torchrun): every rank runs an independent replica on its own
@@ -385,14 +386,15 @@ def reference_arm(args, shape, world, rank):
 
 
 def e2e_slice(shape, arg: int) -> int:
-    """Sequences per slice of the streamed end-to-end path: 0 (no slicing) for batches of
-    up to 1M tokens, else an eighth of the batch (at least one sequence); arg > 0 forces a
-    slice size, arg < 0 turns slicing off."""
+    """Sequences per slice of the streamed end-to-end path: 0 (no slicing: tfl_forward_host)
+    unless the fp32 input is over 4 GB, else a sixteenth of the batch (at least one sequence):
+    small slices keep the copies that nothing overlaps (the first slice in, the last one out)
+    short; arg > 0 forces a slice size, arg < 0 turns slicing off."""
     if arg < 0:
         return 0
     if arg > 0:
         return min(arg, shape.B)
-    return 0 if shape.B * shape.S <= (1 << 20) else max(1, shape.B // 8)
+    return 0 if shape.B * shape.S * shape.d_model * 4 <= (4 << 30) else max(1, shape.B // 16)
 
 
 def config_dict(shape):
