@@ -60,7 +60,7 @@ class TflWeights(ctypes.Structure):
 class TflOptions(ctypes.Structure):
     _fields_ = [("precision", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("wait_timeout_ns", ctypes.c_int64),
                 ("max_workspace_bytes", ctypes.c_int64), ("use_graph", ctypes.c_int32),
-                ("whole_stack", ctypes.c_int32)]
+                ("whole_stack", ctypes.c_int32), ("fp8_corrections", ctypes.c_int32)]
 
 
 class TflError(RuntimeError):

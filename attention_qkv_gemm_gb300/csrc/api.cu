@@ -69,6 +69,20 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D e4m3 (byte) map over a row-major [rows, cols] plane, box {64, box_rows}: 64-byte rows,
+// 64B swizzle (the fp8 operand planes of a 64-wide GEMM k-block).
+bool make_map_2d_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3D fp16 map over qkv [B, S, 3D]: box {atom_cols, box_rows, 1}.
 bool make_map_qkv(CUtensorMap* m, const void* base, uint64_t B, uint64_t S, uint64_t C3, uint32_t atom_cols,
                   uint32_t box_rows) {
@@ -102,11 +116,17 @@ bool make_map_store64(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // One packed weight matrix: fp16 hi (and lo) parts of W * 2^s, and the 2^-s the GEMM applies.
+// In the fp8 operand form (f8) hi holds fp16(W 2^s) 2^11 and the lo storage [N, K] fp16 holds
+// the two e4m3 planes [N, K] bytes each (hi, then lo times 2^11); the GEMM applies 2^-(s+11).
 struct PackedW {
   __half* hi = nullptr;
   __half* lo = nullptr;
   float acc_scale = 1.f;
-  CUtensorMap tm_hi{}, tm_lo{};
+  bool f8 = false;
+  size_t elems = 0;
+  CUtensorMap tm_hi{}, tm_lo{}, tm_lo2{};
+  uint8_t* f8hi() const { return reinterpret_cast<uint8_t*>(lo); }
+  uint8_t* f8lo() const { return reinterpret_cast<uint8_t*>(lo) + elems; }
 };
 
 struct LayerDev {
@@ -196,9 +216,19 @@ struct tfl_handle {
   float* h32 = nullptr;
   __half *n16 = nullptr, *qkv16 = nullptr, *o16 = nullptr, *g16 = nullptr;
   __half *n16lo = nullptr, *g16lo = nullptr;  // precision 2 only
+  // fp8 operand form of the d_model > 128 split GEMMs (QKV, FFN-in, FFN-out): the lo planes'
+  // storage holds the two e4m3 planes of the normed rows / GELU output instead
+  bool f8 = false;
   int* status = nullptr;
   int* sched = nullptr;
   CUtensorMap tm_n16{}, tm_n16lo{}, tm_o16{}, tm_g16{}, tm_g16lo{}, tm_q{}, tm_kv{};
+  CUtensorMap tm_n8hi{}, tm_n8lo{}, tm_g8hi{}, tm_g8lo{};
+  uint8_t* n8hi() const { return f8 ? reinterpret_cast<uint8_t*>(n16lo) : nullptr; }
+  uint8_t* n8lo() const { return f8 ? reinterpret_cast<uint8_t*>(n16lo) + (size_t)M * D : nullptr; }
+  uint8_t* g8hi() const { return f8 ? reinterpret_cast<uint8_t*>(g16lo) : nullptr; }
+  uint8_t* g8lo() const { return f8 ? reinterpret_cast<uint8_t*>(g16lo) + (size_t)M * F : nullptr; }
+  __half* n16lo_fp16() const { return f8 ? nullptr : n16lo; }  // the fp16 lo plane, when that form is used
+  __half* g16lo_fp16() const { return f8 ? nullptr : g16lo; }
   std::vector<GraphEntry> graphs;
   float *hx_dev = nullptr, *hout_dev = nullptr;
   int* hlen_dev = nullptr;
@@ -217,6 +247,28 @@ struct tfl_handle {
 namespace {
 // The fused chain (d_model 128) also computes the next layer's QKV projection in its tail.
 bool chain_fuses_qkv(const tfl_handle* h) { return use_chain(h->D, h->F, h->opt.precision); }
+
+// Tensor maps of the activation planes the GEMMs and attention read (rebuilt whenever the
+// planes move).  Without a lo plane the lo maps repeat the hi ones (never read).
+bool make_activation_maps(tfl_handle* h) {
+  const uint64_t M = (uint64_t)h->M;
+  const int D = h->D, F = h->F;
+  const int atom = h->hd < 64 ? h->hd : 64;
+  bool ok = make_map_2d(&h->tm_n16, h->n16, M, D, kGemmBM) && make_map_2d(&h->tm_o16, h->o16, M, D, kGemmBM) &&
+            make_map_2d(&h->tm_g16, h->g16, M, F, kGemmBM) &&
+            make_map_qkv(&h->tm_q, h->qkv16, h->shape.B, h->shape.S, 3 * D, atom, kAttnBM) &&
+            make_map_qkv(&h->tm_kv, h->qkv16, h->shape.B, h->shape.S, 3 * D, atom, attn_block_n(h->hd));
+  h->tm_n16lo = h->tm_n8hi = h->tm_n8lo = h->tm_n16;
+  h->tm_g16lo = h->tm_g8hi = h->tm_g8lo = h->tm_g16;
+  if (ok && h->f8)
+    ok = make_map_2d_u8(&h->tm_n8hi, h->n8hi(), M, D, kGemmBM) && make_map_2d_u8(&h->tm_n8lo, h->n8lo(), M, D, kGemmBM) &&
+         make_map_2d_u8(&h->tm_g8hi, h->g8hi(), M, F, kGemmBM) && make_map_2d_u8(&h->tm_g8lo, h->g8lo(), M, F, kGemmBM);
+  else if (ok) {
+    if (h->n16lo) ok = make_map_2d(&h->tm_n16lo, h->n16lo, M, D, kGemmBM);
+    if (ok && h->g16lo) ok = make_map_2d(&h->tm_g16lo, h->g16lo, M, F, kGemmBM);
+  }
+  return ok;
+}
 }  // namespace
 
 namespace {
@@ -248,7 +300,8 @@ int stage_f32(const float* src, size_t n, float* tmp, const char* name) {
 // Pack `count` float32 matrices (consecutive rows of one GEMM operand) into
 // hi (and lo) fp16 parts of W * 2^s, s chosen from the largest |w| so that
 // the lo parts sit well inside the normal fp16 range.
-int pack_staged(const float* tmp, size_t off, unsigned* dmax, PackedW& w, bool split, const char* name) {
+int pack_staged(const float* tmp, size_t off, unsigned* dmax, PackedW& w, bool split, const char* name,
+                bool f8 = false) {
   TFL_CUDA(cudaMemset(dmax, 0, sizeof(unsigned)), name);
   TFL_CUDA(launch_absmax(tmp, off, dmax, 0), name);
   unsigned bits = 0;
@@ -263,7 +316,14 @@ int pack_staged(const float* tmp, size_t off, unsigned* dmax, PackedW& w, bool s
   }
   const float scale = std::ldexp(1.0f, s);
   w.acc_scale = std::ldexp(1.0f, -s);
-  TFL_CUDA(launch_split_f16(tmp, w.hi, split ? w.lo : nullptr, off, scale, 0), name);
+  w.f8 = f8 && split;
+  w.elems = off;
+  if (w.f8) {
+    w.acc_scale = std::ldexp(1.0f, -s - 11);
+    TFL_CUDA(launch_split_f8(tmp, w.hi, w.f8hi(), w.f8lo(), off, scale, 0), name);
+  } else {
+    TFL_CUDA(launch_split_f16(tmp, w.hi, split ? w.lo : nullptr, off, scale, 0), name);
+  }
   TFL_CUDA(cudaDeviceSynchronize(), name);
   return TFL_OK;
 }
@@ -282,10 +342,10 @@ int stage_weights(const float* const* src, const size_t* n, int count, float* tm
 }
 
 int pack_weights(const float* const* src, const size_t* n, int count, float* tmp, unsigned* dmax, PackedW& w,
-                 bool split, const char* name) {
+                 bool split, const char* name, bool f8 = false) {
   size_t total = 0;
   const int rc = stage_weights(src, n, count, tmp, &total, name);
-  return rc ? rc : pack_staged(tmp, total, dmax, w, split, name);
+  return rc ? rc : pack_staged(tmp, total, dmax, w, split, name, f8);
 }
 
 int copy_f32(const float* src, size_t n, float* dst, const char* name) {
@@ -346,10 +406,23 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
   const int D = h->D, F = h->F, L = h->L;
   auto maps = [](const CUtensorMap& a, const CUtensorMap& alo, const PackedW& w) {
     GemmMaps m;
-    m.a = a;
+    m.a = m.a2 = a;
     m.alo = alo;
-    m.b = w.tm_hi;
+    m.b = m.b2 = w.tm_hi;
     m.blo = w.tm_lo;
+    return m;
+  };
+  // the GEMMs above d_model 128 that read split activations (QKV, FFN-in, FFN-out): the fp8
+  // operand form (mode 2) when the handle uses it, else the fp16 lo planes
+  const int as_x = h->f8 ? 2 : as, ws_x = h->f8 ? 2 : ws;
+  auto maps_x = [&](const CUtensorMap& a, const CUtensorMap& alo, const CUtensorMap& a8hi, const CUtensorMap& a8lo,
+                    const PackedW& w) {
+    GemmMaps m = maps(a, alo, w);
+    if (h->f8) {
+      m.alo = a8hi;
+      m.a2 = a8lo;
+      m.b2 = w.tm_lo2;
+    }
     return m;
   };
 
@@ -414,7 +487,9 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
     ra.inbf = xbf;
     ra.row.eps = eps;
     ra.row.n16 = h->n16;
-    ra.row.n16lo = h->n16lo;
+    ra.row.n16lo = h->n16lo_fp16();
+    ra.row.n8hi = h->n8hi();
+    ra.row.n8lo = h->n8lo();
     if (pre) {
       ra.row.flags = ROW_NORM16;
       ra.row.gb = h->layers[0].ln1_g;
@@ -443,8 +518,8 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       g.acc_scale = ly.wqkv.acc_scale;
       g.bias = ly.bqkv;
       g.c16 = h->qkv16;
-      TFL_CUDA(launch_gemm(gemm_bn(3 * D, as, D > 128), EPI_BIAS_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.wqkv), g,
-                           h->num_sms, st),
+      TFL_CUDA(launch_gemm(gemm_bn(3 * D, as, D > 128), EPI_BIAS_F16, as_x, ws_x,
+                           maps_x(h->tm_n16, h->tm_n16lo, h->tm_n8hi, h->tm_n8lo, ly.wqkv), g, h->num_sms, st),
                "qkv gemm");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_QKV), "event");
     }
@@ -539,7 +614,9 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ro.eps = eps;
       ro.h32 = h->h32;
       ro.n16 = h->n16;
-      ro.n16lo = h->n16lo;
+      ro.n16lo = h->n16lo_fp16();
+      ro.n8hi = h->n8hi();
+      ro.n8lo = h->n8lo();
       if (pre) {
         ro.flags = ROW_NORM16;
         ro.gb = ly.ln2_g;
@@ -577,9 +654,11 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       g.acc_scale = ly.w1.acc_scale;
       g.bias = ly.b1;
       g.c16 = h->g16;
-      g.c16lo = h->g16lo;
-      TFL_CUDA(launch_gemm(gemm_bn(F, as, D > 128), EPI_BIAS_GELU_F16, as, ws, maps(h->tm_n16, h->tm_n16lo, ly.w1), g,
-                           h->num_sms, st),
+      g.c16lo = h->g16lo_fp16();
+      g.c8hi = h->g8hi();
+      g.c8lo = h->g8lo();
+      TFL_CUDA(launch_gemm(gemm_bn(F, as, D > 128), EPI_BIAS_GELU_F16, as_x, ws_x,
+                           maps_x(h->tm_n16, h->tm_n16lo, h->tm_n8hi, h->tm_n8lo, ly.w1), g, h->num_sms, st),
                "ffn1 gemm");
       TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN1), "event");
     }
@@ -596,7 +675,9 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       ro.eps = eps;
       ro.h32 = h->h32;
       ro.n16 = h->n16;
-      ro.n16lo = h->n16lo;
+      ro.n16lo = h->n16lo_fp16();
+      ro.n8hi = h->n8hi();
+      ro.n8lo = h->n8lo();
       ro.out32 = bf16 ? nullptr : out;
       ro.outbf = outbf;
       if (!pre) {
@@ -615,7 +696,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
       } else {
         ro.flags |= ROW_WRITE_H | ROW_CAST16;
       }
-      const GemmMaps mp = maps(h->tm_g16, h->tm_g16lo, ly.w2);
+      const GemmMaps mp = maps_x(h->tm_g16, h->tm_g16lo, h->tm_g8hi, h->tm_g8lo, ly.w2);
       if (D == 128) {
         if (pre && !last) ro.flags |= ROW_WRITE_H;
         g.row = ro;
@@ -623,7 +704,7 @@ int enqueue(tfl_handle* h, const float* x, const int32_t* lengths, int causal, f
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
       } else {
         g.h32 = h->h32;
-        TFL_CUDA(launch_gemm(gemm_bn(D, as, false), EPI_BIAS_RES_F32, as, ws, mp, g, h->num_sms, st), "ffn2 gemm");
+        TFL_CUDA(launch_gemm(gemm_bn(D, as, false), EPI_BIAS_RES_F32, as_x, ws_x, mp, g, h->num_sms, st), "ffn2 gemm");
         TFL_CUDA(rec_mark(rec, st, TFL_KIND_GEMM_FFN2), "event");
         RowArgs ra;
         ra.c = c;
@@ -650,6 +731,7 @@ int tfl_default_options(tfl_options* o) {
   o->max_workspace_bytes = 0;
   o->use_graph = 1;
   o->whole_stack = 1;
+  o->fp8_corrections = 1;
   return TFL_OK;
 }
 
@@ -681,6 +763,8 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   tfl_default_options(&o);
   if (opt) o = *opt;
   if (o.precision < 0 || o.precision > 2) return fail(TFL_ERR_INVALID_ARG, "precision must be 0, 1 or 2");
+  if (o.fp8_corrections != 0 && o.fp8_corrections != 1)
+    return fail(TFL_ERR_INVALID_ARG, "fp8_corrections must be 0 or 1");
   if (!(o.ln_eps > 0.f)) return fail(TFL_ERR_INVALID_ARG, "ln_eps must be > 0");
   if (o.wait_timeout_ns <= 0) o.wait_timeout_ns = 2000000000LL;
 
@@ -723,6 +807,8 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   h->lay = lay;
   h->fold = use_chain(D, F, o.precision) && shape->norm_placement == 0;
   h->stack = use_stack(*shape, o);
+  // above d_model 128 the split GEMMs (QKV, FFN-in, FFN-out) take the fp8 operand form
+  h->f8 = D > 128 && o.precision == 2 && o.fp8_corrections != 0;
   auto bail = [&](int code) {
     tfl_destroy(h);
     return code;
@@ -808,7 +894,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
       if (!rc && h->fold && (l > 0 || h->stack) &&
           launch_fold_ln(tmp, 3 * D, D, d.ln1_g, d.ln1_b, d.bqkv, 0) != cudaSuccess)
         rc = fail(TFL_ERR_CUDA, "LayerNorm fold of W_qkv failed");
-      if (!rc) rc = pack_staged(tmp, n, dmax, d.wqkv, wsplit, "wq/wk/wv");
+      if (!rc) rc = pack_staged(tmp, n, dmax, d.wqkv, wsplit, "wq/wk/wv", h->f8);
     }
     if (!rc) rc = pack_weights(&src.wo, &DD, 1, tmp, dmax, d.wo, wsplit, "wo");
     {
@@ -816,14 +902,18 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
       if (!rc) rc = stage_weights(&src.w1, &FD, 1, tmp, &n, "w1");
       if (!rc && h->fold && launch_fold_ln(tmp, F, D, d.ln2_g, d.ln2_b, d.b1, 0) != cudaSuccess)
         rc = fail(TFL_ERR_CUDA, "LayerNorm fold of W1 failed");
-      if (!rc) rc = pack_staged(tmp, n, dmax, d.w1, wsplit, "w1");
+      if (!rc) rc = pack_staged(tmp, n, dmax, d.w1, wsplit, "w1", h->f8);
     }
-    if (!rc) rc = pack_weights(&src.w2, &FD, 1, tmp, dmax, d.w2, wsplit, "w2");
+    if (!rc) rc = pack_weights(&src.w2, &FD, 1, tmp, dmax, d.w2, wsplit, "w2", h->f8);
     if (!rc) {
       auto maps = [&](PackedW& pw, uint64_t rows, uint64_t cols, uint32_t box_rows) {
         bool ok = make_map_2d(&pw.tm_hi, pw.hi, rows, cols, box_rows);
-        pw.tm_lo = pw.tm_hi;
-        if (ok && pw.lo) ok = make_map_2d(&pw.tm_lo, pw.lo, rows, cols, box_rows);
+        pw.tm_lo = pw.tm_lo2 = pw.tm_hi;
+        if (ok && pw.f8)
+          ok = make_map_2d_u8(&pw.tm_lo, pw.f8hi(), rows, cols, box_rows) &&
+               make_map_2d_u8(&pw.tm_lo2, pw.f8lo(), rows, cols, box_rows);
+        else if (ok && pw.lo)
+          ok = make_map_2d(&pw.tm_lo, pw.lo, rows, cols, box_rows);
         return ok;
       };
       const int aw = o.precision == 2;
@@ -840,17 +930,7 @@ int tfl_create(const tfl_shape* shape, const tfl_weights* w, const tfl_options* 
   if ((rc = copy_f32(w->lnf_g, D, h->lnf_g, "lnf_g")) != TFL_OK) return bail(rc);
   if ((rc = copy_f32(w->lnf_b, D, h->lnf_b, "lnf_b")) != TFL_OK) return bail(rc);
 
-  const uint64_t M = (uint64_t)h->M;
-  const int atom = h->hd < 64 ? h->hd : 64;
-  bool ok = make_map_2d(&h->tm_n16, h->n16, M, D, kGemmBM) && make_map_2d(&h->tm_o16, h->o16, M, D, kGemmBM) &&
-            make_map_2d(&h->tm_g16, h->g16, M, F, kGemmBM) &&
-            (!h->n16lo || make_map_2d(&h->tm_n16lo, h->n16lo, M, D, kGemmBM)) &&
-            (!h->g16lo || make_map_2d(&h->tm_g16lo, h->g16lo, M, F, kGemmBM)) &&
-            make_map_qkv(&h->tm_q, h->qkv16, shape->B, shape->S, 3 * D, atom, kAttnBM) &&
-            make_map_qkv(&h->tm_kv, h->qkv16, shape->B, shape->S, 3 * D, atom, attn_block_n(h->hd));
-  if (!ok) return bail(fail(TFL_ERR_CUDA, "activation tensor map encoding failed"));
-  if (!h->n16lo) h->tm_n16lo = h->tm_n16;
-  if (!h->g16lo) h->tm_g16lo = h->tm_g16;
+  if (!make_activation_maps(h)) return bail(fail(TFL_ERR_CUDA, "activation tensor map encoding failed"));
   if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(cuda_fail(e, "create"));
   *out = h;
   return TFL_OK;
@@ -1195,11 +1275,12 @@ int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths, i
     float* h32;
     __half *n16, *n16lo, *qkv16, *o16, *g16, *g16lo;
     int* sched;
-    CUtensorMap tm_n16, tm_n16lo, tm_o16, tm_g16, tm_g16lo, tm_q, tm_kv;
+    CUtensorMap tm_n16, tm_n16lo, tm_o16, tm_g16, tm_g16lo, tm_q, tm_kv, tm_n8hi, tm_n8lo, tm_g8hi, tm_g8lo;
   };
-  const Intermediates saved{h->h32,    h->n16,      h->n16lo,   h->qkv16,  h->o16,    h->g16,
-                            h->g16lo,  h->sched,    h->tm_n16,  h->tm_n16lo, h->tm_o16, h->tm_g16,
-                            h->tm_g16lo, h->tm_q,   h->tm_kv};
+  const Intermediates saved{h->h32,       h->n16,     h->n16lo,   h->qkv16,   h->o16,    h->g16,
+                            h->g16lo,     h->sched,   h->tm_n16,  h->tm_n16lo, h->tm_o16, h->tm_g16,
+                            h->tm_g16lo,  h->tm_q,    h->tm_kv,   h->tm_n8hi, h->tm_n8lo, h->tm_g8hi,
+                            h->tm_g8lo};
   auto restore = [&]() {
     h->h32 = saved.h32;
     h->n16 = saved.n16;
@@ -1216,6 +1297,10 @@ int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths, i
     h->tm_g16lo = saved.tm_g16lo;
     h->tm_q = saved.tm_q;
     h->tm_kv = saved.tm_kv;
+    h->tm_n8hi = saved.tm_n8hi;
+    h->tm_n8lo = saved.tm_n8lo;
+    h->tm_g8hi = saved.tm_g8hi;
+    h->tm_g8lo = saved.tm_g8lo;
   };
   h->h32 = reinterpret_cast<float*>(sb + lay.h32);
   h->n16 = reinterpret_cast<__half*>(sb + lay.n16);
@@ -1225,21 +1310,10 @@ int tfl_forward_noalloc(tfl_handle* h, const float* x, const int32_t* lengths, i
   h->g16 = reinterpret_cast<__half*>(sb + lay.g16);
   h->g16lo = h->opt.precision == 2 ? reinterpret_cast<__half*>(sb + lay.g16lo) : nullptr;
   h->sched = reinterpret_cast<int*>(sb + lay.sched);  // zeroed by the launch sequence itself
-  const uint64_t M = (uint64_t)h->M;
-  const int D = h->D, F = h->F;
-  const int atom = h->hd < 64 ? h->hd : 64;
-  bool ok = make_map_2d(&h->tm_n16, h->n16, M, D, kGemmBM) && make_map_2d(&h->tm_o16, h->o16, M, D, kGemmBM) &&
-            make_map_2d(&h->tm_g16, h->g16, M, F, kGemmBM) &&
-            (!h->n16lo || make_map_2d(&h->tm_n16lo, h->n16lo, M, D, kGemmBM)) &&
-            (!h->g16lo || make_map_2d(&h->tm_g16lo, h->g16lo, M, F, kGemmBM)) &&
-            make_map_qkv(&h->tm_q, h->qkv16, h->shape.B, h->shape.S, 3 * D, atom, kAttnBM) &&
-            make_map_qkv(&h->tm_kv, h->qkv16, h->shape.B, h->shape.S, 3 * D, atom, attn_block_n(h->hd));
-  if (!ok) {
+  if (!make_activation_maps(h)) {
     restore();
     return fail(TFL_ERR_CUDA, "scratch tensor map encoding failed");
   }
-  if (!h->n16lo) h->tm_n16lo = h->tm_n16;
-  if (!h->g16lo) h->tm_g16lo = h->tm_g16;
   // The array keeps whatever the last call left, from any handle, shape or precision.
   // Some rows of it are read without being written first (rows of a 128-row tile that
   // lies wholly in padding, read as keys past len_b and multiplied by a zero

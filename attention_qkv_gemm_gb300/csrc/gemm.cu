@@ -15,6 +15,13 @@
 //       the producing kernel.
 // Per 16-wide k-step the MMAs A_hi*W_hi (+ A_lo*W_hi) (+ A_hi*W_lo) all
 // accumulate into the same fp32 accumulator; A_lo*W_lo (~2^-22) is dropped.
+//   F8  fp8 operand form (mode 2, both operands): the two correction terms run
+//       on the fp8 tensor path at twice the fp16 rate.  W_hi is stored as fp16
+//       times 2^11 (exact), and A and W also as e4m3(hi) and e4m3(lo 2^11);
+//       A_hi*(W_hi 2^11) (fp16) + e4m3(A_lo 2^11)*e4m3(W_hi) + e4m3(A_hi)*
+//       e4m3(W_lo 2^11) (kind::f8f6f4, K = 32) share one accumulator at the
+//       scale 2^(s+11).  The e4m3 rounding of a correction term costs ~2^-4 of
+//       a term that is itself ~2^-11 of the product.
 //
 // Epilogues (the row-wise work of section 1.A fused into the GEMM):
 //   EPI_BIAS_F16       QKV projection: c16 = acc + b_qkv
@@ -45,9 +52,14 @@ constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
 template <int BN, int AS, int WS, int EPI>
 struct GemmCfg {
+  static constexpr bool F8 = AS == 2;             // fp8 operand form (then WS == 2 too)
   static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;
   static constexpr int B_BYTES = BN * kGemmBK * 2;
-  static constexpr int STAGE = A_BYTES * (1 + AS) + B_BYTES * (1 + WS);
+  static constexpr int A8_BYTES = kGemmBM * kGemmBK;  // one e4m3 plane of the k-block (64-byte rows)
+  static constexpr int B8_BYTES = BN * kGemmBK;
+  // stage: A_hi [A_lo] W_hi [W_lo], or for F8: A_hi A8hi A8lo W_hi W8hi W8lo
+  static constexpr int STAGE = F8 ? A_BYTES + 2 * A8_BYTES + B_BYTES + 2 * B8_BYTES
+                                  : A_BYTES * (1 + AS) + B_BYTES * (1 + WS);
   // row-statistics exchange, only the row-LayerNorm epilogue has one (the space it
   // frees elsewhere buys the split-operand rings a third stage)
   static constexpr int RED_BYTES = EPI == EPI_BIAS_RES_ROW ? 4 * 2 * kGemmBM * 4 : 0;
@@ -64,6 +76,17 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T on e4m3 operands (kind::f8f6f4, K = 32); the instruction
+// descriptor's A / B format code 0 is e4m3 here, so idesc_f16's encoding serves unchanged.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(1u)
+      : "memory");
+}
 
 // Row mean / rstd of a row split over the two epilogue warps of a lane quarter.
 template <int NH>
@@ -91,6 +114,7 @@ template <int BN, int EPI, int AS, int WS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAlo,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBlo,
+                const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 const GemmArgs args) {
   using C = GemmCfg<BN, AS, WS, EPI>;
   extern __shared__ uint8_t smem_raw[];
@@ -127,6 +151,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmB);
     if (AS) tma_prefetch_desc(&tmAlo);
     if (WS) tma_prefetch_desc(&tmBlo);
+    if (C::F8) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
@@ -164,10 +192,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sa = smem + (size_t)stage * C::STAGE;
           mbar_arrive_expect_tx(&full[stage], C::STAGE);
           tma_load_2d(sa, &tmA, &full[stage], kb * kGemmBK, mb * kGemmBM);
-          if (AS) tma_load_2d(sa + C::A_BYTES, &tmAlo, &full[stage], kb * kGemmBK, mb * kGemmBM);
-          uint8_t* sb = sa + C::A_BYTES * (1 + AS);
-          tma_load_2d(sb, &tmB, &full[stage], kb * kGemmBK, nb * BN);
-          if (WS) tma_load_2d(sb + C::B_BYTES, &tmBlo, &full[stage], kb * kGemmBK, nb * BN);
+          if constexpr (C::F8) {
+            tma_load_2d(sa + C::A_BYTES, &tmAlo, &full[stage], kb * kGemmBK, mb * kGemmBM);
+            tma_load_2d(sa + C::A_BYTES + C::A8_BYTES, &tmA2, &full[stage], kb * kGemmBK, mb * kGemmBM);
+            uint8_t* sb = sa + C::A_BYTES + 2 * C::A8_BYTES;
+            tma_load_2d(sb, &tmB, &full[stage], kb * kGemmBK, nb * BN);
+            tma_load_2d(sb + C::B_BYTES, &tmBlo, &full[stage], kb * kGemmBK, nb * BN);
+            tma_load_2d(sb + C::B_BYTES + C::B8_BYTES, &tmB2, &full[stage], kb * kGemmBK, nb * BN);
+          } else {
+            if (AS) tma_load_2d(sa + C::A_BYTES, &tmAlo, &full[stage], kb * kGemmBK, mb * kGemmBM);
+            uint8_t* sb = sa + C::A_BYTES * (1 + AS);
+            tma_load_2d(sb, &tmB, &full[stage], kb * kGemmBK, nb * BN);
+            if (WS) tma_load_2d(sb + C::B_BYTES, &tmBlo, &full[stage], kb * kGemmBK, nb * BN);
+          }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == C::STAGES) {
@@ -194,16 +231,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)stage * C::STAGE);
-          const uint32_t sal = sa + C::A_BYTES;
-          const uint32_t sb = sa + C::A_BYTES * (1 + AS);
-          const uint32_t sbl = sb + C::B_BYTES;
+          if constexpr (C::F8) {
+            // fp16 A_hi * W_hi 2^11, then the e4m3 corrections (64-byte rows, 64B swizzle)
+            const uint32_t sa8h = sa + C::A_BYTES, sa8l = sa8h + C::A8_BYTES;
+            const uint32_t sb = sa8l + C::A8_BYTES;
+            const uint32_t sb8h = sb + C::B_BYTES, sb8l = sb8h + C::B8_BYTES;
 #pragma unroll
-          for (int k = 0; k < kGemmBK / 16; ++k) {
-            const uint64_t ah = sdesc(sa + k * 32, 16, 1024, kSw128);
-            const uint64_t bh = sdesc(sb + k * 32, 16, 1024, kSw128);
-            umma_f16(d, ah, bh, idesc, (kb | k) != 0);
-            if (AS) umma_f16(d, sdesc(sal + k * 32, 16, 1024, kSw128), bh, idesc, 1u);
-            if (WS) umma_f16(d, ah, sdesc(sbl + k * 32, 16, 1024, kSw128), idesc, 1u);
+            for (int k = 0; k < kGemmBK / 16; ++k)
+              umma_f16(d, sdesc(sa + k * 32, 16, 1024, kSw128), sdesc(sb + k * 32, 16, 1024, kSw128), idesc,
+                       (kb | k) != 0);
+#pragma unroll
+            for (int k = 0; k < kGemmBK / 32; ++k) {
+              umma_f8(d, sdesc(sa8l + k * 32, 16, 512, kSw64), sdesc(sb8h + k * 32, 16, 512, kSw64), idesc);
+              umma_f8(d, sdesc(sa8h + k * 32, 16, 512, kSw64), sdesc(sb8l + k * 32, 16, 512, kSw64), idesc);
+            }
+          } else {
+            const uint32_t sal = sa + C::A_BYTES;
+            const uint32_t sb = sa + C::A_BYTES * (1 + AS);
+            const uint32_t sbl = sb + C::B_BYTES;
+#pragma unroll
+            for (int k = 0; k < kGemmBK / 16; ++k) {
+              const uint64_t ah = sdesc(sa + k * 32, 16, 1024, kSw128);
+              const uint64_t bh = sdesc(sb + k * 32, 16, 1024, kSw128);
+              umma_f16(d, ah, bh, idesc, (kb | k) != 0);
+              if (AS) umma_f16(d, sdesc(sal + k * 32, 16, 1024, kSw128), bh, idesc, 1u);
+              if (WS) umma_f16(d, ah, sdesc(sbl + k * 32, 16, 1024, kSw128), idesc, 1u);
+            }
           }
           mma_issued = true;
           umma_commit(&empty[stage]);
@@ -300,6 +353,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const size_t off = (size_t)m0w * args.N + n0;
           xp_store_f16<64>(st, lane, v, args.c16 + off, args.c16lo ? args.c16lo + off : nullptr, args.N, in_rows);
+          // the fp8 operand form of the output for the next GEMM (GELU output)
+          if (args.c8hi) xp_store_f8pair<64>(st, lane, v, args.c8hi + off, args.c8lo + off, args.N, in_rows);
         }
       } else if constexpr (EPI == EPI_BIAS_RES_F32) {
 #pragma unroll 1
@@ -434,7 +489,7 @@ static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int num_sms
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
   return launch_dependent(gemm_kernel<BN, EPI, AS, WS>, grid, kGemmThreads, C::SMEM, s, mp.a, mp.alo, mp.b, mp.blo,
-                          a);
+                          mp.a2, mp.b2, a);
 }
 
 template <int BN, int EPI, int AS, int WS>
@@ -443,10 +498,14 @@ static cudaError_t prepare_one() {
                               (int)GemmCfg<BN, AS, WS, EPI>::SMEM);
 }
 
-// Every (BN, EPI) pair the planner uses, at the three operand modes (AS, WS) = (0,0), (0,1), (1,1).
+// Every (BN, EPI) pair the planner uses, at the three fp16 operand modes (AS, WS) = (0,0),
+// (0,1), (1,1); and the pairs that run in the fp8 operand form (2,2) above d_model 128.
 #define TFL_GEMM_VARIANTS(X)                                                                       \
   X(128, EPI_BIAS_F16) X(256, EPI_BIAS_F16) X(128, EPI_BIAS_GELU_F16) X(256, EPI_BIAS_GELU_F16) \
   X(128, EPI_BIAS_RES_F32) X(256, EPI_BIAS_RES_F32) X(128, EPI_BIAS_RES_ROW)
+#define TFL_GEMM_F8_VARIANTS(X)                                                                    \
+  X(128, EPI_BIAS_F16) X(256, EPI_BIAS_F16) X(128, EPI_BIAS_GELU_F16) X(256, EPI_BIAS_GELU_F16) \
+  X(128, EPI_BIAS_RES_F32)
 
 cudaError_t prepare_gemm_kernels() {
   cudaError_t e = cudaSuccess;
@@ -456,12 +515,23 @@ cudaError_t prepare_gemm_kernels() {
   if (e == cudaSuccess) e = prepare_one<BN, EPI, 1, 1>();
   TFL_GEMM_VARIANTS(TFL_PREP)
 #undef TFL_PREP
+#define TFL_PREP_F8(BN, EPI) \
+  if (e == cudaSuccess) e = prepare_one<BN, EPI, 2, 2>();
+  TFL_GEMM_F8_VARIANTS(TFL_PREP_F8)
+#undef TFL_PREP_F8
   return e;
 }
 
 cudaError_t launch_gemm(int bn, int epi, int as, int ws, const GemmMaps& mp, const GemmArgs& a, int num_sms,
                         cudaStream_t s) {
-  if (as && !ws) return cudaErrorInvalidValue;
+  if ((as && !ws) || ((as == 2) != (ws == 2))) return cudaErrorInvalidValue;
+  if (as == 2) {
+#define TFL_LAUNCH_F8(BN, EPI) \
+  if (bn == BN && epi == EPI) return launch_one<BN, EPI, 2, 2>(mp, a, num_sms, s);
+    TFL_GEMM_F8_VARIANTS(TFL_LAUNCH_F8)
+#undef TFL_LAUNCH_F8
+    return cudaErrorInvalidValue;
+  }
 #define TFL_LAUNCH(BN, EPI)                                      \
   if (bn == BN && epi == EPI) {                                  \
     if (as) return launch_one<BN, EPI, 1, 1>(mp, a, num_sms, s); \

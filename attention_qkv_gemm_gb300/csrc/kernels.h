@@ -36,6 +36,10 @@ struct RowOps {
   float* h32 = nullptr;                      // [M, D]
   __half* n16 = nullptr;                     // [M, D] fp16 (hi part when split)
   __half* n16lo = nullptr;                   // [M, D] fp16 residual plane, or null
+  // fp8 operand form (instead of n16lo): e4m3 of the fp16 value and e4m3 of its
+  // rounding residual times 2^11, [M, D] bytes each
+  uint8_t* n8hi = nullptr;
+  uint8_t* n8lo = nullptr;
   float* out32 = nullptr;                    // [M, D]
   __nv_bfloat16* outbf = nullptr;            // [M, D] bf16 model output instead of out32 (FINAL)
 };
@@ -67,6 +71,8 @@ struct GemmArgs {
   const float* bias = nullptr;   // [N]
   __half* c16 = nullptr;         // [M, N] for the fp16 epilogues
   __half* c16lo = nullptr;       // [M, N] residual plane (split activations), or null
+  uint8_t* c8hi = nullptr;       // fp8 operand form of c16 (instead of c16lo): e4m3(c16) and
+  uint8_t* c8lo = nullptr;       //   e4m3(residual * 2^11), [M, N] bytes each
   const float* res = nullptr;    // [M, N] residual for the fp32 epilogues (may alias h32)
   float* h32 = nullptr;          // EPI_BIAS_RES_F32 output
   RowOps row;                    // EPI_BIAS_RES_ROW
@@ -181,8 +187,11 @@ cudaError_t prepare_stack_kernel();
 cudaError_t launch_stack(const StackMaps& mp, const StackArgs& a, int num_sms, cudaStream_t s);
 
 // TMA descriptors of one GEMM: A (and its lo plane), W (and its lo part).
+// Operand maps.  Split fp16 form: a / alo, b / blo are the hi / lo planes.  fp8 operand form
+// (operand mode 2): a, b the fp16 hi planes (b pre-scaled by 2^11), alo / blo the e4m3 copies
+// of the hi planes, a2 / b2 the e4m3 residual planes (times 2^11).
 struct GemmMaps {
-  CUtensorMap a, alo, b, blo;
+  CUtensorMap a, alo, b, blo, a2, b2;
 };
 
 // Launch with programmatic dependent launch allowed (the kernel waits on the
@@ -204,7 +213,8 @@ inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 bloc
 }
 
 // Launchers (return cudaError_t of the launch).
-// as: A carries a lo plane; ws: W carries a lo part (as requires ws).
+// as / ws: 1 = A / W carries an fp16 lo plane (as requires ws); 2 = both in the fp8 operand
+// form (as == 2 requires ws == 2).
 cudaError_t launch_gemm(int bn, int epi, int as, int ws, const GemmMaps& mp, const GemmArgs& a, int num_sms,
                         cudaStream_t s);
 cudaError_t launch_attention(int hd, const CUtensorMap& tq, const CUtensorMap& tkv, const AttnArgs& a,
@@ -220,6 +230,10 @@ cudaError_t launch_absmax(const float* src, size_t n, unsigned* out, cudaStream_
 cudaError_t launch_fold_ln(float* w, int rows, int cols, const float* gamma, const float* beta, float* bias,
                            cudaStream_t s);
 cudaError_t launch_split_f16(const float* src, __half* hi, __half* lo, size_t n, float scale, cudaStream_t s);
+// fp8 operand form of x * scale: hi16 = fp16(x s) 2^11 (exact), hi8 = e4m3(fp16(x s)),
+// lo8 = e4m3((x s - fp16(x s)) 2^11).
+cudaError_t launch_split_f8(const float* src, __half* hi16, uint8_t* hi8, uint8_t* lo8, size_t n, float scale,
+                            cudaStream_t s);
 cudaError_t launch_probe_wait(int* status, int64_t timeout_ns, cudaStream_t s);
 
 // Tile sizes shared by the host planner and the kernels.

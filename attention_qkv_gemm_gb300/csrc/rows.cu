@@ -12,6 +12,7 @@
 #include "kernels.h"
 #include "mathfn.cuh"
 #include "ptx.cuh"
+#include "xpose.cuh"
 
 namespace tfl {
 
@@ -61,6 +62,18 @@ __device__ __forceinline__ void store_h4(__half* p, __half* lo, float4 v) {
     w.y = *reinterpret_cast<uint32_t*>(&rb);
     *reinterpret_cast<uint2*>(lo) = w;
   }
+}
+
+// The same 4 values in the fp8 operand form (with the fp16 hi part stored by store_h4):
+// e4m3(fp16(v)) at hi8, e4m3((v - fp16(v)) 2^11) at lo8, 4 bytes each.
+__device__ __forceinline__ void store_f8pair4(uint8_t* hi8, uint8_t* lo8, float4 v) {
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  float h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __half2float(__float2half_rn(x[i]));
+  *reinterpret_cast<uint32_t*>(hi8) = e4m3x4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint32_t*>(lo8) = e4m3x4((x[0] - h[0]) * kF8LoScale, (x[1] - h[1]) * kF8LoScale,
+                                              (x[2] - h[2]) * kF8LoScale, (x[3] - h[3]) * kF8LoScale);
 }
 
 template <int V>
@@ -117,12 +130,14 @@ __global__ void __launch_bounds__(256) rows_kernel(const RowArgs a) {
     for (int k = 0; k < V; ++k) {
       const size_t off = (size_t)m * D + (k * 32 + lane) * 4;
       store_h4(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, y[k]);
+      if (ro.n8hi) store_f8pair4(ro.n8hi + off, ro.n8lo + off, y[k]);
     }
   } else if (ro.flags & ROW_CAST16) {
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       const size_t off = (size_t)m * D + (k * 32 + lane) * 4;
       store_h4(ro.n16 + off, ro.n16lo ? ro.n16lo + off : nullptr, t[k]);
+      if (ro.n8hi) store_f8pair4(ro.n8hi + off, ro.n8lo + off, t[k]);
     }
   }
 }
@@ -258,6 +273,27 @@ __global__ void split_f16_kernel(const float* __restrict__ src, __half* __restri
     hi[i] = h;
     if (lo) lo[i] = __float2half_rn(v - __half2float(h));
   }
+}
+
+// fp8 operand form of x * scale (see launch_split_f8).
+__global__ void split_f8_kernel(const float* __restrict__ src, __half* __restrict__ hi16, uint8_t* __restrict__ hi8,
+                                uint8_t* __restrict__ lo8, size_t n, float scale) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = src[i] * scale;
+    const float h = __half2float(__float2half_rn(v));
+    hi16[i] = __float2half_rn(h * kF8LoScale);  // exact: a power-of-two multiple of an fp16 value below 2^5
+    hi8[i] = (uint8_t)(e4m3x2(h, 0.f) & 0xffu);
+    lo8[i] = (uint8_t)(e4m3x2((v - h) * kF8LoScale, 0.f) & 0xffu);
+  }
+}
+
+cudaError_t launch_split_f8(const float* src, __half* hi16, uint8_t* hi8, uint8_t* lo8, size_t n, float scale,
+                            cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  size_t grid = (n + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  split_f8_kernel<<<(unsigned)grid, 256, 0, s>>>(src, hi16, hi8, lo8, n, scale);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_split_f16(const float* src, __half* hi, __half* lo, size_t n, float scale, cudaStream_t s) {

@@ -107,6 +107,59 @@ __device__ __forceinline__ void pack_bf16(const float* v, uint4* o) {
   }
 }
 
+// ---- fp8 operand form: a value v is carried as h = fp16(v), e4m3(h) and e4m3((v - h) 2^11);
+// the tensor core multiplies the e4m3 planes (kind::f8f6f4) for the two correction terms of a
+// split product, at the scale 2^11 the fp16 product of h with weights pre-scaled by 2^11 shares.
+constexpr float kF8LoScale = 2048.0f;
+
+// Two fp32 values as e4m3 (round to nearest even, saturating), a in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));  // first source -> high byte
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+
+// N values (N multiple of 16) -> the two e4m3 planes of their fp16 rounding, N/16 x 16 bytes each.
+template <int N>
+__device__ __forceinline__ void pack_f8pair(const float* v, uint4* hi8, uint4* lo8) {
+#pragma unroll
+  for (int q = 0; q < N / 16; ++q) {
+    uint32_t wh[4], wl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float* x = v + 16 * q + 4 * k;
+      float h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __half2float(__float2half_rn(x[i]));
+      wh[k] = e4m3x4(h[0], h[1], h[2], h[3]);
+      wl[k] = e4m3x4((x[0] - h[0]) * kF8LoScale, (x[1] - h[1]) * kF8LoScale, (x[2] - h[2]) * kF8LoScale,
+                     (x[3] - h[3]) * kF8LoScale);
+    }
+    hi8[q] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    lo8[q] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  }
+}
+
+// Store the two e4m3 planes of N columns (N = 64) of the warp's 32 rows through the stage.
+template <int N>
+__device__ __forceinline__ void xp_store_f8pair(uint8_t* st, int lane, const float* v, uint8_t* hi_row0,
+                                                uint8_t* lo_row0, size_t pitch_bytes, uint32_t rows) {
+  using X = XStage<N>;
+  uint4 h[N / 16], l[N / 16];
+  pack_f8pair<N>(v, h, l);
+  X::put_row(st, lane, h);
+  __syncwarp();
+  X::store_rows(st, lane, hi_row0, pitch_bytes, rows);
+  __syncwarp();
+  X::put_row(st, lane, l);
+  __syncwarp();
+  X::store_rows(st, lane, lo_row0, pitch_bytes, rows);
+  __syncwarp();
+}
+
 // Store N bf16 columns (N = 32 or 64) of the warp's 32 rows through the stage.
 template <int N>
 __device__ __forceinline__ void xp_store_bf16(uint8_t* st, int lane, const float* v, __nv_bfloat16* row0,

@@ -616,7 +616,8 @@ def main():
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tc_peak,
                 "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": ncu_traffic(dom, shape.name),
                 "algorithmic_flops_per_launch": fl,
-                "note": "split-fp16 operands execute 3 MMAs per 16-wide k-step (2 for o_proj); achieved counts "
+                "note": "split operands: per 16-wide k-step an fp16 product and two e4m3 correction products "
+                        "at twice the fp16 rate (two fp16 MMAs' time; o_proj: two fp16 MMAs); achieved counts "
                         "the algorithmic 2*M*N*K only"}
     else:
         by = kernel_bytes(dom, shape, alg["valid_tokens"])

@@ -92,6 +92,11 @@ typedef struct {
  *   1  weights split (two MMAs per k-step)
  *   2  weights split, and the GEMM activations (normed rows, GELU output)
  *      split too (three MMAs per k-step; the default)
+ * fp8_corrections (precision 2, d_model > 128): the two correction terms of a
+ *   split product, A_lo W_hi and A_hi W_lo, run as e4m3 MMAs (kind::f8f6f4,
+ *   twice the fp16 rate) on e4m3 copies of the hi parts and of the lo parts
+ *   times 2^11, beside the fp16 A_hi W_hi; a k-step then costs two fp16 MMAs'
+ *   time instead of three.  1 (default) on, 0: fp16 lo planes as at d_model 128.
  */
 typedef struct {
     int32_t precision;            /* 0, 1 or 2 (default 2), see above */
@@ -102,6 +107,7 @@ typedef struct {
     int32_t whole_stack;          /* 1 (default): run every layer in one kernel where the
                                      shape allows it (d_model 128, head_dim 32, S <= 128,
                                      precision 2, d_ff <= 2048, n_layers <= 8); 0: per-layer kernels */
+    int32_t fp8_corrections;      /* 1 (default) or 0, see above */
 } tfl_options;
 
 /* Fill *opt with the defaults above.  Returns TFL_OK or TFL_ERR_INVALID_ARG. */

@@ -8,13 +8,15 @@ import synth
 
 
 def run_gpu(shape: synth.Shape, prm, x: np.ndarray, lens, causal: bool, norm_placement: int = 0,
-            use_graph: bool = True, repeat: int = 1):
+            use_graph: bool = True, repeat: int = 1, fp8_corrections: int = None):
     """Run the library forward on cuda:0; returns (out numpy, status code)."""
     import torch
     import attention_qkv_gemm_gb300 as pkg
 
     opts = pkg.tfl_default_options()
     opts.use_graph = 1 if use_graph else 0
+    if fp8_corrections is not None:
+        opts.fp8_corrections = fp8_corrections
     m = pkg.TransformerStack(shape.B, shape.S, shape.d_model, shape.n_heads, shape.d_ff, shape.n_layers, prm,
                              norm_placement=norm_placement, options=opts)
     try:

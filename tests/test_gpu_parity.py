@@ -4,7 +4,8 @@ Every case compares all B*S*D outputs (padded rows must be exactly zero)
 with the graded rule |u - r| <= 2e-3 or <= 0.02 |r|.  Shapes span several
 128-row tiles with a ragged tail (S not a multiple of 128), every supported
 head_dim (32, 64, 256), d_model 128 (fused LayerNorm epilogues) and 1024
-(separate row kernel), causal and key-padding masks, pre- and post-LN.
+(separate row kernel; the split GEMMs' correction terms on the e4m3 tensor path, and as fp16
+products with fp8_corrections = 0), causal and key-padding masks, pre- and post-LN.
 """
 import numpy as np
 import pytest
@@ -16,12 +17,14 @@ from tests.helpers import assert_gate, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-def case(B, S, D, H, F, L, causal, lens, seed=0, norm_placement=0, ln_affine="random", use_graph=True):
+def case(B, S, D, H, F, L, causal, lens, seed=0, norm_placement=0, ln_affine="random", use_graph=True,
+         fp8_corrections=None):
     shape = synth.Shape(B, S, D, H, F, L, causal)
     prm = synth.params(seed, shape, ln_affine=ln_affine)
     x = synth.input_x(seed, shape)
     lens = None if lens is None else np.asarray(lens, dtype=np.int32)
-    u, rc = run_gpu(shape, prm, x, lens, causal, norm_placement, use_graph=use_graph)
+    u, rc = run_gpu(shape, prm, x, lens, causal, norm_placement, use_graph=use_graph,
+                    fp8_corrections=fp8_corrections)
     assert rc == 0
     r = oracle.forward(prm, H, x, lens, causal, norm_placement)
     if lens is not None:
@@ -55,6 +58,13 @@ def test_d1024_hd256(causal):
 
 def test_d1024_hd64():
     case(2, 300, 1024, 16, 512, 1, True, [300, 150], seed=2)
+
+
+def test_d1024_fp16_correction_products():
+    # fp8_corrections = 0: above d_model 128 the correction terms of the split GEMMs run as fp16
+    # products on fp16 lo planes (the default carries them on the e4m3 tensor path)
+    case(2, 300, 1024, 16, 512, 1, True, [300, 150], seed=2, fp8_corrections=0)
+    case(1, 160, 1024, 4, 512, 2, False, [100], seed=3, norm_placement=1, fp8_corrections=0)
 
 
 def test_d1024_post_ln():
