@@ -226,13 +226,9 @@ KERNEL_HEADERS = ["kernels.h", "ptx.cuh", "mathfn.cuh", "xpose.cuh", "chainops.c
 NCU_TRAFFIC = {
     # (kernel, workload): (kernel source fingerprint, bytes per launch); entries whose
     # fingerprint no longer matches the sources report null
-    ("postchain", "B64_S1024_D128_causal_ragged"): ("048a2bf32bcb", 42.617344e6 + 29.616384e6),
-    ("stack", "B2048_S128_D128_H4_F512_L4_keymask"): ("1cb6d8ecd97e", 87.629568e6 + 86.65088e6),  # lengths U[32,128]
-    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("6bbea9362b5c", 208.719104e6 + 50.630144e6),
-    ("gemm_qkv", "B16_S512_D1024_H4_causal"): ("6c76d0778da6", 46.366208e6 + 12.38656e6),
-    ("gemm_oproj", "B16_S512_D1024_H4_causal"): ("6c76d0778da6", 54.559744e6 + 2.208256e6),
-    ("gemm_ffn1", "B16_S512_D1024_H4_causal"): ("6c76d0778da6", 51.211776e6 + 85.44256e6),
-    ("gemm_ffn2", "B16_S512_D1024_H4_causal"): ("6c76d0778da6", 187.330816e6 + 20.681472e6),
+    ("postchain", "B64_S1024_D128_causal_ragged"): ("3308ef9bf974", 42.620416e6 + 29.589504e6),
+    ("stack", "B2048_S128_D128_H4_F512_L4_keymask"): ("ee76cb851076", 87.525632e6 + 86.630912e6),  # lengths U[32,128]
+    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("eec525caff10", 208.818688e6 + 49.862656e6),
 }
 
 
