@@ -381,6 +381,13 @@ def reference_arm(args, shape, world, rank):
     return 0
 
 
+def compute_dtype(shape) -> str:
+    """Arithmetic types of the path: fp16 tensor-core products on split operands (fp32
+    accumulation and fp32 row work), plus e4m3 products for the split GEMMs' correction terms
+    above d_model 128 (the library's default fp8_corrections)."""
+    return "f16+e4m3" if shape.d_model > 128 else "f16"
+
+
 def e2e_slice(shape, arg: int) -> int:
     """Sequences per slice of the streamed end-to-end path: 0 (no slicing: tfl_forward_host)
     unless the fp32 input is over 4 GB, else a sixteenth of the batch (at least one sequence):
@@ -699,7 +706,8 @@ def main():
     line = {
         "metric": "forward_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16", "data": "synthetic", "config": config_dict(shape), "roofline": roof, "cpu_baseline": cpu,
+        "dtype": compute_dtype(shape), "data": "synthetic", "config": config_dict(shape), "roofline": roof,
+        "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "algorithmic": {"valid_tokens": alg["valid_tokens"], "gflop": (alg["linear_flops"] + alg["attn_flops"]) / 1e9,
                         "tflops_achieved": (alg["linear_flops"] + alg["attn_flops"]) / (ms / 1e3) / 1e12,

@@ -111,3 +111,9 @@ def test_e2e_slice_rule():
     assert bench.e2e_slice(many, 0) == 0         # B10000 S128, 655 MB: no slicing
     assert bench.e2e_slice(big, -1) == 0 and bench.e2e_slice(big, 5) == 5
     assert bench.e2e_slice(small, 100) == small.B
+
+
+def test_compute_dtype_names_the_fp8_correction_products():
+    assert bench.compute_dtype(synth.WORKLOADS[4]) == "f16+e4m3"
+    assert bench.compute_dtype(synth.WORKLOADS[3]) == "f16+e4m3"
+    assert bench.compute_dtype(synth.WORKLOADS[1]) == "f16"
