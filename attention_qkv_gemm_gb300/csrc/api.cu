@@ -150,7 +150,8 @@ struct WsLayout {
 // Ints before the tile list in the scheduling area.
 inline size_t tile_list_offset(int n_layers) { return align_up((size_t)n_layers, 32); }
 
-// precision 2 adds the lo planes of the GEMM activations (normed rows, GELU output).
+// precision 2 adds the lo planes of the GEMM activations (normed rows, GELU output); in the fp8
+// operand form the same bytes hold their two e4m3 planes.
 WsLayout ws_layout(const tfl_shape& s, int precision) {
   const size_t M = (size_t)s.B * s.S, D = s.d_model, F = s.d_ff;
   WsLayout w{};

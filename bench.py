@@ -173,7 +173,8 @@ def gemm_flops(kind: str, shape: synth.Shape, valid: float):
 
 def kernel_bytes(kind: str, shape: synth.Shape, valid: float):
     """Algorithmic HBM bytes per launch of the row-streaming kernels (valid rows only;
-    default precision: GEMM activations carry fp16 hi and lo planes)."""
+    default precision: GEMM activations carry an fp16 hi plane and, in the same bytes as an fp16
+    lo plane, its lo plane or its two e4m3 planes)."""
     D, F, L = shape.d_model, shape.d_ff, shape.n_layers
     # the fused chain (d_model 128), averaged over the forward's L launches: attention output
     # in, residual in, then either residual out + the next layer's qkv (fp16; its QKV
