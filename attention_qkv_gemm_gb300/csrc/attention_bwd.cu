@@ -26,7 +26,12 @@
 // P and dS as fp16 pairs written over S and dP, which the next MMAs read as A
 // operands from tensor memory.  Warps: 0 MMA issuer and TMEM owner, 1 TMA
 // producer, 2-5 elementwise and output.  Work items (b, h, 128-row block) are
-// dealt round-robin, heaviest first under causal.
+// dealt round-robin, heaviest first under causal.  dQ double-buffers S in tensor
+// memory (it has room beside dP and one accumulator): the next step's S, and its dP
+// once the elementwise warps hold the current dP in registers, are computed while
+// those warps work, so the tensor core no longer waits for each step's elementwise
+// pass.  dK/dV fills tensor memory with S, dP and two accumulators and runs each step
+// after the previous one's elementwise pass.
 #include <type_traits>
 
 #include "kernels.h"
@@ -44,8 +49,12 @@ struct BwdCfg {
   static constexpr uint32_t SWZ = ROWB == 64 ? kSw64 : kSw128;
   static constexpr int RES = BM * ROWB;          // one resident tile
   static constexpr int STEP = BN * ROWB;         // one streamed tile
-  static constexpr int NST = 2;                  // stages of streamed tile pairs
-  static constexpr int S_COL = 0, DP_COL = 64, ACC_COL = 128;
+  // stages of streamed tile pairs: dQ pipelines the next step's S and dP under the current
+  // step's elementwise work, so a stage frees one step later there
+  static constexpr int NST = MODE == 0 ? 3 : 2;
+  // tensor memory: dQ keeps two S buffers (step parity) beside dP and the accumulator;
+  // dK/dV holds S, dP and two accumulators
+  static constexpr int S_COL = 0, DP_COL = MODE == 0 ? 128 : 64, ACC_COL = MODE == 0 ? 192 : 128;
   static constexpr int TMEM_COLS = 256;
   static constexpr int STAGE_F = MODE == 1 ? 2 * 2 * BN : 0;  // lse2 / D of the step's queries, two buffers
   static constexpr size_t SMEM = 1024 + 2 * (size_t)RES + (size_t)NST * 2 * STEP + STAGE_F * 4 + 256;
@@ -106,7 +115,8 @@ __global__ void __launch_bounds__(192, 2)
   uint64_t* acc_full = bars + 4;
   uint64_t* acc_empty = bars + 5;
   uint64_t* drain = bars + 6;
-  uint64_t* b_full = bars + 7;            // [NST]
+  uint64_t* dp_read = bars + 7;           // dQ: elementwise -> MMA, the step's dP is in registers
+  uint64_t* b_full = bars + 8;            // [NST]
   uint64_t* b_empty = b_full + C::NST;    // [NST]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_empty + C::NST);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -121,6 +131,7 @@ __global__ void __launch_bounds__(192, 2)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
     mbar_init(drain, 1);
+    mbar_init(dp_read, 4);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
@@ -203,7 +214,7 @@ __global__ void __launch_bounds__(192, 2)
       constexpr uint32_t id_acc = idesc_f16(128, HD, 0, 1);
       const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
       int st = 0;
-      uint32_t sph = 0, rph = 0, xph = 0, aph = 0;
+      uint32_t sph = 0, rph = 0, xph = 0, aph = 0, dph = 0;
       bool first_item = true, ok = true;
       for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
         BwdItem it;
@@ -217,6 +228,82 @@ __global__ void __launch_bounds__(192, 2)
           aph ^= 1u;
         }
         tc_fence_after();
+        if constexpr (MODE == 0) {
+          // dQ, pipelined: S of step s goes to S buffer (s - s0) & 1 as soon as its tiles are
+          // in (that buffer last held dS of step s - 2, read by the dQ MMAs issued before);
+          // dP of step s once the elementwise warps have dP of step s - 1 in registers.  The
+          // next step's S and dP thus compute while the elementwise warps work on the current
+          // one.  Step s is released to them (s_full) only after x_full of step s - 1 is seen,
+          // so neither barrier runs more than one phase ahead of its waiter; then dQ += dS K
+          // of step s - 1.
+          int prev_st = 0;  // stage of step s - 1
+          for (int s = s0; s <= s1 && ok; ++s) {
+            int cur_st = st;
+            if (s < s1) {
+              if (!wait_bounded(&b_full[st], sph, wc)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t b1 = smem_u32(sB + (size_t)st * 2 * C::STEP), b2 = b1 + C::STEP;
+              const uint64_t ad1 = sdesc(a1, 16, 8 * C::ROWB, C::SWZ), ad2 = sdesc(a2, 16, 8 * C::ROWB, C::SWZ);
+              const uint64_t bd1 = sdesc(b1, 16, 8 * C::ROWB, C::SWZ), bd2 = sdesc(b2, 16, 8 * C::ROWB, C::SWZ);
+              const uint32_t s_col = C::S_COL + 64 * ((s - s0) & 1);
+#pragma unroll
+              for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk * 32) >> 4);
+                umma_f16(tmem_base + s_col, ad1 + off, bd1 + off, id_s, kk > 0 ? 1u : 0u);
+              }
+              if (s > s0) {
+                if (!wait_bounded(dp_read, dph, wc)) {
+                  ok = false;
+                  break;
+                }
+                dph ^= 1u;
+                tc_fence_after();
+              }
+#pragma unroll
+              for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk * 32) >> 4);
+                umma_f16(tmem_base + C::DP_COL, ad2 + off, bd2 + off, id_s, kk > 0 ? 1u : 0u);
+              }
+              mma_issued = true;
+              if (++st == C::NST) {
+                st = 0;
+                sph ^= 1u;
+              }
+            } else if (s > s0) {
+              // the last step's dP read (every step's dp_read phase is consumed once)
+              if (!wait_bounded(dp_read, dph, wc)) {
+                ok = false;
+                break;
+              }
+              dph ^= 1u;
+            }
+            if (s > s0) {
+              if (!wait_bounded(x_full, xph, wc)) {
+                ok = false;
+                break;
+              }
+              xph ^= 1u;
+              tc_fence_after();
+            }
+            if (s < s1) umma_commit(s_full);
+            if (s > s0) {
+              const uint64_t bd1 = sdesc(smem_u32(sB + (size_t)prev_st * 2 * C::STEP), C::STEP, 8 * C::ROWB, C::SWZ);
+              const uint32_t ds_col = C::S_COL + 64 * ((s - 1 - s0) & 1);
+              const bool acc0 = s - 1 > s0;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t off = (uint32_t)((kk * 16 * C::ROWB) >> 4);
+                umma_f16_ts(tmem_base + C::ACC_COL, tmem_base + ds_col + 8 * kk, bd1 + off, id_acc,
+                            (acc0 || kk > 0) ? 1u : 0u);
+              }
+              umma_commit(&b_empty[prev_st]);
+            }
+            prev_st = cur_st;
+          }
+        } else {
         int pst = 0;  // stage of the step whose second half (accumulating MMAs) is pending
         for (int s = s0; s <= s1 && ok; ++s) {
           if (s < s1) {
@@ -274,6 +361,7 @@ __global__ void __launch_bounds__(192, 2)
             }
           }
         }
+        }
         if (!ok) break;
         umma_commit(res_empty);
         umma_commit(acc_full);
@@ -287,6 +375,10 @@ __global__ void __launch_bounds__(192, 2)
     const int r = q * 32 + lane;     // resident row == TMEM lane
     const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16);
     const float sl2 = args.scale_log2;
+    // dK/dV's elementwise warps meet at a named barrier each step: they leave only on their own
+    // bound, never on another waiter's abort, so that all four leave at the same point
+    WaitCtl ewc = wc;
+    ewc.early_exit = MODE == 0;
     uint32_t sph = 0, aph = 0;
     int sbuf = 0;
     for (int i = blockIdx.x; i < items; i += gridDim.x) {
@@ -311,7 +403,7 @@ __global__ void __launch_bounds__(192, 2)
           sf[t] = v;
           elem_bar();
         }
-        if (!wait_bounded(s_full, sph, wc)) {
+        if (!wait_bounded(s_full, sph, ewc)) {
           ok = false;
           break;
         }
@@ -322,58 +414,80 @@ __global__ void __launch_bounds__(192, 2)
         const int wr0 = it.blk * 128 + q * 32;  // this warp's first resident row
         const bool unmasked = wr0 + 31 < it.len && c0 + 63 < it.len &&
                               (!args.causal || (MODE == 0 ? c0 + 63 <= wr0 : wr0 + 31 <= c0));
-        auto step = [&](auto full_tag) {
+        // P and dS of 32 columns of the step (half 0 or 1) from S and dP in registers
+        auto ew_half = [&](auto full_tag, int half, const float* sv, const float* dv, uint32_t* pp, uint32_t* dd) {
           constexpr bool FULL = decltype(full_tag)::value;
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            float sv[32], dv[32];
-            tmem_ld32(t_row + C::S_COL + 32 * half, sv);
-            tmem_ld32(t_row + C::DP_COL + 32 * half, dv);
-            tmem_wait_ld();
-            uint32_t pp[16], dd[16];
 #pragma unroll
-            for (int e0 = 0; e0 < 32; e0 += 8) {
-              // the 8 columns' log-sum-exp and row sums: per-thread constants for dQ (row =
-              // query), per column from the step's shared staging for dK/dV (row = key)
-              float lse8[8], d8[8];
-              if (MODE == 0) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                  lse8[k] = lse_r;
-                  d8[k] = d_r;
-                }
-              } else {
-                const float4* l4 = reinterpret_cast<const float4*>(sf + 32 * half + e0);
-                const float4* d4 = reinterpret_cast<const float4*>(sf + 64 + 32 * half + e0);
-                const float4 la = l4[0], lb = l4[1], da = d4[0], db = d4[1];
-                lse8[0] = la.x; lse8[1] = la.y; lse8[2] = la.z; lse8[3] = la.w;
-                lse8[4] = lb.x; lse8[5] = lb.y; lse8[6] = lb.z; lse8[7] = lb.w;
-                d8[0] = da.x; d8[1] = da.y; d8[2] = da.z; d8[3] = da.w;
-                d8[4] = db.x; d8[5] = db.y; d8[6] = db.z; d8[7] = db.w;
-              }
-#pragma unroll
-              for (int e = e0; e < e0 + 8; e += 2) {
-                float p2[2], ds2[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  const int col = c0 + 32 * half + e + k;  // streamed position
-                  bool allowed = true;
-                  if constexpr (!FULL)
-                    allowed = MODE == 0 ? (row < it.len && col < it.len && (!args.causal || col <= row))
-                                        : (row < it.len && col < it.len && (!args.causal || row <= col));
-                  const float p = allowed ? ex2(fmaf(sv[e + k], sl2, -lse8[e - e0 + k])) : 0.f;
-                  p2[k] = p;
-                  ds2[k] = p * (dv[e + k] - d8[e - e0 + k]);
-                }
-                const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
-                const __half2 hd = __floats2half2_rn(ds2[0], ds2[1]);
-                pp[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
-                dd[e / 2] = *reinterpret_cast<const uint32_t*>(&hd);
-              }
-            }
+          for (int e0 = 0; e0 < 32; e0 += 8) {
+            // the 8 columns' log-sum-exp and row sums: per-thread constants for dQ (row =
+            // query), per column from the step's shared staging for dK/dV (row = key)
+            float lse8[8], d8[8];
             if (MODE == 0) {
-              tmem_st16_u(t_row + C::S_COL + 16 * half, dd);   // dS over S
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                lse8[k] = lse_r;
+                d8[k] = d_r;
+              }
             } else {
+              const float4* l4 = reinterpret_cast<const float4*>(sf + 32 * half + e0);
+              const float4* d4 = reinterpret_cast<const float4*>(sf + 64 + 32 * half + e0);
+              const float4 la = l4[0], lb = l4[1], da = d4[0], db = d4[1];
+              lse8[0] = la.x; lse8[1] = la.y; lse8[2] = la.z; lse8[3] = la.w;
+              lse8[4] = lb.x; lse8[5] = lb.y; lse8[6] = lb.z; lse8[7] = lb.w;
+              d8[0] = da.x; d8[1] = da.y; d8[2] = da.z; d8[3] = da.w;
+              d8[4] = db.x; d8[5] = db.y; d8[6] = db.z; d8[7] = db.w;
+            }
+#pragma unroll
+            for (int e = e0; e < e0 + 8; e += 2) {
+              float p2[2], ds2[2];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int col = c0 + 32 * half + e + k;  // streamed position
+                bool allowed = true;
+                if constexpr (!FULL)
+                  allowed = MODE == 0 ? (row < it.len && col < it.len && (!args.causal || col <= row))
+                                      : (row < it.len && col < it.len && (!args.causal || row <= col));
+                const float p = allowed ? ex2(fmaf(sv[e + k], sl2, -lse8[e - e0 + k])) : 0.f;
+                p2[k] = p;
+                ds2[k] = p * (dv[e + k] - d8[e - e0 + k]);
+              }
+              const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
+              const __half2 hd = __floats2half2_rn(ds2[0], ds2[1]);
+              pp[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+              dd[e / 2] = *reinterpret_cast<const uint32_t*>(&hd);
+            }
+          }
+        };
+        auto step = [&](auto full_tag) {
+          if constexpr (MODE == 0) {
+            // dQ: the whole dP and the first half of S come in together; once dP is in
+            // registers the MMA thread may compute the next step's dP, and the next step's
+            // S already goes to the other S buffer.  dS is written over this step's S.
+            const uint32_t s_buf = t_row + C::S_COL + 64 * ((s - s0) & 1);
+            float sv[32], dv[32], dn[32];
+            uint32_t pp[16], dd[16];
+            tmem_ld32(s_buf, sv);
+            tmem_ld32(t_row + C::DP_COL, dv);
+            tmem_ld32(t_row + C::DP_COL + 32, dn);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dp_read);
+            ew_half(full_tag, 0, sv, dv, pp, dd);
+            tmem_st16_u(s_buf, dd);  // dS over S, columns 0-31 of the step
+            tmem_ld32(s_buf + 32, sv);
+            tmem_wait_ld();
+            ew_half(full_tag, 1, sv, dn, pp, dd);
+            tmem_st16_u(s_buf + 16, dd);
+          } else {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              float sv[32], dv[32];
+              tmem_ld32(t_row + C::S_COL + 32 * half, sv);
+              tmem_ld32(t_row + C::DP_COL + 32 * half, dv);
+              tmem_wait_ld();
+              uint32_t pp[16], dd[16];
+              ew_half(full_tag, half, sv, dv, pp, dd);
               tmem_st16_u(t_row + C::S_COL + 16 * half, pp);   // P^T over S^T
               tmem_st16_u(t_row + C::DP_COL + 16 * half, dd);  // dS^T over dP^T
             }
@@ -391,7 +505,7 @@ __global__ void __launch_bounds__(192, 2)
       }
       if (!ok) break;
       // ---- accumulators out: fp32 rows of dqkv (rows past len stay as the caller cleared them)
-      if (!wait_bounded(acc_full, aph, wc)) break;
+      if (!wait_bounded(acc_full, aph, ewc)) break;
       aph ^= 1u;
       tc_fence_after();
       const float inv_sqrt = args.inv_sqrt_hd;
