@@ -4,11 +4,13 @@
 // O = softmax(Q K^T / sqrt(hd) + mask) V without materialising the score
 // matrix ("TikTok TechJam 2026 -- Problem 3", section 2.1):
 //   * Keys are taken in sub-blocks of 64.  S = Q K_u^T of sub-block u goes to
-//     tensor memory (fp32), in one of two buffers: once the softmax warps have
-//     turned S of sub-block u into P, the MMA thread issues P V of u and then
-//     Q K^T of u + 2, which runs while the softmax works on u + 1.  One barrier
-//     each way per sub-block: s_full (S ready; also certifies that the P V
-//     which last read the P buffer is done) and p_full (P written, S read).
+//     tensor memory (fp32), in one of two buffers.  Two threads issue the MMAs:
+//     one Q K^T, one P V.  Once the softmax warps have turned S of sub-block u
+//     into P (p_full), the one issues P V of u and the other Q K^T of u + 2,
+//     which runs while the softmax works on u + 1; the softmax writes P of u + 2
+//     after P V of u is done (pv_done).  One issuing thread for both was the
+//     bottleneck: each tcgen05 instruction holds its thread for tens of cycles,
+//     and 8 MMAs and their commits a sub-block took longer than the softmax.
 //   * A warp's sub-blocks that no mask touches (all but the last one or two
 //     of an item) run a body without any mask logic; the masked ones take a
 //     general body.
@@ -35,9 +37,11 @@
 // q, k, v are strided views of the fused QKV output [B, S, 3D] (section 1.A,
 // head-split copies removed); O is written straight into [B, S, H*hd].
 //
-// Warp roles: warp 0 MMA issuer and TMEM owner, warp 1 TMA producer (Q once
-// per work item, K/V blocks into an NST-deep ring), warps 2-5 softmax +
-// output (thread = query row of TMEM lane quarter warp % 4).  Persistent CTAs claim work items from a global
+// Warp roles: warp 0 P V issuer and TMEM owner, warp 1 TMA producer (Q once
+// per work item, K/V blocks into an NST-deep ring), warp 2 Q K^T issuer, warp 3
+// idle, warps 4-7 softmax + output (thread = query row of TMEM lane quarter
+// warp % 4; the four warps form the second warpgroup, which at two CTAs per SM
+// takes registers from the first with setmaxnreg).  Persistent CTAs claim work items from a global
 // atomic counter, heaviest first (causal: the last query blocks have the most
 // keys); the producer publishes each claimed item to the other warps through
 // a small shared-memory ring.
@@ -105,6 +109,8 @@ struct Item {
 };
 
 constexpr int kItemRing = 4;
+// Warps: 0 issues P V (and owns tensor memory), 1 loads, 2 issues Q K^T, 3 idles, 4-7 softmax
+constexpr int kAttnThreads = 256;
 
 // Work item i -> (b, h, query block); false if the block is all padding.  The
 // (b, h) pairs are taken in groups of args.group; within a group the last (the
@@ -143,7 +149,7 @@ __device__ __forceinline__ int item_subblocks(const Item& it, int causal) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
+__global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                 const AttnArgs args) {
   using C = AttnCfg<HD>;
@@ -160,13 +166,12 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   uint64_t* q_empty = bars + 2;  // [NQ] (bars 2 and 3)
   uint64_t* o_full = bars + 4;
   uint64_t* o_empty = bars + 5;
-  uint64_t* drain = bars + 6;
-  // s_full(g) completes once QK^T of sub-block g and every earlier MMA (so P V of
-  // sub-block g - 2, the previous user of P[g & 1]) are done
-  uint64_t* s_full = bars + 7;   // [2] MMA -> softmax: S[b] computed
+  uint64_t* drain = bars + 6;     // abort path: the P V issuer's MMAs are done
+  uint64_t* s_full = bars + 7;   // [2] Q K^T issuer -> softmax: S[b] computed
   uint64_t* p_full = bars + 9;   // [2] softmax -> MMA: P[b] written (S[b] read)
-  uint64_t* pv_done = bars + 11; // [2] MMA -> softmax: P[b] V done (O current; the rescale path)
-  uint64_t* kv_full = bars + 13;
+  uint64_t* pv_done = bars + 11; // [2] P V issuer -> softmax: P[b] V done (P[b] free, O current)
+  uint64_t* drain_qk = bars + 13; // abort path: the Q K^T issuer's MMAs are done
+  uint64_t* kv_full = bars + 14;
   uint64_t* kv_empty = kv_full + C::NST;
   uint64_t* it_full = kv_empty + C::NST;
   uint64_t* it_empty = it_full + kItemRing;
@@ -189,22 +194,23 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     mbar_init(o_full, 1);
     mbar_init(o_empty, 4);
     mbar_init(drain, 1);
+    mbar_init(drain_qk, 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(&it_full[s], 1);
-      mbar_init(&it_empty[s], 5);  // the MMA warp and the four softmax warps
+      mbar_init(&it_empty[s], 6);  // the two MMA issuers and the four softmax warps
     }
     *abort_flag = 0;
     *never_flag = 0;
     fence_barrier_init();
   }
-  // Warp 0 issues the MMAs: the oldest warp is the one the scheduler prefers
-  // when the running warp stalls, which keeps the MMA issue from being starved
-  // by the softmax warps sharing its scheduler.
-  constexpr int kMmaWarp = 0, kProdWarp = 1;
+  // Two MMA issuers: one thread issuing both products of every sub-block (4 + 4 MMAs
+  // and their commits, each tcgen05 instruction holding the thread for tens of cycles)
+  // took longer per sub-block than the softmax, which then waited for S.
+  constexpr int kMmaWarp = 0, kProdWarp = 1, kQkWarp = 2;
   if (warp == kProdWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmKV);
@@ -214,6 +220,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
   const WaitCtl wc{args.c.status, abort_flag, args.c.timeout_ns};
   grid_wait_prior();  // everything below reads or writes what earlier kernels use
 
@@ -225,6 +232,12 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
   uint32_t q_issued = 0, q_par = 0;  // producer: Q buffers with loads in flight, and their parities
   bool mma_issued = false;
 
+  // Two CTAs of 256 threads launch with 128 registers a thread: warpgroup 0 (issuers,
+  // loader, one idle warp) hands registers to the softmax warpgroup, 4 x 32 x 64 +
+  // 4 x 32 x 192 = 256 x 128.  Each warpgroup changes its count at one point, at the top
+  // of its branch.
+  if (warp < 4) {
+  if constexpr (C::CTAS_PER_SM == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ TMA producer + scheduler
     if (lane == 0) {
@@ -283,25 +296,31 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kQkWarp) {
    if (lane == 0) {
-    // ------------------------------------------------------------ MMA issuer (one thread)
+    // ------------------------------------------------------------ MMA issuers (one thread each)
+    // Warp 2 issues S = Q K^T of every sub-block, warp 0 O += P V.  Both follow the item
+    // ring and number the sub-blocks of all items this CTA runs (sub-block g uses S and P
+    // buffer g & 1).  Q K^T of sub-block g writes S[g & 1] once the softmax has read it for
+    // sub-block g - 2 (p_full); P V of g reads P[g & 1] once the softmax has written it
+    // (p_full).  The softmax in turn writes P[g & 1] only after P V of g - 2 (pv_done).
     // Key rows at or past len_b hold exact zeros (the QKV producers write padding rows
     // as zeros; rows past S are zero-filled by the TMA), so whole key blocks are used.
+    const bool is_qk = warp == kQkWarp;
     constexpr uint32_t idesc_qk = idesc_f16(128, C::SUB, 0, 0);
     constexpr uint32_t idesc_pv = idesc_f16(128, HD, 0, 1);
     const uint32_t d_o = tmem_base + C::O_COL;
-    int st = 0, pst = 0, ik = 0;  // stage of the next QK / of the next PV
+    int st = 0, ik = 0;  // stage of the next sub-block
     uint32_t kvph = 0, qph = 0, oeph = 0, itph = 0;  // qph: parity bit per Q buffer
     int qb_i = 0;    // Q buffer of the current item
-    uint32_t g = 0;  // sub-blocks of all earlier items: sub-block g uses S/P buffer g & 1
+    uint32_t g = 0;  // sub-blocks of all earlier items
     bool first_item = true, ok = true;
-    // S[b] = Q K^T for the keys of half h of stage s
     // Operand descriptors: built once; a buffer / stage / half only moves the
     // start-address field (shared-memory byte offset / 16, which stays below 2^14).
     const uint64_t qd0 = sdesc(smem_u32(sQ), 16, 8 * C::ROWB, C::SWZ);
     const uint64_t kd0 = sdesc(smem_u32(sK), 16, 8 * C::ROWB, C::SWZ);
     const uint64_t vd0 = sdesc(smem_u32(sV), BN * C::ROWB, 8 * C::ROWB, C::SWZ);
+    // S[b] = Q K^T for the keys of half h of stage s
     auto issue_qk = [&](int s, int h, uint32_t b) {
       const uint64_t ad0 = qd0 + (uint32_t)((qb_i * C::Q_BYTES) >> 4);
       const uint64_t bd0 = kd0 + (uint32_t)((s * C::KV_BYTES + h * C::SUB * C::ROWB) >> 4);
@@ -342,62 +361,70 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       Item it;
       decode_item(i, args, nqb, BN, it);
       const int nsub = item_subblocks(it, args.causal);
-      if (!wait_bounded(&q_full[qb_i], (qph >> qb_i) & 1u, wc)) break;
-      qph ^= 1u << qb_i;
-      tc_fence_after();
-      const uint32_t g0 = g;
-      // QK^T of sub-block u, once its keys are resident and its S buffer has been read
-      auto qk = [&](int u) -> bool {
-        const uint32_t gg = g0 + u, b = gg & 1u;
+      if (is_qk) {
+        if (!wait_bounded(&q_full[qb_i], (qph >> qb_i) & 1u, wc)) break;
+        qph ^= 1u << qb_i;
+      }
+      for (int u = 0; u < nsub; ++u) {
+        const uint32_t gg = g + u, b = gg & 1u;
         const int h = u % C::SUBS;
-        if (h == 0) {
-          if (!wait_bounded(&kv_full[st], kvph, wc)) return false;
-          tc_fence_after();
+        const bool stage_done = h == C::SUBS - 1 || u == nsub - 1;
+        if (is_qk) {
+          // S[b] was last read by the softmax for sub-block gg - 2
+          if (gg >= 2 && !wait_bounded(&p_full[b], ((gg - 2) >> 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+        } else {
+          if (!wait_bounded(&p_full[b], (gg >> 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          if (u == 0 && !first_item) {
+            if (!wait_bounded(o_empty, oeph, wc)) {
+              ok = false;
+              break;
+            }
+            oeph ^= 1u;
+          }
         }
-        // S[b] was last read by sub-block gg - 2, whose P this thread has already waited for
-        issue_qk(st, h, b);
+        if (h == 0) {
+          if (!wait_bounded(&kv_full[st], kvph, wc)) {
+            ok = false;
+            break;
+          }
+        }
+        tc_fence_after();
         mma_issued = true;
-        umma_commit(&s_full[b]);
-        if (u == nsub - 1) umma_commit(&q_empty[qb_i]);
-        if (h == C::SUBS - 1 || u == nsub - 1) {
+        if (is_qk) {
+          issue_qk(st, h, b);
+          umma_commit(&s_full[b]);
+          if (u == nsub - 1) umma_commit(&q_empty[qb_i]);
+        } else {
+          issue_pv(st, h, b, u > 0);
+          umma_commit(&pv_done[b]);
+          // P V of the stage's last sub-block comes after the softmax read S of both, so
+          // the Q K^T products that read its keys are done too
+          if (stage_done) umma_commit(&kv_empty[st]);
+          if (u == nsub - 1) umma_commit(o_full);
+        }
+        if (stage_done) {
           if (++st == C::NST) {
             st = 0;
             kvph ^= 1u;
           }
         }
-        return true;
-      };
-      // P V of sub-block u, once its probabilities are in P[b]
-      auto pv = [&](int u) -> bool {
-        const uint32_t gg = g0 + u, b = gg & 1u;
-        const int h = u % C::SUBS;
-        if (!wait_bounded(&p_full[b], (gg >> 1) & 1u, wc)) return false;
-        if (u == 0 && !first_item) {
-          if (!wait_bounded(o_empty, oeph, wc)) return false;
-          oeph ^= 1u;
-        }
-        tc_fence_after();
-        const bool stage_done = h == C::SUBS - 1 || u == nsub - 1;
-        issue_pv(pst, h, b, u > 0);
-        umma_commit(&pv_done[b]);
-        if (stage_done) umma_commit(&kv_empty[pst]);
-        if (u == nsub - 1) umma_commit(o_full);
-        if (stage_done && ++pst == C::NST) pst = 0;
-        return true;
-      };
-      for (int u = 0; ok && u < C::LOOKAHEAD && u < nsub; ++u) ok = qk(u);
-      for (int u = 0; ok && u < nsub; ++u) {
-        if (!pv(u)) ok = false;
-        else if (u + C::LOOKAHEAD < nsub && !qk(u + C::LOOKAHEAD)) ok = false;
       }
       if (!ok) break;
-      g = g0 + nsub;
+      g += nsub;
       first_item = false;
       if (++qb_i == C::NQ) qb_i = 0;
     }
    }
+  }
   } else {
-    // ------------------------------------------------------------ softmax + output (warps 2-5)
+    if constexpr (C::CTAS_PER_SM == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
+    // ------------------------------------------------------------ softmax + output (warps 4-7)
     const int q = warp & 3;          // TMEM lane quarter of this warp
     const int r = q * 32 + lane;     // query row within the block == TMEM lane
     const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16);
@@ -405,7 +432,7 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
     const float sl2 = args.scale_log2;
     uint32_t oph = 0, itph = 0, g = 0;
     int ik = 0;
-    uint8_t* xst = sX + (warp - 2) * C::XPW;
+    uint8_t* xst = sX + (warp - 4) * C::XPW;
 
     while (true) {
       if (!wait_bounded(&it_full[ik], itph, wc)) break;
@@ -554,7 +581,11 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
           f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
           l_run += a0 + a1;
         }
-        // P[b] is free: s_full(g) completed after P V of sub-block g - 2
+        // P[b] was last read by P V of sub-block g - 2
+        if (g >= 2) {
+          if (!wait_bounded(&pv_done[b], ((g - 2) >> 1) & 1u, wc)) return false;
+          tc_fence_after();
+        }
         tmem_st32_u(t_row + C::P_COL + b * (C::SUB / 2), pk);
         tmem_wait_st();
         tc_fence_before();
@@ -612,9 +643,10 @@ __global__ void __launch_bounds__(192, AttnCfg<HD>::CTAS_PER_SM)
       for (int s = 0; s < C::NST; ++s)
         if (issued_mask & (1u << s)) wait_bounded(&kv_full[s], (issued_par >> s) & 1u, dc);
     }
-    if (warp == kMmaWarp && lane == 0 && mma_issued) {
-      umma_commit(drain);
-      wait_bounded(drain, 0, dc);
+    if ((warp == kMmaWarp || warp == kQkWarp) && lane == 0 && mma_issued) {
+      uint64_t* dr = warp == kMmaWarp ? drain : drain_qk;
+      umma_commit(dr);
+      wait_bounded(dr, 0, dc);
     }
     __syncthreads();
   }
@@ -633,7 +665,7 @@ static cudaError_t launch_attn_hd(const CUtensorMap& tq, const CUtensorMap& tkv,
   const int cap = num_sms * C::CTAS_PER_SM;
   const int grid = items < cap ? items : cap;
   if (grid <= 0) return cudaSuccess;
-  return launch_dependent(kern, grid, 192, C::SMEM, s, tq, tkv, a);
+  return launch_dependent(kern, grid, kAttnThreads, C::SMEM, s, tq, tkv, a);
 }
 
 cudaError_t prepare_attention_kernels() {

@@ -229,7 +229,7 @@ NCU_TRAFFIC = {
     # fingerprint no longer matches the sources report null
     ("postchain", "B64_S1024_D128_causal_ragged"): ("3308ef9bf974", 42.620416e6 + 29.589504e6),
     ("stack", "B2048_S128_D128_H4_F512_L4_keymask"): ("ee76cb851076", 87.525632e6 + 86.630912e6),  # lengths U[32,128]
-    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("eec525caff10", 208.818688e6 + 49.862656e6),
+    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("e0204649b2b7", 209.003264e6 + 49.925632e6),
     ("gemm_qkv", "B16_S512_D1024_H4_causal"): ("f4a5a3a4c7ff", 46.386176e6 + 11.332864e6),
     ("gemm_oproj", "B16_S512_D1024_H4_causal"): ("f4a5a3a4c7ff", 54.558976e6 + 2.426624e6),
     ("gemm_ffn1", "B16_S512_D1024_H4_causal"): ("f4a5a3a4c7ff", 51.184384e6 + 86.635264e6),
