@@ -4,11 +4,12 @@
 // O = softmax(Q K^T / sqrt(hd) + mask) V without materialising the score
 // matrix ("TikTok TechJam 2026 -- Problem 3", section 2.1):
 //   * Keys are taken in sub-blocks of 64.  S = Q K_u^T of sub-block u goes to
-//     tensor memory (fp32), in one of two buffers.  Two threads issue the MMAs:
-//     one Q K^T, one P V.  Once the softmax warps have turned S of sub-block u
-//     into P (p_full), the one issues P V of u and the other Q K^T of u + 2,
-//     which runs while the softmax works on u + 1; the softmax writes P of u + 2
-//     after P V of u is done (pv_done).  One issuing thread for both was the
+//     tensor memory (fp32), in one of three buffers; the softmax writes P of u
+//     (fp16) over the S it read.  Two threads issue the MMAs: one Q K^T, one
+//     P V.  Once the softmax warps have written P of sub-block u (p_full), the
+//     P V thread issues P V of u; once that is done (pv_done), the Q K^T thread
+//     issues Q K^T of u + 3 into the same buffer, which runs while the softmax
+//     works on u + 1 and u + 2.  One issuing thread for both products was the
 //     bottleneck: each tcgen05 instruction holds its thread for tens of cycles,
 //     and 8 MMAs and their commits a sub-block took longer than the softmax.
 //   * A warp's sub-blocks that no mask touches (all but the last one or two
@@ -71,15 +72,13 @@ struct AttnCfg {
   static constexpr int NST = HD == 32 ? 4 : 2;
   static constexpr int CTAS_PER_SM = HD <= 64 ? 2 : 1;
   // Keys are taken 64 at a time (a sub-block; a K/V stage holds BN / 64 of
-  // them).  Tensor memory: S[b] (fp32) at 64 b and P[b] (fp16 pairs) at
-  // 128 + 32 b for the two sub-block buffers b, O from O_COL.
+  // them).  Tensor memory: S[b] (fp32) at 64 b for three sub-block buffers b
+  // (sub-block g uses buffer g mod 3), P (fp16 pairs) written over the first 32
+  // columns of its own S, O from O_COL.
   static constexpr int SUB = 64;
   static constexpr int SUBS = BN / SUB;
   static constexpr int S_COL = 0;
-  static constexpr int P_COL = 128;
-  // QK^T of sub-block u + LOOKAHEAD is issued right after P V of sub-block u:
-  // at most 2 (two S buffers) and at most the sub-blocks the K/V ring holds.
-  static constexpr int LOOKAHEAD = NST * SUBS >= 2 ? 2 : 1;
+  static constexpr int NSB = 3;  // S buffers (P is written over the S it came from)
   static constexpr int O_COL = HD <= 64 ? 192 : 256;
   static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
   static constexpr size_t SMEM = 1024 + (size_t)NQ * Q_BYTES + (size_t)NST * 2 * KV_BYTES + XP_BYTES + 384;
@@ -167,11 +166,11 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
   uint64_t* o_full = bars + 4;
   uint64_t* o_empty = bars + 5;
   uint64_t* drain = bars + 6;     // abort path: the P V issuer's MMAs are done
-  uint64_t* s_full = bars + 7;   // [2] Q K^T issuer -> softmax: S[b] computed
-  uint64_t* p_full = bars + 9;   // [2] softmax -> MMA: P[b] written (S[b] read)
-  uint64_t* pv_done = bars + 11; // [2] P V issuer -> softmax: P[b] V done (P[b] free, O current)
-  uint64_t* drain_qk = bars + 13; // abort path: the Q K^T issuer's MMAs are done
-  uint64_t* kv_full = bars + 14;
+  uint64_t* s_full = bars + 7;   // [3] Q K^T issuer -> softmax: S[b] computed
+  uint64_t* p_full = bars + 10;  // [3] softmax -> P V issuer: P written over S[b]
+  uint64_t* pv_done = bars + 13; // [3] P V issuer -> Q K^T issuer, softmax: P V of buffer b done
+  uint64_t* drain_qk = bars + 16; // abort path: the Q K^T issuer's MMAs are done
+  uint64_t* kv_full = bars + 17;
   uint64_t* kv_empty = kv_full + C::NST;
   uint64_t* it_full = kv_empty + C::NST;
   uint64_t* it_empty = it_full + kItemRing;
@@ -186,7 +185,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
       mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NSB; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 4);
       mbar_init(&pv_done[b], 1);
@@ -300,10 +299,10 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
    if (lane == 0) {
     // ------------------------------------------------------------ MMA issuers (one thread each)
     // Warp 2 issues S = Q K^T of every sub-block, warp 0 O += P V.  Both follow the item
-    // ring and number the sub-blocks of all items this CTA runs (sub-block g uses S and P
-    // buffer g & 1).  Q K^T of sub-block g writes S[g & 1] once the softmax has read it for
-    // sub-block g - 2 (p_full); P V of g reads P[g & 1] once the softmax has written it
-    // (p_full).  The softmax in turn writes P[g & 1] only after P V of g - 2 (pv_done).
+    // ring and number the sub-blocks of all items this CTA runs (sub-block g uses buffer
+    // g mod 3, phase g / 3 of its barriers).  P V of g reads the P the softmax wrote over
+    // S[g mod 3] (p_full); Q K^T of g writes S[g mod 3] once P V of g - 3 has read the
+    // buffer (pv_done), which also means the softmax is done with it.
     // Key rows at or past len_b hold exact zeros (the QKV producers write padding rows
     // as zeros; rows past S are zero-filled by the TMA), so whole key blocks are used.
     const bool is_qk = warp == kQkWarp;
@@ -339,7 +338,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
     // O += P[b] V for the keys of half h of stage s (P from tensor memory)
     auto issue_pv = [&](int s, int h, uint32_t b, bool accumulate) {
       const uint64_t bd0 = vd0 + (uint32_t)((s * C::KV_BYTES + h * C::SUB * C::ROWB) >> 4);
-      const uint32_t pa = tmem_base + C::P_COL + b * (C::SUB / 2);
+      const uint32_t pa = tmem_base + C::S_COL + b * C::SUB;
 #pragma unroll
       for (int kk = 0; kk < C::SUB / 16; ++kk) {
         const uint64_t bd = bd0 + (uint32_t)((kk * 16 * C::ROWB) >> 4);
@@ -366,17 +365,17 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
         qph ^= 1u << qb_i;
       }
       for (int u = 0; u < nsub; ++u) {
-        const uint32_t gg = g + u, b = gg & 1u;
+        const uint32_t gg = g + u, b = gg % 3u, ph = (gg / 3u) & 1u;
         const int h = u % C::SUBS;
         const bool stage_done = h == C::SUBS - 1 || u == nsub - 1;
         if (is_qk) {
-          // S[b] was last read by the softmax for sub-block gg - 2
-          if (gg >= 2 && !wait_bounded(&p_full[b], ((gg - 2) >> 1) & 1u, wc)) {
+          // S[b] last held S and P of sub-block gg - 3, which P V has read
+          if (gg >= 3 && !wait_bounded(&pv_done[b], ph ^ 1u, wc)) {
             ok = false;
             break;
           }
         } else {
-          if (!wait_bounded(&p_full[b], (gg >> 1) & 1u, wc)) {
+          if (!wait_bounded(&p_full[b], ph, wc)) {
             ok = false;
             break;
           }
@@ -479,9 +478,9 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
       // S of sub-block gg from tensor memory (the columns that can be non-zero),
       // once its QK^T has completed; the caller waits for the load
       auto load_s = [&](uint32_t gg, int mode) -> bool {
-        if (!wait_bounded(&s_full[gg & 1u], (gg >> 1) & 1u, wc)) return false;
+        if (!wait_bounded(&s_full[gg % 3u], (gg / 3u) & 1u, wc)) return false;
         tc_fence_after();
-        const uint32_t t_s = t_row + C::S_COL + (gg & 1u) * C::SUB;
+        const uint32_t t_s = t_row + C::S_COL + (gg % 3u) * C::SUB;
         if (mode != kNone) {
           tmem_ld32(t_s, sv);
           if (mode != kTriLo) tmem_ld32(t_s + 32, sv + 32);
@@ -490,7 +489,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
       };
       auto body = [&](auto full_tag, int u) -> bool {
         constexpr bool FULL = decltype(full_tag)::value;
-        const uint32_t b = g & 1u;
+        const uint32_t b = g % 3u;
         const int k0 = u * C::SUB;
         const int mode = FULL ? kFull : mode_of(u);
         uint32_t pk[C::SUB / 2];
@@ -538,7 +537,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
             if (u > 0) {
               // O must hold P V of every earlier sub-block of this item before it is rescaled
               const uint32_t gp = g - 1;
-              if (!wait_bounded(&pv_done[gp & 1u], (gp >> 1) & 1u, wc)) return false;
+              if (!wait_bounded(&pv_done[gp % 3u], (gp / 3u) & 1u, wc)) return false;
               tc_fence_after();
               const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
 #pragma unroll 1
@@ -581,12 +580,8 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<HD>::CTAS_PER_SM)
           f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
           l_run += a0 + a1;
         }
-        // P[b] was last read by P V of sub-block g - 2
-        if (g >= 2) {
-          if (!wait_bounded(&pv_done[b], ((g - 2) >> 1) & 1u, wc)) return false;
-          tc_fence_after();
-        }
-        tmem_st32_u(t_row + C::P_COL + b * (C::SUB / 2), pk);
+        // P over the first 32 columns of this sub-block's S (read above)
+        tmem_st32_u(t_row + C::S_COL + b * C::SUB, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
