@@ -13,7 +13,7 @@ Prints ONE JSON line (rank 0).  Keys beyond the base contract:
   e2e           tokens/s from pinned host x / out, host<->device traffic inside
                 the timed region: tfl_forward_host (the kernels read x and write
                 out across the host link) or, for inputs over 4 GB,
-                tfl_forward_streamed (batch slices of a sixteenth of the batch,
+                tfl_forward_streamed (batch slices of a thirty-second of the batch,
                 their copies overlapping the forward of other slices)
   clocks        SM clock samples taken during the timed region
 With --impl reference the fp64 oracle itself is timed as the reference arm.
@@ -229,7 +229,7 @@ NCU_TRAFFIC = {
     # fingerprint no longer matches the sources report null
     ("postchain", "B64_S1024_D128_causal_ragged"): ("3308ef9bf974", 42.620416e6 + 29.589504e6),
     ("stack", "B2048_S128_D128_H4_F512_L4_keymask"): ("ee76cb851076", 87.525632e6 + 86.630912e6),  # lengths U[32,128]
-    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("e0204649b2b7", 209.003264e6 + 49.925632e6),
+    ("attention", "B2_S16384_D1024_H16_F4096_L1_causal"): ("82bcd7cfdc72", 209.170944e6 + 49.693184e6),
     ("gemm_qkv", "B16_S512_D1024_H4_causal"): ("f4a5a3a4c7ff", 46.386176e6 + 11.332864e6),
     ("gemm_oproj", "B16_S512_D1024_H4_causal"): ("f4a5a3a4c7ff", 54.558976e6 + 2.426624e6),
     ("gemm_ffn1", "B16_S512_D1024_H4_causal"): ("f4a5a3a4c7ff", 51.184384e6 + 86.635264e6),
@@ -395,14 +395,14 @@ def compute_dtype(shape) -> str:
 
 def e2e_slice(shape, arg: int) -> int:
     """Sequences per slice of the streamed end-to-end path: 0 (no slicing: tfl_forward_host)
-    unless the fp32 input is over 4 GB, else a sixteenth of the batch (at least one sequence):
-    small slices keep the copies that nothing overlaps (the first slice in, the last one out)
-    short; arg > 0 forces a slice size, arg < 0 turns slicing off."""
+    unless the fp32 input is over 4 GB, else a thirty-second of the batch (at least one
+    sequence): small slices keep the copies that nothing overlaps (the first slice in, the last
+    one out) short; arg > 0 forces a slice size, arg < 0 turns slicing off."""
     if arg < 0:
         return 0
     if arg > 0:
         return min(arg, shape.B)
-    return 0 if shape.B * shape.S * shape.d_model * 4 <= (4 << 30) else max(1, shape.B // 16)
+    return 0 if shape.B * shape.S * shape.d_model * 4 <= (4 << 30) else max(1, shape.B // 32)
 
 
 def config_dict(shape):

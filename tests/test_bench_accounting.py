@@ -106,7 +106,7 @@ def test_whole_stack_accounting():
 
 def test_e2e_slice_rule():
     big, small, many = synth.WORKLOADS[4], synth.WORKLOADS[1], synth.WORKLOADS[2]
-    assert bench.e2e_slice(big, 0) == 2          # 13 GB of input: a sixteenth of the batch
+    assert bench.e2e_slice(big, 0) == 1          # 13 GB of input: a thirty-second of the batch
     assert bench.e2e_slice(small, 0) == 0        # 33.5 MB: no slicing
     assert bench.e2e_slice(many, 0) == 0         # B10000 S128, 655 MB: no slicing
     assert bench.e2e_slice(big, -1) == 0 and bench.e2e_slice(big, 5) == 5
