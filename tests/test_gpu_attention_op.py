@@ -69,6 +69,10 @@ def _check(u, r, bound, what):
     (3, 64, 1, 32, True, [64, 1, 0]),
     (1, 1024, 2, 64, True, None),
     (2, 520, 3, 32, True, [519, 260]),
+    # more work items than CTAs (two per SM): each CTA runs several items of 1 to 5 key
+    # sub-blocks, so the forward's sub-block buffers rotate across item boundaries
+    (40, 320, 8, 64, True, [320 - 7 * i for i in range(40)]),
+    (64, 200, 4, 32, False, [200 - 3 * i for i in range(64)]),
 ])
 def test_attention_forward_lse_and_backward_within_rounding_bounds(B, S, H, hd, causal, lens):
     qkv, dout, o, lse, dqkv = _run(B, S, H, hd, causal, lens, seed=S + H)
