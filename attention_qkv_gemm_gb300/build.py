@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -24,6 +25,46 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["gemm.cu", "attention.cu", "attention_bwd.cu", "postchain.cu", "stack.cu", "rows.cu", "api.cu"]
+
+# The attention kernels that run two CTAs of 256 threads per SM move registers from their first
+# warpgroup to the second with setmaxnreg (64 and 192 a thread).  That balances only when the
+# kernel launches with exactly 128 registers a thread: launched with fewer, setmaxnreg.inc would
+# wait on the GPU for registers that never come free.  ptxas reports the launch count of every
+# entry function; a build that does not give these kernels exactly 128 is refused.
+SETMAXNREG_LAUNCH_REGS = {
+    "_ZN3tfl11attn_kernelILi32EEEv": 128,  # attn_kernel<32>
+    "_ZN3tfl11attn_kernelILi64EEEv": 128,  # attn_kernel<64>
+}
+PTXAS_INFO_SOURCES = {"attention.cu"}
+
+
+def launch_registers(ptxas_log: str) -> dict:
+    """Registers a thread at launch of each entry function in a ``-Xptxas -v`` log."""
+    regs, cur = {}, None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            cur = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and cur is not None:
+            regs[cur] = int(m.group(1))
+            cur = None
+    return regs
+
+
+def check_launch_registers(ptxas_log: str, required: dict = SETMAXNREG_LAUNCH_REGS) -> None:
+    """Raise unless every kernel whose mangled name starts with a key of ``required`` was
+    compiled, and launches with exactly the given registers a thread."""
+    regs = launch_registers(ptxas_log)
+    for prefix, want in required.items():
+        got = {k: v for k, v in regs.items() if k.startswith(prefix)}
+        if not got:
+            raise RuntimeError(f"ptxas reported no register count for {prefix}")
+        for k, v in got.items():
+            if v != want:
+                raise RuntimeError(f"{k} launches with {v} registers a thread; its setmaxnreg split "
+                                   f"needs exactly {want}")
 
 
 def _nvcc() -> str:
@@ -56,7 +97,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+        info = extra if extra or src not in PTXAS_INFO_SOURCES else ["-Xptxas", "-v"]
+        cmd = [nvcc, *ARCH, *FLAGS, *info, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
 
@@ -66,6 +108,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     for src, _, r in results:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        if src in PTXAS_INFO_SOURCES:
+            check_launch_registers(r.stdout + r.stderr)
         if verbose or ptxas_info:
             logs.append(f"== {src}\n{r.stdout}{r.stderr}")
     tmp = LIB + ".tmp"
