@@ -412,6 +412,159 @@ def config_dict(shape):
             "l2": "flushed (256 MiB write) between timed steps", "seed": 0}
 
 
+# An instrumented copy of the forward attention kernel for --attn-cycles (profiling only):
+# clock64 counters around each wait and each issue sequence of the two MMA-issuing threads, and
+# around the softmax warps' wait for S and their sub-block loop, summed per role into a device
+# array that tfl_attn_cycles_fetch reads and clears.  The copy is made from csrc/attention.cu at
+# run time by inserting text at fixed anchors (each must occur exactly once, or the mode stops),
+# and built into a separate library under _build/cycles/ that nothing else loads.
+# Slots: 0-4 P V thread (total, waiting for P, waiting for the K/V stage, issuing MMAs and
+# commits, sub-blocks), 8-12 the same for the Q K^T thread (its first wait is for P V of the
+# buffer's previous sub-block), 5-7 softmax warps (total, waiting for S, the sub-block loop),
+# 13 softmax warps' output phase.
+ATTN_CYCLE_PATCHES = [
+    ("namespace tfl {\n",
+     "namespace tfl {\n__device__ unsigned long long g_attn_cycles[16];\n"),
+    ("    bool first_item = true, ok = true;\n",
+     "    bool first_item = true, ok = true;\n"
+     "    long long cy_w = 0, cy_kv = 0, cy_is = 0, cy_n = 0;\n"
+     "    const long long cy_t0 = clock64();\n"),
+    ("        if (is_qk) {\n          // S[b] last held",
+     "        const long long cy_a = clock64();\n        if (is_qk) {\n          // S[b] last held"),
+    ("        if (h == 0) {\n          if (!wait_bounded(&kv_full[st], kvph, wc)) {",
+     "        const long long cy_b = clock64();\n        cy_w += cy_b - cy_a;\n"
+     "        if (h == 0) {\n          if (!wait_bounded(&kv_full[st], kvph, wc)) {"),
+    ("        tc_fence_after();\n        mma_issued = true;\n",
+     "        const long long cy_c = clock64();\n        cy_kv += cy_c - cy_b;\n"
+     "        tc_fence_after();\n        mma_issued = true;\n"),
+    ("        if (stage_done) {\n          if (++st == C::NST) {",
+     "        cy_is += clock64() - cy_c;\n        if (stage_done) {\n          if (++st == C::NST) {"),
+    ("      g += nsub;\n",
+     "      g += nsub;\n      cy_n += nsub;\n"),
+    ("      if (++qb_i == C::NQ) qb_i = 0;\n    }\n   }\n  }\n  } else {",
+     "      if (++qb_i == C::NQ) qb_i = 0;\n    }\n"
+     "    {\n      const int cy_o = is_qk ? 8 : 0;\n"
+     "      atomicAdd(&g_attn_cycles[cy_o + 0], (unsigned long long)(clock64() - cy_t0));\n"
+     "      atomicAdd(&g_attn_cycles[cy_o + 1], (unsigned long long)cy_w);\n"
+     "      atomicAdd(&g_attn_cycles[cy_o + 2], (unsigned long long)cy_kv);\n"
+     "      atomicAdd(&g_attn_cycles[cy_o + 3], (unsigned long long)cy_is);\n"
+     "      atomicAdd(&g_attn_cycles[cy_o + 4], (unsigned long long)cy_n);\n    }\n"
+     "   }\n  }\n  } else {"),
+    ("    uint8_t* xst = sX + (warp - 4) * C::XPW;\n",
+     "    uint8_t* xst = sX + (warp - 4) * C::XPW;\n"
+     "    long long cy_s = 0, cy_body = 0, cy_out = 0;\n"
+     "    const long long cy_t0 = clock64();\n"),
+    ("        if (!wait_bounded(&s_full[gg % 3u], (gg / 3u) & 1u, wc)) return false;\n",
+     "        const long long cy_a = clock64();\n"
+     "        if (!wait_bounded(&s_full[gg % 3u], (gg / 3u) & 1u, wc)) return false;\n"
+     "        cy_s += clock64() - cy_a;\n"),
+    ("      int u = 0;\n      for (; ok && u < nfull; ++u, ++g) ok = body(std::true_type{}, u);\n"
+     "      for (; ok && u < nsub; ++u, ++g) ok = body(std::false_type{}, u);\n",
+     "      int u = 0;\n      const long long cy_b = clock64();\n"
+     "      for (; ok && u < nfull; ++u, ++g) ok = body(std::true_type{}, u);\n"
+     "      for (; ok && u < nsub; ++u, ++g) ok = body(std::false_type{}, u);\n"
+     "      cy_body += clock64() - cy_b;\n      const long long cy_o = clock64();\n"),
+    ("      if (lane == 0) mbar_arrive(o_empty);\n    }\n  }\n\n  // ---",
+     "      if (lane == 0) mbar_arrive(o_empty);\n      cy_out += clock64() - cy_o;\n    }\n"
+     "    if (lane == 0) {\n"
+     "      atomicAdd(&g_attn_cycles[5], (unsigned long long)(clock64() - cy_t0));\n"
+     "      atomicAdd(&g_attn_cycles[6], (unsigned long long)cy_s);\n"
+     "      atomicAdd(&g_attn_cycles[7], (unsigned long long)cy_body);\n"
+     "      atomicAdd(&g_attn_cycles[13], (unsigned long long)cy_out);\n    }\n  }\n\n  // ---"),
+    ("}  // namespace tfl\n",
+     "}  // namespace tfl\n\n"
+     "extern \"C\" int tfl_attn_cycles_fetch(unsigned long long* out) {\n"
+     "  cudaError_t e = cudaMemcpyFromSymbol(out, tfl::g_attn_cycles, 16 * sizeof(unsigned long long));\n"
+     "  static const unsigned long long zero[16] = {0};\n"
+     "  if (e == cudaSuccess) e = cudaMemcpyToSymbol(tfl::g_attn_cycles, zero, sizeof(zero));\n"
+     "  return (int)e;\n}\n"),
+]
+
+
+def attention_cycles_source(src: str) -> str:
+    """attention.cu with the --attn-cycles counters inserted (every anchor exactly once)."""
+    for anchor, repl in ATTN_CYCLE_PATCHES:
+        n = src.count(anchor)
+        if n != 1:
+            raise RuntimeError(f"--attn-cycles: an anchor occurs {n} times in attention.cu "
+                               f"(the kernel changed; update ATTN_CYCLE_PATCHES): {anchor[:60]!r}")
+        src = src.replace(anchor, repl)
+    return src
+
+
+def build_attention_cycles_lib() -> str:
+    """Compile the instrumented attention copy and link it with the library's other objects into
+    _build/cycles/libtfl_cycles.so; the same launch-register check as the library build."""
+    from attention_qkv_gemm_gb300 import build as libbuild
+    libbuild.build()
+    out = os.path.join(libbuild.BUILD, "cycles")
+    os.makedirs(out, exist_ok=True)
+    with open(os.path.join(libbuild.CSRC, "attention.cu")) as f:
+        src = attention_cycles_source(f.read())
+    cu, obj, lib = (os.path.join(out, n) for n in ("attention_cycles.cu", "attention_cycles.o",
+                                                  "libtfl_cycles.so"))
+    with open(cu, "w") as f:
+        f.write(src)
+    nvcc = libbuild._nvcc()
+    r = subprocess.run([nvcc, *libbuild.ARCH, *libbuild.FLAGS, "-Xptxas", "-v", "-c", cu, "-o", obj],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on the instrumented attention:\n{r.stdout}\n{r.stderr}")
+    libbuild.check_launch_registers(r.stdout + r.stderr)
+    objs = [os.path.join(libbuild.BUILD, os.path.splitext(s)[0] + ".o") for s in libbuild.SOURCES
+            if s != "attention.cu"]
+    r = subprocess.run([nvcc, *libbuild.ARCH, "-shared", "-o", lib, obj, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return lib
+
+
+def attention_cycles_bench(args):
+    """The forward attention kernel's cycles per 64-key sub-block and CTA, per role, from the
+    instrumented copy (B,S,H,head_dim,causal; one warm-up launch, then --steps launches)."""
+    import ctypes
+    import torch
+    import attention_qkv_gemm_gb300 as pkg
+    B, S, H, hd, causal = [int(v) for v in args.attn_cycles.split(",")]
+    lib = pkg.load(build_attention_cycles_lib())
+    buf = (ctypes.c_ulonglong * 16)()
+    D = H * hd
+    g = torch.Generator(device="cuda").manual_seed(0)
+    qkv = torch.randn(B, S, 3 * D, device="cuda", generator=g).half()
+    o = torch.empty(B, S, D, device="cuda", dtype=torch.float16)
+    lse = torch.empty(B, H, S, device="cuda", dtype=torch.float32)
+    a = pkg.tfl_attn_create(B, S, H, hd)
+    sp = torch.cuda.current_stream().cuda_stream
+    fwd = lambda: pkg.tfl_attn_forward(a, qkv.data_ptr(), None, causal, o.data_ptr(), lse.data_ptr(), sp)
+    fwd()
+    torch.cuda.synchronize()
+    if lib.tfl_attn_cycles_fetch(buf) != 0:
+        raise RuntimeError("tfl_attn_cycles_fetch failed")
+    for _ in range(args.steps):
+        fwd()
+    torch.cuda.synchronize()
+    if pkg.tfl_attn_status(a, sp) != 0:
+        raise RuntimeError(pkg.tfl_last_error())
+    if lib.tfl_attn_cycles_fetch(buf) != 0:
+        raise RuntimeError("tfl_attn_cycles_fetch failed")
+    pkg.tfl_attn_destroy(a)
+    c = [float(v) for v in buf]
+    n_pv, n_qk = c[4], c[12]  # sub-blocks summed over the CTAs (each issuer sees every sub-block)
+    warps = 4.0 * n_pv        # the softmax counters are summed over four warps a CTA
+    per = lambda v, n: round(v / n, 1) if n else None
+    line = {"metric": "attention_cycles_per_subblock", "unit": "SM cycles per 64-key sub-block and CTA",
+            "config": {"B": B, "S": S, "n_heads": H, "head_dim": hd, "causal": bool(causal), "launches": args.steps},
+            "pv_thread": {"total": per(c[0], n_pv), "waiting_for_p": per(c[1], n_pv),
+                          "waiting_for_kv": per(c[2], n_pv), "issuing": per(c[3], n_pv)},
+            "qk_thread": {"total": per(c[8], n_qk), "waiting_for_pv": per(c[9], n_qk),
+                          "waiting_for_kv": per(c[10], n_qk), "issuing": per(c[11], n_qk)},
+            "softmax_warp": {"total": per(c[5] * 4, warps), "waiting_for_s": per(c[6] * 4, warps),
+                             "subblock_loop": per(c[7] * 4, warps), "output": per(c[13] * 4, warps)},
+            "note": "instrumented copy of attention.cu (clock64 around each wait and issue sequence); "
+                    "the counters slow the kernel a few per cent"}
+    print(json.dumps(line))
+
+
 def attention_backward_bench(args):
     """Standalone attention (tfl_attn_forward / tfl_attn_backward) on random fp16 q, k, v and
     dO of the given shape: CUDA-event time of each, against the dense tensor peak.
@@ -492,12 +645,17 @@ def main():
                     help="tfl_options.whole_stack: 1 (default) or 0 (per-layer kernels)")
     ap.add_argument("--attn-bwd", default="",
                     help="B,S,H,head_dim,causal: time the standalone attention forward + backward instead")
+    ap.add_argument("--attn-cycles", default="",
+                    help="B,S,H,head_dim,causal: cycles per sub-block of the forward attention kernel's roles, "
+                         "from an instrumented copy (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
     world, rank, local = dist_env()
     if args.attn_bwd and args.impl == "ours":
         return attention_backward_bench(args)
+    if args.attn_cycles and args.impl == "ours":
+        return attention_cycles_bench(args)
     shape = custom_shape(args.shape) if args.shape else workload(args.workload)
     if args.impl == "reference":
         return reference_arm(args, shape, world, rank)

@@ -117,3 +117,27 @@ def test_compute_dtype_names_the_fp8_correction_products():
     assert bench.compute_dtype(synth.WORKLOADS[4]) == "f16+e4m3"
     assert bench.compute_dtype(synth.WORKLOADS[3]) == "f16+e4m3"
     assert bench.compute_dtype(synth.WORKLOADS[1]) == "f16"
+
+
+def test_attention_cycles_copy_applies_and_builds(tmp_path):
+    # --attn-cycles instruments attention.cu by inserting counters at fixed anchors; every
+    # anchor must still match the kernel exactly once, and the copy must compile with the same
+    # launch-register count as the library (its setmaxnreg split needs it)
+    import subprocess
+    from attention_qkv_gemm_gb300 import build as libbuild
+    with open(f"{libbuild.CSRC}/attention.cu") as f:
+        src = f.read()
+    out = bench.attention_cycles_source(src)
+    assert out.count("atomicAdd(&g_attn_cycles[") == 9
+    assert 'extern "C" int tfl_attn_cycles_fetch' in out
+    cu = tmp_path / "attention_cycles.cu"
+    cu.write_text(out)
+    r = subprocess.run([libbuild._nvcc(), *libbuild.ARCH, *libbuild.FLAGS, "-Xptxas", "-v", "-c", str(cu),
+                        "-o", str(tmp_path / "a.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    libbuild.check_launch_registers(r.stdout + r.stderr)
+
+
+def test_attention_cycles_copy_refuses_a_changed_kernel():
+    with pytest.raises(RuntimeError, match="anchor"):
+        bench.attention_cycles_source("namespace tfl {\n}  // namespace tfl\n")
