@@ -1,4 +1,5 @@
-"""Exhaustive interleaving model of the forward attention kernel's hand-off protocol (CPU).
+"""Exhaustive interleaving models of the attention kernels' hand-off protocols (CPU): the
+forward kernel below, and the backward dQ kernel further down.
 
 The kernel (csrc/attention.cu) runs five roles per CTA: a loader (work items, Q, K/V stages),
 a thread issuing Q K^T, a thread issuing P V, and four softmax warps.  They meet at mbarriers
@@ -157,58 +158,20 @@ def build_programs(items, ring, warps, rescale, mutation=None):
     return progs, bars, fills, g0
 
 
-def explore(items, ring, warps, rescale, mutation=None, limit=3_000_000):
-    """Visit every reachable state; returns their number.  Raises AssertionError on a deadlock,
-    a parity wait two phases behind its barrier, or a hazard."""
-    progs, bars, fills, g0 = build_programs(items, ring, warps, rescale, mutation)
+def run_model(progs, bars, key_bar, issuers, hazard_free, limit=3_000_000):
+    """Visit every reachable state of the roles ``progs`` (name -> action list); returns their
+    number.  ``issuers`` are the roles whose mma / commit actions queue up and complete in order;
+    ``key_bar`` maps a load to the barrier it arrives on; ``hazard_free(kind, arg, pcs, comp,
+    loaded)`` evaluates a check action (pcs by role name, comp: completed queue entries by
+    issuer, loaded: the completed loads).  Raises AssertionError on a deadlock, a parity wait two
+    phases behind its barrier, or a hazard."""
     roles = sorted(progs)
     ridx = {r: k for k, r in enumerate(roles)}
     bar_names = sorted(bars)
     bidx = {n: k for k, n in enumerate(bar_names)}
-    key_bar = {a[2]: a[1] for a in progs["load"] if a[0] == "tma"}
-    # the issuers' queues: every mma / commit in issue order
-    queue = {t: [a for a in progs[t] if a[0] in ("mma", "commit")] for t in ("qk", "pv")}
-    qpos = {t: {a[2]: k for k, a in enumerate(queue[t]) if a[0] == "mma"} for t in ("qk", "pv")}
+    queue = {t: [a for a in progs[t] if a[0] in ("mma", "commit")] for t in issuers}
     issued_at = {t: [sum(1 for a in progs[t][:pc] if a[0] in ("mma", "commit")) for pc in range(len(progs[t]) + 1)]
-                 for t in ("qk", "pv")}
-    n_items = len(items)
-    item_of = {gg: i for i in range(n_items) for gg in range(g0[i], g0[i] + items[i])}
-    fill_of = {gg: f for f, (_, subs) in enumerate(fills) for gg in subs}
-    o_read_pc = {}  # (item, warp) -> pc just after that warp's read of the item's O
-    for r in roles:
-        for pc, a in enumerate(progs[r]):
-            if a[0] == "mark":
-                o_read_pc[(a[1][1], a[1][2])] = pc + 1
-
-    def done(comp, t, key):  # MMA `key` of thread t has completed
-        return comp[0 if t == "qk" else 1] > qpos[t][key]
-
-    def hazard_free(kind, arg, pcs, comp, loaded):
-        if kind == "read_s":
-            return done(comp, "qk", ("QK", arg))
-        if kind in ("write_p", "qk_issue_buffer"):
-            return arg < 3 or done(comp, "pv", ("PV", arg - 3))
-        if kind == "qk_issue":
-            i = item_of[arg]
-            return ((arg < 3 or done(comp, "pv", ("PV", arg - 3))) and ("Q", i) in loaded
-                    and ("KV", fill_of[arg]) in loaded)
-        if kind == "rescale":
-            return done(comp, "pv", ("PV", arg - 1))
-        if kind == "pv_issue":
-            i = item_of[arg]
-            if arg == g0[i] and i > 0 and any(pcs[ridx[f"sm{w}"]] < o_read_pc[(i - 1, w)] for w in range(warps)):
-                return False  # O still being read by a softmax warp
-            return ("KV", fill_of[arg]) in loaded
-        if kind == "read_o":
-            return all(done(comp, "pv", ("PV", gg)) for gg in range(g0[arg], g0[arg] + items[arg]))
-        if kind == "kv_load":
-            s = fills[arg][0]
-            prev = [k for k in range(arg) if fills[k][0] == s]
-            return not prev or all(done(comp, "qk", ("QK", gg)) and done(comp, "pv", ("PV", gg))
-                                   for gg in fills[prev[-1]][1])
-        if kind == "q_load":
-            return arg < NQ or all(done(comp, "qk", ("QK", gg)) for gg in range(g0[arg - NQ], g0[arg - NQ] + items[arg - NQ]))
-        raise AssertionError(kind)
+                 for t in issuers}
 
     def arrive(barst, name):
         b = list(barst)
@@ -219,9 +182,9 @@ def explore(items, ring, warps, rescale, mutation=None, limit=3_000_000):
         b[bidx[name]] = (k, miss)
         return tuple(b)
 
-    # state: pcs, completed MMA/commit counts (qk, pv), loads in flight, loads completed,
+    # state: pcs, completed queue entries per issuer, loads in flight, loads completed,
     # barriers as (completed phases, arrivals still missing in the current phase)
-    start = (tuple(0 for _ in roles), (0, 0), frozenset(), frozenset(),
+    start = (tuple(0 for _ in roles), tuple(0 for _ in issuers), frozenset(), frozenset(),
              tuple((0, bars[n].count) for n in bar_names))
     seen = {start}
     stack = [start]
@@ -247,15 +210,15 @@ def explore(items, ring, warps, rescale, mutation=None, limit=3_000_000):
             elif a[0] == "tma":
                 succ.append((npcs, comp, inflight | {a[2]}, loaded, barst))
             elif a[0] == "check":
-                if not hazard_free(a[1], a[2], pcs, comp, loaded):
+                if not hazard_free(a[1], a[2], dict(zip(roles, pcs)), dict(zip(issuers, comp)), loaded):
                     raise AssertionError(f"{r}: hazard {a[1]}({a[2]})")
                 succ.append((npcs, comp, inflight, loaded, barst))
             else:
                 raise AssertionError(a)
-        for t, ci in (("qk", 0), ("pv", 1)):  # an issuer's oldest queued MMA or commit completes
+        for ci, t in enumerate(issuers):  # an issuer's oldest queued MMA or commit completes
             if comp[ci] < issued_at[t][pcs[ridx[t]]]:
                 e = queue[t][comp[ci]]
-                ncomp = (comp[0] + (ci == 0), comp[1] + (ci == 1))
+                ncomp = comp[:ci] + (comp[ci] + 1,) + comp[ci + 1:]
                 succ.append((pcs, ncomp, inflight, loaded, arrive(barst, e[2]) if e[0] == "commit" else barst))
         for key in inflight:  # a load completes
             succ.append((pcs, comp, inflight - {key}, loaded | {key}, arrive(barst, key_bar[key])))
@@ -271,6 +234,58 @@ def explore(items, ring, warps, rescale, mutation=None, limit=3_000_000):
                 if len(seen) > limit:
                     raise RuntimeError("state space too large for the test")
     return len(seen)
+
+
+def mark_pcs(progs):
+    """(mark key) -> (role, pc just after the mark)."""
+    return {a[1]: (r, pc + 1) for r in progs for pc, a in enumerate(progs[r]) if a[0] == "mark"}
+
+
+def explore(items, ring, warps, rescale, mutation=None):
+    """The forward kernel's protocol on the work list ``items`` (sub-blocks per item)."""
+    progs, bars, fills, g0 = build_programs(items, ring, warps, rescale, mutation)
+    key_bar = {a[2]: a[1] for a in progs["load"] if a[0] == "tma"}
+    qpos = {t: {a[2]: k for k, a in enumerate([a for a in progs[t] if a[0] in ("mma", "commit")]) if a[0] == "mma"}
+            for t in ("qk", "pv")}
+    n_items = len(items)
+    item_of = {gg: i for i in range(n_items) for gg in range(g0[i], g0[i] + items[i])}
+    fill_of = {gg: f for f, (_, subs) in enumerate(fills) for gg in subs}
+    marks = mark_pcs(progs)
+
+    def done(comp, t, key):  # MMA `key` of thread t has completed
+        return comp[t] > qpos[t][key]
+
+    def hazard_free(kind, arg, pcs, comp, loaded):
+        if kind == "read_s":
+            return done(comp, "qk", ("QK", arg))
+        if kind == "write_p":
+            return arg < 3 or done(comp, "pv", ("PV", arg - 3))
+        if kind == "qk_issue":
+            return ((arg < 3 or done(comp, "pv", ("PV", arg - 3))) and ("Q", item_of[arg]) in loaded
+                    and ("KV", fill_of[arg]) in loaded)
+        if kind == "rescale":
+            return done(comp, "pv", ("PV", arg - 1))
+        if kind == "pv_issue":
+            i = item_of[arg]
+            if arg == g0[i] and i > 0:
+                for w in range(warps):
+                    r, pc = marks[("o_read", i - 1, w)]
+                    if pcs[r] < pc:
+                        return False  # O still being read by a softmax warp
+            return ("KV", fill_of[arg]) in loaded
+        if kind == "read_o":
+            return all(done(comp, "pv", ("PV", gg)) for gg in range(g0[arg], g0[arg] + items[arg]))
+        if kind == "kv_load":
+            s = fills[arg][0]
+            prev = [k for k in range(arg) if fills[k][0] == s]
+            return not prev or all(done(comp, "qk", ("QK", gg)) and done(comp, "pv", ("PV", gg))
+                                   for gg in fills[prev[-1]][1])
+        if kind == "q_load":
+            return arg < NQ or all(done(comp, "qk", ("QK", gg))
+                                   for gg in range(g0[arg - NQ], g0[arg - NQ] + items[arg - NQ]))
+        raise AssertionError(kind)
+
+    return run_model(progs, bars, key_bar, ["qk", "pv"], hazard_free)
 
 
 # (sub-blocks of each work item, item ring slots, softmax warps, rescale wait on every sub-block)
@@ -306,3 +321,163 @@ def test_the_pv_threads_o_empty_wait_is_implied(warps):
     # and a warp writes it only after reading the previous item's O: without the o_empty wait
     # nothing changes
     explore([1, 2, 1], 2, warps, True, "pv_skips_o_empty")
+
+
+# ---------------------------------------------------------------------------------------------
+# The backward dQ kernel (csrc/attention_bwd.cu, dQ mode): a loader (resident Q and dO per work
+# item, K_j / V_j tiles per 64-key step into a ring of BWD_NST stages), one MMA-issuing thread and
+# the elementwise warps.  Step s of an item computes S into S buffer s mod 2 (counted from the
+# item's first step) as soon as its tiles are in, dP into the single dP buffer once the warps hold
+# the previous step's dP in registers (dp_read), releases the step to the warps (s_full) only
+# after the previous step's dS is written (x_full), then accumulates dQ += dS K of the previous
+# step.  The warps read S and dP, arrive on dp_read, write dS over S, arrive on x_full, and read
+# out the accumulator at the end of the item (acc_full / acc_empty).
+BWD_NST = 3
+
+
+def build_dq(items, warps, mutation=None):
+    bars = {}
+
+    def bar(name, count):
+        bars[name] = Bar(name, count)
+        return name
+
+    res_full, res_empty = bar("res_full", 1), bar("res_empty", 1)
+    s_full, x_full, dp_read = bar("s_full", 1), bar("x_full", warps), bar("dp_read", warps)
+    acc_full, acc_empty = bar("acc_full", 1), bar("acc_empty", warps)
+    b_full = [bar(f"b_full{k}", 1) for k in range(BWD_NST)]
+    b_empty = [bar(f"b_empty{k}", 1) for k in range(BWD_NST)]
+    t0 = list(itertools.accumulate([0] + items))[:-1]  # global index of each item's first step
+    buf = {t0[i] + s: s % 2 for i in range(len(items)) for s in range(items[i])}
+
+    load = []
+    for i, n in enumerate(items):
+        load += [("wait", res_empty, i - 1), ("check", "res_load", i), ("tma", res_full, ("R", i))]
+        for s in range(n):
+            t = t0[i] + s
+            load += [("wait", b_empty[t % BWD_NST], t // BWD_NST - 1), ("check", "stage_load", t),
+                     ("tma", b_full[t % BWD_NST], ("B", t))]
+
+    mma = []
+    for i, n in enumerate(items):
+        mma.append(("wait", res_full, i))
+        if i > 0:
+            mma.append(("wait", acc_empty, i - 1))
+        for s in range(n + 1):
+            t = t0[i] + s
+            if s < n:
+                mma += [("wait", b_full[t % BWD_NST], t // BWD_NST), ("check", "s_issue", t), ("mma", "mma", ("S", t))]
+                if s > 0:
+                    mma.append(("wait", dp_read, t - 1))
+                mma += [("check", "dp_issue", t), ("mma", "mma", ("DP", t))]
+            elif s > 0:
+                mma.append(("wait", dp_read, t - 1))
+            if s > 0 and mutation != "s_full_before_x_full":
+                mma.append(("wait", x_full, t - 1))
+            if s < n:
+                mma.append(("commit", "mma", s_full))
+            if s > 0 and mutation == "s_full_before_x_full":
+                mma.append(("wait", x_full, t - 1))
+            if s > 0:
+                mma += [("check", "acc_issue", t - 1), ("mma", "mma", ("ACC", t - 1)),
+                        ("commit", "mma", b_empty[(t - 1) % BWD_NST])]
+        mma += [("commit", "mma", res_empty), ("commit", "mma", acc_full)]
+
+    def elementwise(w):
+        prog = []
+        for i, n in enumerate(items):
+            for s in range(n):
+                t = t0[i] + s
+                # S (first half) and all of dP are loaded, then dp_read; S's second half is
+                # loaded and dS written over S after it
+                prog.append(("wait", s_full, t))
+                if mutation == "dp_read_before_load":
+                    prog.append(("arrive", dp_read))
+                prog += [("check", "ew_read", t), ("mark", ("dp_read", t, w))]
+                if mutation != "dp_read_before_load":
+                    prog.append(("arrive", dp_read))
+                prog += [("check", "ew_write", t), ("mark", ("x", t, w)), ("arrive", x_full)]
+            prog += [("wait", acc_full, i), ("check", "acc_read", i), ("mark", ("acc_read", i, w)), ("arrive", acc_empty)]
+        return prog
+
+    progs = {"load": load, "mma": mma}
+    for w in range(warps):
+        progs[f"ew{w}"] = elementwise(w)
+    return progs, bars, t0, buf
+
+
+def explore_dq(items, warps, mutation=None):
+    """The dQ kernel's protocol on the work list ``items`` (steps per item)."""
+    progs, bars, t0, buf = build_dq(items, warps, mutation)
+    key_bar = {a[2]: a[1] for a in progs["load"] if a[0] == "tma"}
+    entries = [a for a in progs["mma"] if a[0] in ("mma", "commit")]
+    qpos = {a[2]: k for k, a in enumerate(entries) if a[0] == "mma"}
+    mma_pc = {a[2]: pc for pc, a in enumerate(progs["mma"]) if a[0] == "mma"}
+    marks = mark_pcs(progs)
+    n_steps = sum(items)
+    item_of = {t0[i] + s: i for i in range(len(items)) for s in range(items[i])}
+
+    def done(comp, key):
+        return comp["mma"] > qpos[key]
+
+    def issued(pcs, key):
+        return pcs["mma"] > mma_pc[key]
+
+    def passed(pcs, key):  # every warp is past the mark
+        return all(pcs[r] >= pc for (k, r, pc) in ((k, *marks[k]) for k in marks)
+                   if k[0] == key[0] and k[1:-1] == key[1:])
+
+    def prev_user(t):  # the previous step that used t's S buffer
+        return max((u for u in range(t) if buf[u] == buf[t]), default=None)
+
+    def next_user(t):
+        return min((u for u in range(t + 1, n_steps) if buf[u] == buf[t]), default=None)
+
+    def hazard_free(kind, arg, pcs, comp, loaded):
+        if kind == "s_issue":  # S buffer: the warps are done with its previous step
+            u = prev_user(arg)
+            return ("B", arg) in loaded and ("R", item_of[arg]) in loaded and (
+                u is None or (passed(pcs, ("x", u)) and issued(pcs, ("ACC", u))))
+        if kind == "dp_issue":  # the dP buffer: every warp holds the previous step's dP
+            return arg == 0 or passed(pcs, ("dp_read", arg - 1))
+        if kind == "ew_read":
+            nu = next_user(arg)
+            return (done(comp, ("S", arg)) and done(comp, ("DP", arg))
+                    and (nu is None or not issued(pcs, ("S", nu)))
+                    and (arg + 1 >= n_steps or not issued(pcs, ("DP", arg + 1))))
+        if kind == "ew_write":
+            nu = next_user(arg)
+            return nu is None or not issued(pcs, ("S", nu))
+        if kind == "acc_issue":  # dS written by every warp; a new item's accumulator read out
+            i = item_of[arg]
+            if arg == t0[i] and i > 0 and not passed(pcs, ("acc_read", i - 1)):
+                return False
+            return passed(pcs, ("x", arg))
+        if kind == "acc_read":
+            return all(done(comp, ("ACC", t)) for t in range(t0[arg], t0[arg] + items[arg]))
+        if kind == "stage_load":
+            u = arg - BWD_NST
+            return u < 0 or all(done(comp, (k, u)) for k in ("S", "DP", "ACC"))
+        if kind == "res_load":
+            return arg == 0 or all(done(comp, (k, t)) for k in ("S", "DP")
+                                   for t in range(t0[arg - 1], t0[arg - 1] + items[arg - 1]))
+        raise AssertionError(kind)
+
+    return run_model(progs, bars, key_bar, ["mma"], hazard_free)
+
+
+@pytest.mark.parametrize("items,warps", [([3], 1), ([2, 1], 1), ([1, 3], 2), ([2, 2], 2), ([4, 1, 2], 1)])
+def test_dq_protocol_has_no_deadlock_aliasing_or_hazard(items, warps):
+    assert explore_dq(items, warps) > 100
+
+
+@pytest.mark.parametrize("mutation,items,warps", [
+    # step s released before the warps' dS of step s - 1 is seen: one warp runs a step ahead,
+    # and x_full's phase completes on its two arrivals (two warps), or wraps (one warp)
+    ("s_full_before_x_full", [4], 2),
+    ("s_full_before_x_full", [4], 1),
+    ("dp_read_before_load", [3], 1),    # dP overwritten before the warps hold it
+])
+def test_the_dq_model_catches_a_planted_mistake(mutation, items, warps):
+    with pytest.raises(AssertionError):
+        explore_dq(items, warps, mutation)
