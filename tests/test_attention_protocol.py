@@ -481,3 +481,136 @@ def test_dq_protocol_has_no_deadlock_aliasing_or_hazard(items, warps):
 def test_the_dq_model_catches_a_planted_mistake(mutation, items, warps):
     with pytest.raises(AssertionError):
         explore_dq(items, warps, mutation)
+
+
+# ---------------------------------------------------------------------------------------------
+# The backward dK/dV kernel (csrc/attention_bwd.cu, dK/dV mode): resident K and V per work item,
+# Q_j / dO_j tiles per 64-query step in a ring of DKV_NST stages, one MMA-issuing thread, the
+# elementwise warps.  Each step: the warps stage the step's log-sum-exp and row sums in one of two
+# shared buffers (each warp writes part, every warp reads all of it) and meet at a named barrier
+# before reading; the MMA thread computes S^T and dP^T of step s into
+# the single S and dP buffers after the previous step's accumulating MMAs (dV += P^T dO,
+# dK += dS^T Q), which it issues once the warps have written P^T and dS^T over S and dP (x_full).
+DKV_NST = 2
+
+
+def build_dkv(items, warps, mutation=None):
+    bars = {}
+
+    def bar(name, count):
+        bars[name] = Bar(name, count)
+        return name
+
+    res_full, res_empty = bar("res_full", 1), bar("res_empty", 1)
+    s_full, x_full = bar("s_full", 1), bar("x_full", warps)
+    acc_full, acc_empty = bar("acc_full", 1), bar("acc_empty", warps)
+    ebar = bar("elem_bar", warps)  # the named barrier, arrive-and-wait
+    b_full = [bar(f"b_full{k}", 1) for k in range(DKV_NST)]
+    b_empty = [bar(f"b_empty{k}", 1) for k in range(DKV_NST)]
+    t0 = list(itertools.accumulate([0] + items))[:-1]
+
+    load = []
+    for i, n in enumerate(items):
+        load += [("wait", res_empty, i - 1), ("check", "res_load", i), ("tma", res_full, ("R", i))]
+        for s in range(n):
+            t = t0[i] + s
+            load += [("wait", b_empty[t % DKV_NST], t // DKV_NST - 1), ("check", "stage_load", t),
+                     ("tma", b_full[t % DKV_NST], ("B", t))]
+
+    mma = []
+    for i, n in enumerate(items):
+        mma.append(("wait", res_full, i))
+        if i > 0:
+            mma.append(("wait", acc_empty, i - 1))
+        for s in range(n + 1):
+            t = t0[i] + s
+            if s < n:
+                mma.append(("wait", b_full[t % DKV_NST], t // DKV_NST))
+            step = [("check", "s_issue", t), ("mma", "mma", ("S", t)), ("commit", "mma", s_full)] if s < n else []
+            if mutation == "s_before_acc":
+                mma += step
+            if s > 0:
+                mma += [("wait", x_full, t - 1), ("check", "acc_issue", t - 1), ("mma", "mma", ("ACC", t - 1)),
+                        ("commit", "mma", b_empty[(t - 1) % DKV_NST])]
+            if mutation != "s_before_acc":
+                mma += step
+        mma += [("commit", "mma", res_empty), ("commit", "mma", acc_full)]
+
+    def elementwise(w):
+        prog = []
+        for i, n in enumerate(items):
+            for s in range(n):
+                t = t0[i] + s
+                # each warp stages its part of the step's values, which every warp then reads
+                prog += [("check", "sf_write", t), ("mark", ("sfw", t, w))]
+                if mutation != "no_named_barrier":
+                    prog += [("arrive", ebar), ("wait", ebar, t)]
+                prog += [("wait", s_full, t), ("check", "ew_read", t), ("mark", ("sf", t, w)),
+                         ("mark", ("x", t, w)), ("arrive", x_full)]
+            prog += [("wait", acc_full, i), ("check", "acc_read", i), ("mark", ("acc_read", i, w)), ("arrive", acc_empty)]
+        return prog
+
+    progs = {"load": load, "mma": mma}
+    for w in range(warps):
+        progs[f"ew{w}"] = elementwise(w)
+    return progs, bars, t0
+
+
+def explore_dkv(items, warps, mutation=None):
+    """The dK/dV kernel's protocol on the work list ``items`` (steps per item)."""
+    progs, bars, t0 = build_dkv(items, warps, mutation)
+    key_bar = {a[2]: a[1] for a in progs["load"] if a[0] == "tma"}
+    entries = [a for a in progs["mma"] if a[0] in ("mma", "commit")]
+    qpos = {a[2]: k for k, a in enumerate(entries) if a[0] == "mma"}
+    mma_pc = {a[2]: pc for pc, a in enumerate(progs["mma"]) if a[0] == "mma"}
+    marks = mark_pcs(progs)
+    item_of = {t0[i] + s: i for i in range(len(items)) for s in range(items[i])}
+
+    def done(comp, key):
+        return comp["mma"] > qpos[key]
+
+    def issued(pcs, key):
+        return pcs["mma"] > mma_pc[key]
+
+    def passed(pcs, key):
+        return all(pcs[r] >= pc for k, (r, pc) in marks.items() if k[0] == key[0] and k[1:-1] == key[1:])
+
+    def hazard_free(kind, arg, pcs, comp, loaded):
+        if kind == "s_issue":  # S and dP hold P^T, dS^T of the previous step until its MMAs read them
+            return (("B", arg) in loaded and ("R", item_of[arg]) in loaded
+                    and (arg == 0 or (passed(pcs, ("x", arg - 1)) and issued(pcs, ("ACC", arg - 1)))))
+        if kind == "ew_read":  # S and dP computed and not yet overwritten; every warp's staging written
+            nxt = ("S", arg + 1)
+            return (done(comp, ("S", arg)) and (nxt not in mma_pc or not issued(pcs, nxt))
+                    and passed(pcs, ("sfw", arg)))
+        if kind == "acc_issue":
+            i = item_of[arg]
+            if arg == t0[i] and i > 0 and not passed(pcs, ("acc_read", i - 1)):
+                return False
+            return passed(pcs, ("x", arg))
+        if kind == "acc_read":
+            return all(done(comp, ("ACC", t)) for t in range(t0[arg], t0[arg] + items[arg]))
+        if kind == "stage_load":
+            u = arg - DKV_NST
+            return u < 0 or (done(comp, ("S", u)) and done(comp, ("ACC", u)))
+        if kind == "res_load":
+            return arg == 0 or all(done(comp, ("S", t)) for t in range(t0[arg - 1], t0[arg - 1] + items[arg - 1]))
+        if kind == "sf_write":  # staging buffer t mod 2: every warp is done with step t - 2
+            return arg < 2 or passed(pcs, ("sf", arg - 2))
+        raise AssertionError(kind)
+
+    return run_model(progs, bars, key_bar, ["mma"], hazard_free)
+
+
+@pytest.mark.parametrize("items,warps", [([3], 1), ([2, 1], 2), ([1, 3], 2), ([4, 1, 2], 1)])
+def test_dkv_protocol_has_no_deadlock_aliasing_or_hazard(items, warps):
+    assert explore_dkv(items, warps) > 100
+
+
+@pytest.mark.parametrize("mutation,items,warps", [
+    ("s_before_acc", [3], 1),        # S^T overwrites P^T before dV += P^T dO has read it
+    ("no_named_barrier", [3], 2),    # a warp reads the step's staged values before another wrote its part
+])
+def test_the_dkv_model_catches_a_planted_mistake(mutation, items, warps):
+    with pytest.raises(AssertionError):
+        explore_dkv(items, warps, mutation)
