@@ -519,6 +519,25 @@ def build_attention_cycles_lib() -> str:
     return lib
 
 
+def attention_cycles_report(c, B, S, H, hd, causal, launches):
+    """Cycles per 64-key sub-block and CTA for each role, from the summed counter slots of the
+    instrumented attention copy (see ATTN_CYCLE_PATCHES)."""
+    n_pv, n_qk = c[4], c[12]  # sub-blocks summed over the CTAs (each issuer sees every sub-block)
+    warps = 4.0 * n_pv        # the softmax counters are summed over the four warps of each CTA: per warp
+    per = lambda v, n: round(v / n, 1) if n else None
+    line = {"metric": "attention_cycles_per_subblock", "unit": "SM cycles per 64-key sub-block and CTA",
+            "config": {"B": B, "S": S, "n_heads": H, "head_dim": hd, "causal": bool(causal), "launches": launches},
+            "pv_thread": {"total": per(c[0], n_pv), "waiting_for_p": per(c[1], n_pv),
+                          "waiting_for_kv": per(c[2], n_pv), "issuing": per(c[3], n_pv)},
+            "qk_thread": {"total": per(c[8], n_qk), "waiting_for_pv": per(c[9], n_qk),
+                          "waiting_for_kv": per(c[10], n_qk), "issuing": per(c[11], n_qk)},
+            "softmax_warp": {"total": per(c[5], warps), "waiting_for_s": per(c[6], warps),
+                             "subblock_loop": per(c[7], warps), "output": per(c[13], warps)},
+            "note": "instrumented copy of attention.cu (clock64 around each wait and issue sequence); "
+                    "the counters slow the kernel a few per cent"}
+    return line
+
+
 def attention_cycles_bench(args):
     """The forward attention kernel's cycles per 64-key sub-block and CTA, per role, from the
     instrumented copy (B,S,H,head_dim,causal; one warm-up launch, then --steps launches)."""
@@ -548,21 +567,7 @@ def attention_cycles_bench(args):
     if lib.tfl_attn_cycles_fetch(buf) != 0:
         raise RuntimeError("tfl_attn_cycles_fetch failed")
     pkg.tfl_attn_destroy(a)
-    c = [float(v) for v in buf]
-    n_pv, n_qk = c[4], c[12]  # sub-blocks summed over the CTAs (each issuer sees every sub-block)
-    warps = 4.0 * n_pv        # the softmax counters are summed over four warps a CTA
-    per = lambda v, n: round(v / n, 1) if n else None
-    line = {"metric": "attention_cycles_per_subblock", "unit": "SM cycles per 64-key sub-block and CTA",
-            "config": {"B": B, "S": S, "n_heads": H, "head_dim": hd, "causal": bool(causal), "launches": args.steps},
-            "pv_thread": {"total": per(c[0], n_pv), "waiting_for_p": per(c[1], n_pv),
-                          "waiting_for_kv": per(c[2], n_pv), "issuing": per(c[3], n_pv)},
-            "qk_thread": {"total": per(c[8], n_qk), "waiting_for_pv": per(c[9], n_qk),
-                          "waiting_for_kv": per(c[10], n_qk), "issuing": per(c[11], n_qk)},
-            "softmax_warp": {"total": per(c[5] * 4, warps), "waiting_for_s": per(c[6] * 4, warps),
-                             "subblock_loop": per(c[7] * 4, warps), "output": per(c[13] * 4, warps)},
-            "note": "instrumented copy of attention.cu (clock64 around each wait and issue sequence); "
-                    "the counters slow the kernel a few per cent"}
-    print(json.dumps(line))
+    print(json.dumps(attention_cycles_report([float(v) for v in buf], B, S, H, hd, causal, args.steps)))
 
 
 def attention_backward_bench(args):

@@ -141,3 +141,18 @@ def test_attention_cycles_copy_applies_and_builds(tmp_path):
 def test_attention_cycles_copy_refuses_a_changed_kernel():
     with pytest.raises(RuntimeError, match="anchor"):
         bench.attention_cycles_source("namespace tfl {\n}  // namespace tfl\n")
+
+
+def test_attention_cycles_report_divides_per_subblock_and_warp():
+    # two CTAs of 10 sub-blocks: issuer counters summed over the CTAs, softmax counters over the
+    # four warps of each CTA as well
+    c = [0.0] * 16
+    c[4] = c[12] = 20.0
+    c[0], c[1], c[2], c[3] = 1000 * 20.0, 300 * 20.0, 50 * 20.0, 600 * 20.0
+    c[8], c[9], c[10], c[11] = 900 * 20.0, 200 * 20.0, 80 * 20.0, 500 * 20.0
+    c[5], c[6], c[7], c[13] = (v * 20 * 4 for v in (1000.0, 150.0, 980.0, 15.0))
+    r = bench.attention_cycles_report(c, 2, 16384, 16, 64, 1, 3)
+    assert r["pv_thread"] == {"total": 1000.0, "waiting_for_p": 300.0, "waiting_for_kv": 50.0, "issuing": 600.0}
+    assert r["qk_thread"] == {"total": 900.0, "waiting_for_pv": 200.0, "waiting_for_kv": 80.0, "issuing": 500.0}
+    assert r["softmax_warp"] == {"total": 1000.0, "waiting_for_s": 150.0, "subblock_loop": 980.0, "output": 15.0}
+    assert r["config"]["launches"] == 3
