@@ -1,5 +1,5 @@
-"""Exhaustive interleaving models of the attention kernels' hand-off protocols (CPU): the
-forward kernel below, and the backward dQ kernel further down.
+"""Exhaustive interleaving models of the kernels' hand-off protocols (CPU): the forward
+attention kernel first, then the backward dQ and dK/dV kernels and the projection GEMM.
 
 The kernel (csrc/attention.cu) runs five roles per CTA: a loader (work items, Q, K/V stages),
 a thread issuing Q K^T, a thread issuing P V, and four softmax warps.  They meet at mbarriers
@@ -614,3 +614,100 @@ def test_dkv_protocol_has_no_deadlock_aliasing_or_hazard(items, warps):
 def test_the_dkv_model_catches_a_planted_mistake(mutation, items, warps):
     with pytest.raises(AssertionError):
         explore_dkv(items, warps, mutation)
+
+
+# ---------------------------------------------------------------------------------------------
+# The projection GEMM (csrc/gemm.cu): a loader filling a ring of GEMM_STAGES k-block stages, one
+# MMA-issuing thread accumulating each tile's k-blocks into one of two tensor-memory
+# accumulators, and the epilogue warps reading a finished accumulator.  Per tile the MMA thread
+# waits until the epilogue has read the accumulator's previous tile (acce), then for each
+# k-block waits for the stage (full), issues, and frees the stage (commit empty); it commits accf
+# after the last k-block.  The epilogue warps wait accf, read, and arrive on acce.
+GEMM_STAGES = 3
+
+
+def build_gemm(tiles, num_k, warps, mutation=None):
+    bars = {}
+
+    def bar(name, count):
+        bars[name] = Bar(name, count)
+        return name
+
+    full = [bar(f"full{k}", 1) for k in range(GEMM_STAGES)]
+    empty = [bar(f"empty{k}", 1) for k in range(GEMM_STAGES)]
+    accf = [bar(f"accf{k}", 1) for k in range(2)]
+    acce = [bar(f"acce{k}", warps) for k in range(2)]
+    load, mma = [], []
+    j = 0  # k-block load index over the CTA's tiles
+    for t in range(tiles):
+        for kb in range(num_k):
+            load += [("wait", empty[j % GEMM_STAGES], j // GEMM_STAGES - 1), ("check", "stage_load", j),
+                     ("tma", full[j % GEMM_STAGES], ("K", j))]
+            j += 1
+    j = 0
+    for t in range(tiles):
+        a = t % 2
+        if mutation != "mma_skips_acce":
+            mma.append(("wait", acce[a], t // 2 - 1))
+        for kb in range(num_k):
+            s = j % GEMM_STAGES
+            mma.append(("wait", full[s], j // GEMM_STAGES))
+            if mutation == "empty_before_mma":
+                mma.append(("commit", "mma", empty[s]))
+            mma += [("check", "mma_issue", (t, kb, j)), ("mma", "mma", ("M", j))]
+            if mutation != "empty_before_mma":
+                mma.append(("commit", "mma", empty[s]))
+            j += 1
+        mma.append(("commit", "mma", accf[a]))
+
+    def epilogue(w):
+        prog = []
+        for t in range(tiles):
+            prog += [("wait", accf[t % 2], t // 2), ("check", "acc_read", t), ("mark", ("acc_read", t, w)),
+                     ("arrive", acce[t % 2])]
+        return prog
+
+    progs = {"load": load, "mma": mma}
+    for w in range(warps):
+        progs[f"epi{w}"] = epilogue(w)
+    return progs, bars
+
+
+def explore_gemm(tiles, num_k, warps, mutation=None):
+    """The GEMM's protocol for ``tiles`` tiles of ``num_k`` k-blocks on one CTA."""
+    progs, bars = build_gemm(tiles, num_k, warps, mutation)
+    key_bar = {a[2]: a[1] for a in progs["load"] if a[0] == "tma"}
+    entries = [a for a in progs["mma"] if a[0] in ("mma", "commit")]
+    qpos = {a[2]: k for k, a in enumerate(entries) if a[0] == "mma"}
+    marks = mark_pcs(progs)
+
+    def done(comp, key):
+        return comp["mma"] > qpos[key]
+
+    def passed(pcs, key):
+        return all(pcs[r] >= pc for k, (r, pc) in marks.items() if k[0] == key[0] and k[1:-1] == key[1:])
+
+    def hazard_free(kind, arg, pcs, comp, loaded):
+        if kind == "stage_load":  # the stage's previous k-block has been read by its MMAs
+            return arg < GEMM_STAGES or done(comp, ("M", arg - GEMM_STAGES))
+        if kind == "mma_issue":  # operands loaded; the first k-block overwrites the accumulator
+            t, kb, j = arg
+            if ("K", j) not in loaded:
+                return False
+            return kb > 0 or t < 2 or passed(pcs, ("acc_read", t - 2))
+        if kind == "acc_read":
+            return all(done(comp, ("M", arg * num_k + kb)) for kb in range(num_k))
+        raise AssertionError(kind)
+
+    return run_model(progs, bars, key_bar, ["mma"], hazard_free)
+
+
+@pytest.mark.parametrize("tiles,num_k,warps", [(3, 2, 1), (4, 1, 2), (2, 4, 2), (5, 2, 1)])
+def test_gemm_protocol_has_no_deadlock_aliasing_or_hazard(tiles, num_k, warps):
+    assert explore_gemm(tiles, num_k, warps) > 100
+
+
+@pytest.mark.parametrize("mutation", ["mma_skips_acce", "empty_before_mma"])
+def test_the_gemm_model_catches_a_planted_mistake(mutation):
+    with pytest.raises(AssertionError):
+        explore_gemm(4, 2, 2, mutation)
