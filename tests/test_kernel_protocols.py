@@ -1,5 +1,6 @@
 """Exhaustive interleaving models of the kernels' hand-off protocols (CPU): the forward
-attention kernel first, then the backward dQ and dK/dV kernels and the projection GEMM.
+attention kernel first, then the backward dQ and dK/dV kernels, the projection GEMM and the fused
+post-attention chain.
 
 The kernel (csrc/attention.cu) runs five roles per CTA: a loader (work items, Q, K/V stages),
 a thread issuing Q K^T, a thread issuing P V, and four softmax warps.  They meet at mbarriers
@@ -711,3 +712,234 @@ def test_gemm_protocol_has_no_deadlock_aliasing_or_hazard(tiles, num_k, warps):
 def test_the_gemm_model_catches_a_planted_mistake(mutation):
     with pytest.raises(AssertionError):
         explore_gemm(4, 2, 2, mutation)
+
+
+# ---------------------------------------------------------------------------------------------
+# The fused post-attention chain (csrc/postchain.cu, d_model 128, pre-LN): a loader (the
+# attention output tile O per tile; weight blocks through a two-slot ring in the order Wo, W1_0,
+# W1_1, then W2_c and W1_(c+2) per d_ff chunk c, then the next layer's W_qkv in three blocks), an
+# issuer for o_proj / FFN-out / next-layer QKV (one thread), an issuer for FFN-in (another), and
+# the epilogue warps, which meet at one named barrier in each row-statistics exchange (two slot
+# pairs, used alternately).  Tensor memory: A1 / t / OUT and then N (the next QKV's input) in
+# [0, 128), N2 [128, 256), G [256, 384), GP [384, 512); the next layer's q, k, v are computed
+# into [128, 256), [256, 384), [384, 512).
+def build_chain(tiles, nch, warps, fuse, mutation=None):
+    bars = {}
+
+    def bar(name, count):
+        bars[name] = Bar(name, count)
+        return name
+
+    o_full, o_free = bar("o_full", 1), bar("o_free", 1)
+    acc_full, acc_read = bar("acc_full", 1), bar("acc_read", warps)
+    out_full, out_read = bar("out_full", 1), bar("out_read", warps)
+    g_full, g_read = bar("g_full", 1), bar("g_read", warps)
+    gp_ready, gp_free = bar("gp_ready", warps), bar("gp_free", 1)
+    n_ready = bar("n_ready", warps)
+    qkv_full = [bar(f"qkv_full{j}", 1) for j in range(3)]
+    r_full = [bar(f"r_full{k}", 1) for k in range(2)]
+    r_empty = [bar(f"r_empty{k}", 1) for k in range(2)]
+    epi = bar("epi_bar", warps)  # the named barrier, arrive-and-wait
+
+    order = [("Wo",), ("W1", 0)] + ([("W1", 1)] if nch > 1 else [])
+    for c in range(nch):
+        order.append(("W2", c))
+        if c + 2 < nch:
+            order.append(("W1", c + 2))
+    if fuse:
+        order += [("Q", j) for j in range(3)]
+    units = len(order)
+    pos = {u: k for k, u in enumerate(order)}
+    # the issuers' own index formulas agree with the loader's order
+    for k in range(nch):
+        assert pos[("W1", k)] == (1 if k == 0 else (2 if k == 1 else 2 * k))
+        assert pos[("W2", k)] == (3 + 2 * k if k <= nch - 2 else 2 * nch)
+
+    load = []
+    for ts in range(tiles):
+        load += [("wait", o_free, ts - 1), ("check", "o_load", ts), ("tma", o_full, ("O", ts))]
+        for k in range(units):
+            g = ts * units + k
+            load += [("wait", r_empty[g % 2], g // 2 - 1), ("check", "ring_load", g), ("tma", r_full[g % 2], ("U", g))]
+
+    def take(g):
+        return [("wait", r_full[g % 2], g // 2)]
+
+    mma1, mma2 = [], []
+    for ts in range(tiles):
+        g0 = ts * units
+        if ts > 0:
+            mma1.append(("wait", out_read, ts - 1))
+        mma1 += [("wait", o_full, ts)] + take(g0) + [
+            ("check", "op_issue", ts), ("mma", "mma1", ("OP", ts)), ("commit", "mma1", r_empty[g0 % 2]),
+            ("commit", "mma1", o_free), ("commit", "mma1", acc_full)]
+        for c in range(nch):
+            g = g0 + pos[("W2", c)]
+            mma1 += [("wait", gp_ready, ts * nch + c)] + take(g) + [
+                ("check", "f2_issue", (ts, c)), ("mma", "mma1", ("F2", ts, c)), ("commit", "mma1", r_empty[g % 2]),
+                ("commit", "mma1", gp_free)]
+        mma1.append(("commit", "mma1", out_full))
+        if fuse:
+            mma1.append(("wait", n_ready, ts))
+            for j in range(3):
+                g = g0 + pos[("Q", j)]
+                mma1 += take(g) + [("check", "qkv_issue", (ts, j)), ("mma", "mma1", ("QKV", ts, j)),
+                                   ("commit", "mma1", r_empty[g % 2]), ("commit", "mma1", qkv_full[j])]
+            if mutation != "next_oproj_before_qkv_done":
+                mma1.append(("wait", qkv_full[2], ts))
+
+        def ffn1(k):
+            g = g0 + pos[("W1", k)]
+            return take(g) + [("check", "f1_issue", (ts, k)), ("mma", "mma2", ("F1", ts, k)),
+                              ("commit", "mma2", r_empty[g % 2]), ("commit", "mma2", g_full)]
+        mma2 += [("wait", acc_read, ts)] + ffn1(0)
+        for c in range(nch):
+            if mutation != "ffn1_before_g_read":
+                mma2.append(("wait", g_read, ts * nch + c))
+            if c + 1 < nch:
+                mma2 += ffn1(c + 1)
+
+    def epilogue(w):
+        prog, n = [], 0  # n: row-statistics exchanges so far
+
+        def stats():
+            nonlocal n
+            step = [("check", "red_write", n)]
+            if mutation != "no_named_barrier":
+                step += [("arrive", epi), ("wait", epi, n)]
+            step.append(("mark", ("red_read", n, w)))
+            n += 1
+            return step
+        for ts in range(tiles):
+            prog += [("wait", acc_full, ts), ("check", "read_a1", ts), ("mark", ("a1w", ts, w))]
+            prog += stats()
+            prog += [("check", "n2_write", ts), ("mark", ("n2w", ts, w)), ("arrive", acc_read)]
+            for c in range(nch):
+                k = ts * nch + c
+                prog += [("wait", g_full, k), ("check", "read_g", (ts, c)), ("mark", ("gread", ts, c, w)),
+                         ("arrive", g_read)]
+                if k > 0 and mutation != "gp_write_without_gp_free":
+                    prog.append(("wait", gp_free, k - 1))
+                prog += [("check", "gp_write", (ts, c)), ("mark", ("gpw", ts, c, w)), ("arrive", gp_ready)]
+            prog += [("wait", out_full, ts), ("check", "read_out", ts), ("mark", ("outread", ts, w)),
+                     ("arrive", out_read)]
+            if fuse:
+                prog += stats()
+                prog += [("mark", ("nw", ts, w)), ("arrive", n_ready)]
+                for j in range(3):
+                    prog += [("wait", qkv_full[j], ts), ("check", "read_qkv", (ts, j)), ("mark", ("qkvread", ts, j, w))]
+        return prog
+
+    progs = {"load": load, "mma1": mma1, "mma2": mma2}
+    for w in range(warps):
+        progs[f"epi{w}"] = epilogue(w)
+    return progs, bars, units, pos
+
+
+def explore_chain(tiles, nch, warps, fuse, mutation=None):
+    """The chain's protocol for ``tiles`` tiles of ``nch`` d_ff chunks on one CTA."""
+    progs, bars, units, pos = build_chain(tiles, nch, warps, fuse, mutation)
+    key_bar = {a[2]: a[1] for a in progs["load"] if a[0] == "tma"}
+    qpos = {t: {a[2]: k for k, a in enumerate([a for a in progs[t] if a[0] in ("mma", "commit")]) if a[0] == "mma"}
+            for t in ("mma1", "mma2")}
+    mma_pc = {a[2]: (t, pc) for t in ("mma1", "mma2") for pc, a in enumerate(progs[t]) if a[0] == "mma"}
+    marks = mark_pcs(progs)
+    unit_mma = {}  # ring unit -> the MMA that reads it
+    for ts in range(tiles):
+        for u, k in pos.items():
+            key = {"Wo": ("OP", ts), "W1": ("F1", ts, u[-1]), "W2": ("F2", ts, u[-1]), "Q": ("QKV", ts, u[-1])}[u[0]]
+            unit_mma[ts * units + k] = key
+
+    def owner(key):
+        return "mma2" if key[0] == "F1" else "mma1"
+
+    def done(comp, key):
+        t = owner(key)
+        return comp[t] > qpos[t][key]
+
+    def issued(pcs, key):
+        t, pc = mma_pc[key]
+        return pcs[t] > pc
+
+    def passed(pcs, key):
+        return all(pcs[r] >= pc for k, (r, pc) in marks.items() if k[0] == key[0] and k[1:-1] == key[1:])
+
+    def loaded_unit(ts, u, loaded):
+        return ("U", ts * units + pos[u]) in loaded
+
+    def hazard_free(kind, arg, pcs, comp, loaded):
+        if kind == "o_load":
+            return arg == 0 or done(comp, ("OP", arg - 1))
+        if kind == "ring_load":
+            return arg < 2 or done(comp, unit_mma[arg - 2])
+        if kind == "op_issue":  # A1 free: OUT read, and N read by the previous tile's QKV MMAs
+            ts = arg
+            if ("O", ts) not in loaded or not loaded_unit(ts, ("Wo",), loaded):
+                return False
+            return ts == 0 or (passed(pcs, ("outread", ts - 1)) and
+                               (not fuse or all(done(comp, ("QKV", ts - 1, j)) for j in range(3))))
+        if kind == "read_a1":
+            return done(comp, ("OP", arg))
+        if kind == "n2_write":  # N2 free: FFN-in of the previous tile done, its q read by every warp
+            ts = arg
+            return ts == 0 or (all(done(comp, ("F1", ts - 1, k)) for k in range(nch)) and
+                               (not fuse or passed(pcs, ("qkvread", ts - 1, 0))))
+        if kind == "f1_issue":
+            ts, k = arg
+            if not loaded_unit(ts, ("W1", k), loaded) or not passed(pcs, ("n2w", ts)):
+                return False
+            if k > 0:
+                return passed(pcs, ("gread", ts, k - 1))
+            return ts == 0 or (passed(pcs, ("gread", ts - 1, nch - 1)) and
+                               (not fuse or passed(pcs, ("qkvread", ts - 1, 1))))
+        if kind == "read_g":
+            ts, c = arg
+            nxt = ("F1", ts, c + 1)
+            return done(comp, ("F1", ts, c)) and (c + 1 >= nch or not issued(pcs, nxt))
+        if kind == "gp_write":  # GP free: FFN-out of the previous chunk done, the previous tile's v read
+            ts, c = arg
+            k = ts * nch + c
+            prev = (ts, c - 1) if c > 0 else (ts - 1, nch - 1)
+            if k > 0 and not done(comp, ("F2",) + prev):
+                return False
+            return not (fuse and c == 0 and ts > 0) or passed(pcs, ("qkvread", ts - 1, 2))
+        if kind == "f2_issue":
+            ts, c = arg
+            return (loaded_unit(ts, ("W2", c), loaded) and passed(pcs, ("gpw", ts, c))
+                    and passed(pcs, ("a1w", ts)))
+        if kind == "read_out":
+            return all(done(comp, ("F2", arg, c)) for c in range(nch))
+        if kind == "qkv_issue":  # N written; q over N2 after FFN-in; k over G after its last read
+            ts, j = arg
+            if not loaded_unit(ts, ("Q", j), loaded) or not passed(pcs, ("nw", ts)):
+                return False
+            if j == 0:
+                return all(done(comp, ("F1", ts, k)) for k in range(nch))
+            if j == 1:
+                return passed(pcs, ("gread", ts, nch - 1))
+            return True  # v over GP: FFN-out of the last chunk was issued before, by this thread
+        if kind == "read_qkv":  # (their regions' next writers check that every warp has read them)
+            ts, j = arg
+            return done(comp, ("QKV", ts, j))
+        if kind == "red_write":  # slot pair n % 2: every warp has read exchange n - 2
+            return arg < 2 or passed(pcs, ("red_read", arg - 2))
+        raise AssertionError(kind)
+
+    return run_model(progs, bars, key_bar, ["mma1", "mma2"], hazard_free)
+
+
+@pytest.mark.parametrize("tiles,nch,warps,fuse", [(2, 1, 1, True), (2, 2, 1, True), (2, 3, 1, False),
+                                                  (2, 2, 2, True), (3, 1, 2, False)])
+def test_chain_protocol_has_no_deadlock_aliasing_or_hazard(tiles, nch, warps, fuse):
+    assert explore_chain(tiles, nch, warps, fuse) > 100
+
+
+@pytest.mark.parametrize("mutation,tiles,nch,warps,fuse", [
+    ("next_oproj_before_qkv_done", 2, 1, 1, True),  # o_proj overwrites N under the QKV products
+    ("no_named_barrier", 2, 1, 2, True),            # a warp writes N2 while another reads q
+    ("ffn1_before_g_read", 1, 2, 1, False),         # G overwritten before the epilogue read it
+    ("gp_write_without_gp_free", 1, 2, 1, False),   # GP rewritten under FFN-out
+])
+def test_the_chain_model_catches_a_planted_mistake(mutation, tiles, nch, warps, fuse):
+    with pytest.raises(AssertionError):
+        explore_chain(tiles, nch, warps, fuse, mutation)
