@@ -1,6 +1,6 @@
 """Exhaustive interleaving models of the kernels' hand-off protocols (CPU): the forward
-attention kernel first, then the backward dQ and dK/dV kernels, the projection GEMM and the fused
-post-attention chain.
+attention kernel first, then the backward dQ and dK/dV kernels, the projection GEMM, the fused
+post-attention chain and the whole-stack kernel.
 
 The kernel (csrc/attention.cu) runs five roles per CTA: a loader (work items, Q, K/V stages),
 a thread issuing Q K^T, a thread issuing P V, and four softmax warps.  They meet at mbarriers
@@ -943,3 +943,266 @@ def test_chain_protocol_has_no_deadlock_aliasing_or_hazard(tiles, nch, warps, fu
 def test_the_chain_model_catches_a_planted_mistake(mutation, tiles, nch, warps, fuse):
     with pytest.raises(AssertionError):
         explore_chain(tiles, nch, warps, fuse, mutation)
+
+
+# ---------------------------------------------------------------------------------------------
+# The whole-stack kernel (csrc/stack.cu, S <= 128, d_model 128, pre-LN): per sequence and layer
+# ("tile-layer" s), one MMA thread issues k, v, q (into accumulators A and B of tensor memory),
+# per head S = Q K^T into A, P V into B and the row sums, o_proj onto the residual R and FFN-out;
+# another issues FFN-in into A; the epilogue warps drain k and v to shared memory, q into
+# tensor memory, run each head's softmax (a named-barrier exchange of the row maximum, P over S),
+# form O / l, and run the chain's three phases; the sequence's output leaves through per-warp
+# stages that reuse the K tiles' shared memory.  Tensor memory: R [0, 128); N, then Q [128, 192)
+# and O / l [192, 256), then N2, in [128, 256); A [256, 384): k, q, S / P of each head, G;
+# B [384, 512): v, each head's O, GP.  HEADS heads per layer (the kernel has four; the model two).
+STACK_HEADS = 2
+
+
+def build_stack(seqs, layers, nch, warps, mutation=None):
+    bars = {}
+
+    def bar(name, count):
+        bars[name] = Bar(name, count)
+        return name
+
+    H = STACK_HEADS
+    per_tile = ["n_ready", "k_read", "kv_ready", "q_ready", "o_ready", "acc_read"]
+    b = {n: bar(n, warps) for n in per_tile}
+    for n in ["acc_k", "acc_v", "acc_q", "acc_full", "out_full", "s_full", "g_full", "gp_free"]:
+        b[n] = bar(n, 1)
+    for n in ["p_full", "g_read", "gp_ready"]:
+        b[n] = bar(n, warps)
+    pv_done = [bar(f"pv_done{h}", 1) for h in range(H)]
+    r_full = [bar(f"r_full{k}", 1) for k in range(2)]
+    r_empty = [bar(f"r_empty{k}", 1) for k in range(2)]
+    epi = bar("epi_bar", warps)
+
+    order = [("K",), ("V",), ("Q",), ("Wo",), ("W1", 0)] + ([("W1", 1)] if nch > 1 else [])
+    for c in range(nch):
+        order.append(("W2", c))
+        if c + 2 < nch:
+            order.append(("W1", c + 2))
+    units = len(order)
+    pos = {u: k for k, u in enumerate(order)}
+    assert units == 4 + 2 * nch
+    for k in range(nch):  # the issuers' index formulas agree with the loader's order
+        assert pos[("W1", k)] == 3 + (1 if k == 0 else (2 if k == 1 else 2 * k))
+        assert pos[("W2", k)] == 3 + (3 + 2 * k if k <= nch - 2 else 2 * nch)
+    tl = seqs * layers  # tile-layers
+
+    load = []
+    for s in range(tl):
+        for k in range(units):
+            g = s * units + k
+            load += [("wait", r_empty[g % 2], g // 2 - 1), ("check", "ring_load", g), ("tma", r_full[g % 2], ("U", g))]
+
+    def take(g):
+        return [("wait", r_full[g % 2], g // 2)]
+
+    def mm(t, key, g=None):
+        acts = [("check", "issue", key), ("mma", t, key)]
+        if g is not None:
+            acts.append(("commit", t, r_empty[g % 2]))
+        return acts
+
+    mma1, mma2 = [], []
+    for s in range(tl):
+        g0 = s * units
+        mma1.append(("wait", b["n_ready"], s))
+        mma1 += take(g0) + mm("mma1", ("K", s), g0) + [("commit", "mma1", b["acc_k"])]
+        mma1 += take(g0 + 1) + mm("mma1", ("V", s), g0 + 1) + [("commit", "mma1", b["acc_v"])]
+        if mutation != "q_before_k_read":
+            mma1.append(("wait", b["k_read"], s))
+        mma1 += take(g0 + 2) + mm("mma1", ("Q", s), g0 + 2) + [("commit", "mma1", b["acc_q"])]
+        mma1.append(("wait", b["kv_ready"], s))
+        if mutation != "s_before_q_ready":
+            mma1.append(("wait", b["q_ready"], s))
+        for h in range(H):
+            mma1 += mm("mma1", ("S", s, h)) + [("commit", "mma1", b["s_full"]), ("wait", b["p_full"], s * H + h)]
+            mma1 += mm("mma1", ("PV", s, h)) + [("commit", "mma1", pv_done[h])]
+        mma1 += [("wait", b["o_ready"], s)] + take(g0 + 3) + mm("mma1", ("OP", s), g0 + 3) + [
+            ("commit", "mma1", b["acc_full"])]
+        for c in range(nch):
+            g = g0 + pos[("W2", c)]
+            mma1 += [("wait", b["gp_ready"], s * nch + c)] + take(g) + mm("mma1", ("F2", s, c), g) + [
+                ("commit", "mma1", b["gp_free"])]
+        mma1.append(("commit", "mma1", b["out_full"]))
+        if mutation != "ffn1_skips_acc_read":
+            mma2.append(("wait", b["acc_read"], s))
+        for c in range(nch):
+            if c > 0:
+                mma2.append(("wait", b["g_read"], s * nch + c - 1))
+            g = g0 + pos[("W1", c)]
+            mma2 += take(g) + mm("mma2", ("F1", s, c), g) + [("commit", "mma2", b["g_full"])]
+        mma2.append(("wait", b["g_read"], s * nch + nch - 1))
+
+    def epilogue(w):
+        prog, n = [], 0
+
+        def exchange():  # a named-barrier exchange through two alternating slot pairs
+            nonlocal n
+            acts = [("check", "red_write", n)]
+            if mutation != "no_named_barrier":
+                acts += [("arrive", epi), ("wait", epi, n)]
+            acts.append(("mark", ("red_read", n, w)))
+            n += 1
+            return acts
+        for i in range(seqs):
+            for l in range(layers):
+                s = i * layers + l
+                prog += exchange() + [("check", "nr_write", s), ("mark", ("nw", s, w)), ("arrive", b["n_ready"])]
+                prog += [("wait", b["acc_k"], s), ("check", "done", ("K", s)), ("mark", ("kread", s, w)),
+                         ("arrive", b["k_read"]), ("check", "sk_write", s), ("mark", ("skw", s, w)),
+                         ("wait", b["acc_v"], s), ("check", "done", ("V", s)), ("check", "sv_write", s),
+                         ("mark", ("svw", s, w)), ("arrive", b["kv_ready"])]
+                prog += [("wait", b["acc_q"], s), ("check", "done", ("Q", s)), ("check", "q_write", s),
+                         ("mark", ("qw", s, w)), ("arrive", b["q_ready"])]
+                for h in range(H):
+                    prog += [("wait", b["s_full"], s * H + h), ("check", "read_s", (s, h)),
+                             ("mark", ("sread", s, h, w))]
+                    prog += exchange()
+                    prog += [("check", "p_write", (s, h)), ("mark", ("pw", s, h, w)), ("arrive", b["p_full"])]
+                for h in range(H):
+                    if mutation != "o_without_pv_done":
+                        prog.append(("wait", pv_done[h], s))
+                    prog.append(("check", "done", ("PV", s, h)))
+                prog += [("mark", ("ow", s, w)), ("arrive", b["o_ready"])]
+                prog += [("wait", b["acc_full"], s), ("check", "done", ("OP", s)), ("mark", ("p1r", s, w))]
+                prog += exchange() + [("check", "n2_write", s), ("mark", ("n2w", s, w)), ("arrive", b["acc_read"])]
+                for c in range(nch):
+                    k = s * nch + c
+                    prog += [("wait", b["g_full"], k), ("check", "read_g", (s, c)), ("mark", ("gread", s, c, w)),
+                             ("arrive", b["g_read"])]
+                    if k > 0:
+                        prog.append(("wait", b["gp_free"], k - 1))
+                    prog += [("check", "gp_write", (s, c)), ("mark", ("gpw", s, c, w)), ("arrive", b["gp_ready"])]
+                prog += [("wait", b["out_full"], s)] + [("check", "done", ("F2", s, c)) for c in range(nch)]
+            prog += exchange() + [("check", "stage_write", i), ("mark", ("stw", i, w))]
+        return prog
+
+    progs = {"load": load, "mma1": mma1, "mma2": mma2}
+    for w in range(warps):
+        progs[f"epi{w}"] = epilogue(w)
+    return progs, bars, units, pos
+
+
+def explore_stack(seqs, layers, nch, warps, mutation=None):
+    """The whole-stack kernel's protocol for ``seqs`` sequences of ``layers`` layers on one CTA."""
+    progs, bars, units, pos = build_stack(seqs, layers, nch, warps, mutation)
+    H = STACK_HEADS
+    key_bar = {a[2]: a[1] for a in progs["load"] if a[0] == "tma"}
+    qpos = {t: {a[2]: k for k, a in enumerate([a for a in progs[t] if a[0] in ("mma", "commit")]) if a[0] == "mma"}
+            for t in ("mma1", "mma2")}
+    mma_pc = {a[2]: (t, pc) for t in ("mma1", "mma2") for pc, a in enumerate(progs[t]) if a[0] == "mma"}
+    marks = mark_pcs(progs)
+    unit_mma = {}
+    for s in range(seqs * layers):
+        for u, k in pos.items():
+            unit_mma[s * units + k] = {"K": ("K", s), "V": ("V", s), "Q": ("Q", s), "Wo": ("OP", s),
+                                       "W1": ("F1", s) + u[1:], "W2": ("F2", s) + u[1:]}[u[0]]
+
+    def done(comp, key):
+        t = "mma2" if key[0] == "F1" else "mma1"
+        return comp[t] > qpos[t][key]
+
+    def issued(pcs, key):
+        t, pc = mma_pc[key]
+        return pcs[t] > pc
+
+    def passed(pcs, key):
+        return all(pcs[r] >= pc for k, (r, pc) in marks.items() if k[0] == key[0] and k[1:-1] == key[1:])
+
+    def unit_loaded(s, u, loaded):
+        return ("U", s * units + pos[u]) in loaded
+
+    def issue_ok(key, pcs, comp, loaded):
+        kind, s = key[0], key[1]
+        if kind == "K":  # A free: the previous tile-layer's last G read; N written
+            return (unit_loaded(s, ("K",), loaded) and passed(pcs, ("nw", s))
+                    and (s == 0 or passed(pcs, ("gread", s - 1, nch - 1))))
+        if kind == "V":  # B: its previous content, GP, was read by this thread's FFN-out before
+            return unit_loaded(s, ("V",), loaded) and passed(pcs, ("nw", s))
+        if kind == "Q":  # A again: k drained by every warp
+            return unit_loaded(s, ("Q",), loaded) and passed(pcs, ("kread", s))
+        if kind == "S":  # q and the K tiles written; A held q (h = 0) or P of the previous head
+            return passed(pcs, ("qw", s)) and passed(pcs, ("skw", s))
+        if kind == "PV":  # P written by every warp, V tiles in shared memory
+            return passed(pcs, ("pw", s, key[2])) and passed(pcs, ("svw", s))
+        if kind == "OP":  # O / l pairs written by every warp; R holds the residual
+            return unit_loaded(s, ("Wo",), loaded) and passed(pcs, ("ow", s)) and passed(pcs, ("nw", s))
+        if kind == "F1":  # N2 written; A: P of the last head read by its P V, or G read
+            c = key[2]
+            if not unit_loaded(s, ("W1", c), loaded) or not passed(pcs, ("n2w", s)):
+                return False
+            return done(comp, ("PV", s, H - 1)) if c == 0 else passed(pcs, ("gread", s, c - 1))
+        if kind == "F2":  # GP written by every warp; R holds t 2^s2 (phase 1 done)
+            c = key[2]
+            return unit_loaded(s, ("W2", c), loaded) and passed(pcs, ("gpw", s, c)) and passed(pcs, ("n2w", s))
+        raise AssertionError(key)
+
+    def hazard_free(kind, arg, pcs, comp, loaded):
+        if kind == "issue":
+            return issue_ok(arg, pcs, comp, loaded)
+        if kind == "done":
+            return done(comp, arg)
+        if kind == "ring_load":
+            return arg < 2 or done(comp, unit_mma[arg - 2])
+        if kind == "nr_write":  # N over N2 of the previous tile-layer (FFN-in done reading it)
+            s = arg
+            return s == 0 or all(done(comp, ("F1", s - 1, c)) for c in range(nch))
+        if kind == "sk_write":  # the K tiles: the previous S products done, the output stages written
+            s = arg
+            if s > 0 and not all(done(comp, ("S", s - 1, h)) for h in range(H)):
+                return False
+            i = s // layers
+            return s % layers or i == 0 or passed(pcs, ("stw", i - 1))
+        if kind == "sv_write":
+            s = arg
+            return s == 0 or all(done(comp, ("PV", s - 1, h)) for h in range(H))
+        if kind == "q_write":  # Q over N, which the k, v, q products have read
+            return done(comp, ("Q", arg))
+        if kind == "read_s":
+            s, h = arg
+            return done(comp, ("S", s, h)) and (h + 1 >= H or not issued(pcs, ("S", s, h + 1)))
+        if kind == "p_write":  # P over S columns other warps read
+            s, h = arg
+            return passed(pcs, ("sread", s, h))
+        if kind == "n2_write":  # N2 over Q and O / l: the S products and o_proj have read them
+            s = arg
+            return done(comp, ("OP", s)) and all(done(comp, ("S", s, h)) for h in range(H))
+        if kind == "read_g":
+            s, c = arg
+            return done(comp, ("F1", s, c)) and (c + 1 >= nch or not issued(pcs, ("F1", s, c + 1)))
+        if kind == "gp_write":  # GP over each head's O (read by every warp) or the previous GP
+            s, c = arg
+            k = s * nch + c
+            prev = (s, c - 1) if c > 0 else (s - 1, nch - 1)
+            if k > 0 and not done(comp, ("F2",) + prev):
+                return False
+            return c > 0 or passed(pcs, ("ow", s))
+        if kind == "stage_write":  # the output stages over the K tiles
+            i = arg
+            s = i * layers + layers - 1
+            return all(done(comp, ("S", s, h)) for h in range(H))
+        if kind == "red_write":
+            return arg < 2 or passed(pcs, ("red_read", arg - 2))
+        raise AssertionError(kind)
+
+    return run_model(progs, bars, key_bar, ["mma1", "mma2"], hazard_free)
+
+
+@pytest.mark.parametrize("seqs,layers,nch,warps", [(1, 2, 1, 1), (2, 1, 2, 1), (1, 2, 2, 2), (2, 2, 1, 1)])
+def test_stack_protocol_has_no_deadlock_aliasing_or_hazard(seqs, layers, nch, warps):
+    assert explore_stack(seqs, layers, nch, warps) > 100
+
+
+@pytest.mark.parametrize("mutation,seqs,layers,nch,warps", [
+    ("q_before_k_read", 1, 1, 1, 1),       # q overwrites k before every warp drained it
+    ("no_named_barrier", 1, 1, 1, 2),      # P over S columns another warp has not read
+    ("s_before_q_ready", 1, 1, 1, 1),      # S computed before q is in tensor memory
+    ("ffn1_skips_acc_read", 1, 1, 1, 1),   # FFN-in before N2 is written
+    ("o_without_pv_done", 1, 1, 1, 1),     # O read before P V completed
+])
+def test_the_stack_model_catches_a_planted_mistake(mutation, seqs, layers, nch, warps):
+    with pytest.raises(AssertionError):
+        explore_stack(seqs, layers, nch, warps, mutation)
